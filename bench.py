@@ -1,0 +1,349 @@
+"""Benchmark of the paged-KV attention hot path on one GB300 (or N replicas).
+
+A step is one decode step of one attention layer on the Qwen3-0.6B-shaped
+workload (batch 64, 16 q / 8 kv heads, head_dim 128, block_size 256,
+context_lens ~ U{1..4096}, pool sized for all sequences + 20 %, random block
+permutation, bf16 N(0,1)):
+  1. slot mapping of each sequence's newest token (address translation),
+  2. store_kvcache of the 64 new K/V rows,
+  3. split-KV GQA decode attention over all context tokens.
+All inputs are resident in HBM before the timed region; L2 is flushed (a
+256 MiB write) before every timed step.  The printed `value` is decode
+tokens/s (one layer) over all ranks; `e2e` is the same metric through the
+public API with the step's inputs copied from pinned host memory and the
+output copied back inside the timed region.  The decode kernel's own CUDA-
+event time gives the HBM roofline fraction.  The CPU oracle, timed on the
+host cores on a bounded sample, is reported as `cpu_baseline`.
+
+`--impl reference` runs the CPU oracle (the only reference this path has) on
+the same workload and prints its own line.
+
+Multi-GPU (torchrun): every rank serves its own batch of 64 sequences with
+its own pool (replicas, weak scaling); no collective is on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn tokens/s and HBM GB/s vs GB300 peak; prefill TFLOP/s"
+WORKLOAD = ("qwen3-0.6b decode step, 1 layer: batch 64, 16 q / 8 kv heads, head_dim 128, block_size 256, "
+            "context_lens ~ U[1,4096], pool = 1.2x blocks needed, random block permutation, "
+            "slot mapping + store_kvcache + split-KV decode")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, 1900.0, "fallback"
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+DECODE_SOURCES = ["paged_kv_cache_store_gb300/csrc/pa_decode.cu", "paged_kv_cache_store_gb300/csrc/pa_internal.cuh"]
+
+
+def recorded_traffic(kernel: str, workload_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(kernel, {}).get(workload_key)
+    if not rec or rec.get("source_digest") != source_digest(DECODE_SOURCES):
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv") \
+            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/pa_clocks_{os.getpid()}.csv"
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for ln in f:
+                c = [x.strip() for x in ln.split(",")]
+                if len(c) < 9:
+                    continue
+                try:
+                    sm.append(float(c[1]))
+                    mx.append(float(c[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, c[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def time_oracle_step(inp, O, budget_s: float):
+    """Runs the oracle's step (slot mapping, store, decode) on the workload for
+    about budget_s seconds; returns (tokens/s, steps)."""
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        kc, vc = inp.k_cache.copy(), inp.v_cache.copy()
+        slots = np.array([O.decode_slot(inp.block_tables[b], inp.block_size, int(inp.context_lens[b]))
+                          for b in range(inp.batch)], np.int32)
+        O.store_kvcache(inp.new_k, inp.new_v, kc, vc, slots)
+        O.decode(inp.q, kc, vc, inp.block_tables, inp.context_lens, inp.scale)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return steps * inp.batch / el, steps, el
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle as O
+    from paged_kv_cache_store_gb300.workloads import decode_config
+    inp = decode_config(2)
+    O.lib()
+    for _ in range(args.warmup):
+        time_oracle_step(inp, O, 0.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time_oracle_step(inp, O, 0.0)
+    el = time.perf_counter() - t0
+    value = args.steps * inp.batch / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16)",
+            "config": {"workload": WORKLOAD, "global_batch": inp.batch, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"full workload, {args.steps} steps"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl")
+    import paged_kv_cache_store_gb300 as pa
+    from paged_kv_cache_store_gb300.workloads import decode_config
+
+    dev = torch.device("cuda", local)
+    inp = decode_config(2)
+
+    def to_dev(a, dt):
+        if dt == torch.bfloat16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    kc, vc = to_dev(inp.k_cache, torch.bfloat16), to_dev(inp.v_cache, torch.bfloat16)
+    q = to_dev(inp.q, torch.bfloat16)
+    nk, nv = to_dev(inp.new_k, torch.bfloat16), to_dev(inp.new_v, torch.bfloat16)
+    bt, ctx = to_dev(inp.block_tables, torch.int32), to_dev(inp.context_lens, torch.int32)
+    slots = torch.empty(inp.batch, dtype=torch.int32, device=dev)
+    out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
+    wsp = pa.decode_workspace(inp.batch, inp.num_q_heads, inp.num_kv_heads, inp.head_dim, 0,
+                              inp.max_blocks, inp.block_size, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    L2 = "flushed (256 MiB write) before every timed step; KV pool 621 MiB > L2"
+
+    def step():
+        pa.slot_mapping_decode(bt, ctx, inp.block_size, out=slots)
+        pa.store_kvcache(nk, nv, kc, vc, slots)
+        pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    code, where = pa.get_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} at {where}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            e = ev[i]
+            e[0].record(stream)
+            pa.slot_mapping_decode(bt, ctx, inp.block_size, out=slots)
+            e[1].record(stream)
+            pa.store_kvcache(nk, nv, kc, vc, slots)
+            e[2].record(stream)
+            pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out)
+            e[3].record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    store_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = sum(step_ms)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * inp.batch * args.steps / (total_ms / 1000.0)
+
+    # End to end through the public API: host inputs -> device, step, output -> host.
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_q = pin(inp.q.view(np.int16)).view(torch.bfloat16)
+    h_nk, h_nv = pin(inp.new_k.view(np.int16)).view(torch.bfloat16), pin(inp.new_v.view(np.int16)).view(torch.bfloat16)
+    h_bt, h_ctx = pin(inp.block_tables), pin(inp.context_lens)
+    h_out = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_nk, h_nv, h_bt, h_ctx))
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps + 2):
+        if i >= 2:
+            flush.zero_()
+            e2e_ev[i - 2][0].record(stream)
+        q.copy_(h_q, non_blocking=True)
+        nk.copy_(h_nk, non_blocking=True)
+        nv.copy_(h_nv, non_blocking=True)
+        bt.copy_(h_bt, non_blocking=True)
+        ctx.copy_(h_ctx, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        if i >= 2:
+            e2e_ev[i - 2][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e_value = ws * inp.batch * args.steps / (float(t.item()) / 1000.0)
+
+    code, where = pa.get_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} at {where}")
+
+    if rank == 0:
+        hbm, _, peak_kind = peaks()
+        kv_bytes = int(inp.context_lens.astype(np.int64).sum()) * inp.num_kv_heads * inp.head_dim * 2 * 2
+        qo_bytes = 2 * inp.batch * inp.num_q_heads * inp.head_dim * 2
+        alg_bytes = kv_bytes + qo_bytes
+        dec_avg = sum(dec_ms) / len(dec_ms)
+        achieved = alg_bytes / (dec_avg / 1000.0) / 1e9
+        traffic = recorded_traffic("decode_kernel", "qwen3-0.6b")
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
+            "data": "synthetic (seeded N(0,1) bf16, random block tables)",
+            "config": {"workload": WORKLOAD, "global_batch": inp.batch * ws, "seq_len": "U[1,4096]",
+                       "parallelism": f"replicas x{ws}", "l2": L2},
+            "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": hbm,
+                         "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
+                         "frac_of_nominal_8TBps": achieved / 8000.0, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": alg_bytes, "decode_ms": dec_avg,
+                         "store_ms": sum(store_ms) / len(store_ms)},
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline:
+            import oracle as O
+            O.lib()
+            tps, steps, el = time_oracle_step(inp, O, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"{steps} full steps of the same workload ({el:.1f} s, 1 thread)"}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,249 @@
+/*
+ * pa.h -- C ABI of the paged-KV attention library (libpa.so), sm_103a.
+ *
+ * Three operations make up the path, in the order one model layer calls them
+ * on a stream: pa_store_kvcache writes this step's new K/V rows into the
+ * block pool, then pa_decode (one query token per sequence) or
+ * pa_prefill_varlen (many query tokens per sequence, causal) reads K/V back
+ * through the block tables.  Two helpers, pa_slot_mapping_decode and
+ * pa_slot_mapping_prefill, build the slot_mapping the store consumes.
+ *
+ * Sources (web pages that define the operations):
+ *   [NV12] "12. 推理加速(二):nano-vllm — 1200 行手写 vLLM" (chuoer47.github.io),
+ *          §12.6 "Attention 层: Paged KV Cache", §12.7 "ModelRunner".
+ *   [NV05] kyonqi.github.io "nano-vllm/05", ModelRunner: prepare_prefill,
+ *          prepare_decode, prepare_block_tables, run_model.
+ *   [VD]   "vLLM 深度解读" (luoboask.github.io), §3 "PagedAttention CUDA Kernel".
+ *   [PA3]  "Nano-vLLM 源码解读 - 3. PagedAttention" (yeyulingfeng.com),
+ *          §3 two-level mapping, §4 slot_mapping, §5 block size.
+ *
+ * Conventions shared by every entry point
+ *   - Element type: bf16 for q, k, v, caches and outputs (passed as void*).
+ *   - KV pool: one layer's k_cache and v_cache are each a contiguous
+ *     [num_blocks, block_size, num_kv_heads, head_dim] array; slot s is the
+ *     row k_cache + s*num_kv_heads*head_dim ([NV12 §12.7 allocate_kv_cache];
+ *     [PA3 §3]).  The physical slot of logical position p of a sequence is
+ *     block_table[p / block_size] * block_size + p % block_size.
+ *   - block_tables: int32 [batch, max_blocks_per_seq], row-major; entries
+ *     past a sequence's ceil(len/block_size) blocks are never read and may be
+ *     -1 ([NV05 prepare_block_tables]).
+ *   - head_dim must be 128 and num_q_heads a multiple of num_kv_heads with
+ *     num_q_heads/num_kv_heads in {1, 2, 4, 8}; query head h reads kv head
+ *     h / (num_q_heads/num_kv_heads).  Other shapes return PA_ERR_UNSUPPORTED.
+ *   - block_size must be a positive multiple of 16 (256 is the tuned case).
+ *   - Pointers are device pointers unless stated.  Base pointers of bf16
+ *     arrays must be 16-byte aligned and row strides multiples of 8 elements.
+ *   - Ownership: the caller owns every buffer and the stream.  No entry point
+ *     allocates or frees device memory, and none synchronises the stream
+ *     except pa_get_device_error.  Work is enqueued on `stream` in call order,
+ *     so a store followed by an attention call on the same stream is ordered.
+ *   - Errors: host-side argument checks return a status before anything is
+ *     enqueued; pa_last_error_message() gives the detail (thread-local).  A
+ *     launch failure returns PA_ERR_CUDA.  Problems only visible on the device
+ *     (an out-of-range slot or block id, a context longer than its table, a
+ *     wait that timed out) never fault: the kernel skips the access, records
+ *     the first one in a device error word and carries on; read it with
+ *     pa_get_device_error.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, bad stride */
+    PA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim != 128, ...) */
+    PA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    PA_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
+    PA_ERR_DEVICE_CHECK = 5   /* a kernel recorded a device-side error */
+} pa_status;
+
+/* Device-side error codes reported by pa_get_device_error. */
+enum {
+    PA_DEV_OK = 0,
+    PA_DEV_TIMEOUT = 1,        /* a bounded wait gave up; where = kernel id */
+    PA_DEV_BAD_SLOT = 2,       /* store: slot >= num_slots; where = token index */
+    PA_DEV_BAD_CONTEXT = 3,    /* context length < 0 or > max_blocks_per_seq*block_size;
+                                  where = sequence index */
+    PA_DEV_BAD_BLOCK = 4,      /* checked mode: block id outside [0, num_blocks);
+                                  where = sequence*max_blocks_per_seq + logical block */
+    PA_DEV_BAD_SEQLENS = 5     /* prefill: cu_seqlens not monotone or Lq > Lk;
+                                  where = sequence index */
+};
+
+/* Library version (major*10000 + minor*100 + patch). */
+PA_API int pa_version(void);
+
+/* Static string for a status code. */
+PA_API const char *pa_status_str(pa_status status);
+
+/* Detail of the last non-OK status returned on the calling thread ("" if none). */
+PA_API const char *pa_last_error_message(void);
+
+/*
+ * pa_store_kvcache -- scatter this step's K/V rows into the pool.
+ * [NV12 §12.6 store_kvcache / store_kvcache_kernel; PA3 §4]
+ *
+ * For each token i in [0, num_tokens) with slot = slot_mapping[i] >= 0:
+ *   k_cache[slot*Hkv*D + j] = key[i*key_row_stride + j]   for j < Hkv*D,
+ * and the same for value -> v_cache.  Negative slots are padding (CUDA-graph
+ * batches are padded with -1) and write nothing.  A slot >= num_slots is not
+ * written and is recorded as PA_DEV_BAD_SLOT.
+ *
+ *   key, value           bf16 [num_tokens, *]: token i's Hkv*D values start at
+ *                        key + i*key_row_stride (elements) and are contiguous
+ *                        ([Hkv, D] row-major), so fused-QKV views are allowed.
+ *   key_row_stride,
+ *   value_row_stride     elements between tokens; >= Hkv*D, multiple of 8.
+ *   k_cache, v_cache     bf16 pools [num_slots / block_size, block_size, Hkv, D].
+ *   slot_mapping         int32 [num_tokens]; non-negative entries must be distinct.
+ *   num_slots            num_blocks * block_size (bounds check only).
+ * Copies are bit-exact.  num_tokens == 0 is a no-op.
+ */
+PA_API pa_status pa_store_kvcache(const void *key, int64_t key_row_stride, const void *value,
+                           int64_t value_row_stride, void *k_cache, void *v_cache,
+                           const int32_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                           int32_t head_dim, int64_t num_slots, pa_stream_t stream);
+
+/*
+ * pa_slot_mapping_decode -- slot of each sequence's newest token.
+ * [PA3 §4 "Decode 路径"; NV05 prepare_decode]
+ *
+ * slot_mapping[b] = block_tables[b][(ctx-1)/B]*B + (ctx-1)%B with
+ * ctx = context_lens[b], i.e. last block * B + tokens in last block - 1;
+ * context_lens[b] == 0 (a padded row) gives -1.
+ *   slot_mapping   int32 [batch] (output, device).
+ */
+PA_API pa_status pa_slot_mapping_decode(int32_t *slot_mapping, const int32_t *block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                 int32_t batch, int32_t block_size, pa_stream_t stream);
+
+/*
+ * pa_slot_mapping_prefill -- slots of the uncached suffix of every sequence.
+ * [PA3 §4 "Prefill 路径"; NV12 §12.7 prepare_prefill]
+ *
+ * Sequence s computes positions [c, Lk) with Lk = cu_seqlens_k[s+1] -
+ * cu_seqlens_k[s], Lq = cu_seqlens_q[s+1] - cu_seqlens_q[s], c = Lk - Lq (c
+ * may sit mid-block: chunked prefill).  Query row cu_seqlens_q[s] + i gets
+ * the slot of position c + i.
+ *   slot_mapping   int32 [total_q] (output, device), total_q = cu_seqlens_q[num_seqs].
+ */
+PA_API pa_status pa_slot_mapping_prefill(int32_t *slot_mapping, const int32_t *block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t *cu_seqlens_q,
+                                  const int32_t *cu_seqlens_k, int32_t num_seqs, int32_t total_q,
+                                  int32_t block_size, pa_stream_t stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
+ * this shape when called with the same max_context_len (<= 0: derived from
+ * max_blocks_per_seq*block_size).
+ */
+PA_API size_t pa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t max_context_len,
+                                int32_t max_blocks_per_seq, int32_t block_size);
+
+/*
+ * pa_decode_workspace_init -- zero a workspace (cudaMemsetAsync on stream).
+ * The split-merge counters at its start must be zero before a workspace's
+ * first pa_decode call; every call that completes leaves them zero again.
+ * Re-initialise after a call that reported a device error.
+ */
+PA_API pa_status pa_decode_workspace_init(void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_decode -- paged split-KV GQA decode attention, one query per sequence.
+ * [NV12 §12.6 flash_attn_with_kvcache; VD §3 paged_attention_v1_kernel]
+ *
+ * For sequence b, query head h, kv head g = h / (Hq/Hkv), ctx = context_lens[b]:
+ *   s_p = softmax_scale * <q[b,h,:], K[slot(b,p), g, :]>   for p < ctx,
+ *   out[b,h,:] = sum_p softmax(s)_p * V[slot(b,p), g, :]    (bf16, RNE),
+ * where slot(b,p) = block_tables[b][p/B]*B + p%B.  The query is the token at
+ * position ctx-1 and sees all ctx keys, including its own (store it first).
+ * ctx == 0 writes zeros and reads nothing.  Long contexts are split across
+ * CTAs (online softmax per split, log-sum-exp merge of the partials).
+ *
+ *   out                bf16 [batch, Hq, D] contiguous.
+ *   q                  bf16; row b (Hq*D contiguous values) at q + b*q_row_stride.
+ *   k_cache, v_cache   the layer's pools (see conventions); num_blocks blocks.
+ *   block_tables       int32 [batch, max_blocks_per_seq].
+ *   context_lens       int32 [batch], each in [0, max_blocks_per_seq*block_size].
+ *   softmax_scale      usually 1/sqrt(head_dim).
+ *   max_context_len    an upper bound on context_lens (sizes the split count);
+ *                      <= 0 means max_blocks_per_seq*block_size.
+ *   workspace          device scratch of >= pa_decode_workspace_size(...)
+ *                      bytes, zeroed once (pa_decode_workspace_init).  One
+ *                      workspace must not be used by two calls that may run
+ *                      at the same time.
+ * batch == 0 is a no-op; batch <= 4096.
+ */
+PA_API pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *k_cache,
+                    const void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *context_lens, int32_t batch, int32_t num_q_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                    float softmax_scale, int32_t max_context_len, void *workspace,
+                    size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_prefill_varlen -- varlen causal attention for prompt (prefill) tokens.
+ * [NV12 §12.6 flash_attn_varlen_func and its cu_seqlens example; NV05 prepare_prefill]
+ *
+ * Sequence s owns query rows [cu_seqlens_q[s], cu_seqlens_q[s+1]) (Lq rows)
+ * and Lk = cu_seqlens_k[s+1] - cu_seqlens_k[s] >= Lq keys; the first
+ * c = Lk - Lq keys were cached earlier (prefix-cache hits).  Query i sits at
+ * position c + i and, with causal != 0, sees keys 0..c+i (bottom-right
+ * alignment); with causal == 0 it sees all Lk keys.  Sequences never
+ * interact.
+ *   out            bf16 [total_q, Hq, D] contiguous.
+ *   q              bf16; row t at q + t*q_row_stride, Hq*D contiguous values.
+ *   k, v           block_tables != NULL: the layer's caches (keys of sequence s
+ *                  at slot(s, j)); the suffix must already be stored.
+ *                  block_tables == NULL: contiguous rows, key j of sequence s
+ *                  at k + (cu_seqlens_k[s] + j)*kv_row_stride, Hkv*D values.
+ *   kv_row_stride  elements between rows in the contiguous case (ignored otherwise).
+ *   max_seqlen_q, max_seqlen_k  upper bounds of Lq and Lk (size the grid).
+ *   num_blocks     pool size in blocks (paged case; bounds TMA reads).
+ */
+PA_API pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_stride, const void *k,
+                            const void *v, int64_t kv_row_stride, const int32_t *block_tables,
+                            int32_t max_blocks_per_seq, const int32_t *cu_seqlens_q,
+                            const int32_t *cu_seqlens_k, int32_t num_seqs, int32_t max_seqlen_q,
+                            int32_t max_seqlen_k, int32_t num_q_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                            float softmax_scale, int32_t causal, pa_stream_t stream);
+
+/*
+ * pa_set_checked -- enable (1) or disable (0) extra device checks for calls
+ * made after it on any thread: block ids outside [0, num_blocks) are then
+ * recorded as PA_DEV_BAD_BLOCK (reads of them return zeros either way).
+ */
+PA_API pa_status pa_set_checked(int32_t enabled);
+
+/*
+ * pa_get_device_error -- synchronise `stream`, return the first device-side
+ * error recorded on the current device since the last call (code 0 if none)
+ * and clear it.  Returns PA_ERR_DEVICE_CHECK if an error was recorded.
+ * code and where may be NULL.
+ */
+PA_API pa_status pa_get_device_error(pa_stream_t stream, int32_t *code, int64_t *where);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

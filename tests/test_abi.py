@@ -1,0 +1,113 @@
+"""The C ABI library loads and exports every symbol include/pa.h declares;
+host-side argument checks reject bad calls before anything reaches a GPU.
+CPU only: no call here launches a kernel."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_store_gb300 as pa
+from paged_kv_cache_store_gb300 import build as pabuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    pabuild.build()
+    return pa.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER, encoding="utf-8").read()
+    return sorted(set(re.findall(r"PA_API\s+[\w\s\*]*?\b(pa_\w+)\s*\(", text)))
+
+
+def test_header_symbols_are_exported(L):
+    names = declared_symbols()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in pa.h but not exported"
+    assert set(names) == set(pa.SIGNATURES), "binding signatures and header disagree"
+
+
+def test_only_api_symbols_exported():
+    out = os.popen(f"nm -D --defined-only {pa.LIB_PATH}").read()
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert exported == set(declared_symbols())
+
+
+def test_status_strings(L):
+    assert L.pa_status_str(0) == b"PA_OK"
+    assert L.pa_status_str(3) == b"PA_ERR_WORKSPACE"
+    assert L.pa_status_str(99) == b"PA_ERR_UNKNOWN"
+    assert L.pa_version() >= 10000
+
+
+def test_workspace_size_host_math(L):
+    # Short contexts: one chunk per sequence still reserves counters + partials for 1 split.
+    small = L.pa_decode_workspace_size(4, 16, 8, 128, 256, 1, 256)
+    assert small > 0
+    # 64 sequences, 16 q heads, 8 kv heads, up to 4096 tokens in 256-token chunks: 16 splits.
+    n = L.pa_decode_workspace_size(64, 16, 8, 128, 4096, 16, 256)
+    assert n >= 64 * 16 * 16 * (128 * 4 + 8)
+    # Unsupported head_dim gives 0.
+    assert L.pa_decode_workspace_size(64, 16, 8, 64, 4096, 16, 256) == 0
+    # A very long context caps the number of splits (chunks grow instead).
+    big = L.pa_decode_workspace_size(1, 8, 8, 128, 1 << 20, 4096, 256)
+    assert big <= 1 * 8 * 512 * (128 * 4 + 8) + 4096
+
+
+def _msg(L):
+    return L.pa_last_error_message().decode()
+
+
+def test_store_argument_checks(L):
+    p = C.c_void_p(16)
+    assert L.pa_store_kvcache(None, 1024, p, 1024, p, p, p, 4, 8, 128, 1024, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_store_kvcache(p, 1024, p, 1024, p, p, p, 4, 8, 64, 1024, None) == pa.PA_ERR_UNSUPPORTED
+    assert L.pa_store_kvcache(p, 1020, p, 1024, p, p, p, 4, 8, 128, 1 << 20, None) == pa.PA_ERR_INVALID_ARG
+    assert "stride" in _msg(L)
+    assert L.pa_store_kvcache(p, 1028, p, 1028, p, p, p, 4, 8, 128, 1 << 20, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_store_kvcache(C.c_void_p(18), 1024, p, 1024, p, p, p, 4, 8, 128, 1 << 20, None) == \
+        pa.PA_ERR_INVALID_ARG
+    assert "aligned" in _msg(L)
+    assert L.pa_store_kvcache(p, 1024, p, 1024, p, p, p, 0, 8, 128, 1024, None) == pa.PA_OK  # no-op
+
+
+def _decode(L, **kw):
+    p = C.c_void_p(256)
+    a = dict(out=p, q=p, q_row_stride=2048, k=p, v=p, bt=p, mb=16, ctx=p, batch=4, hq=16, hkv=8, d=128,
+             B=256, nb=64, scale=0.088, maxctx=0, ws=p, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return L.pa_decode(a["out"], a["q"], a["q_row_stride"], a["k"], a["v"], a["bt"], a["mb"], a["ctx"],
+                       a["batch"], a["hq"], a["hkv"], a["d"], a["B"], a["nb"], a["scale"], a["maxctx"],
+                       a["ws"], a["wsb"], a["stream"])
+
+
+def test_decode_argument_checks(L):
+    assert _decode(L, batch=0) == pa.PA_OK
+    assert _decode(L, q=None) == pa.PA_ERR_INVALID_ARG
+    assert _decode(L, hq=12, hkv=8) == pa.PA_ERR_INVALID_ARG
+    assert _decode(L, hq=24, hkv=8) == pa.PA_ERR_UNSUPPORTED     # group of 3
+    assert _decode(L, d=64) == pa.PA_ERR_UNSUPPORTED
+    assert _decode(L, B=24) == pa.PA_ERR_UNSUPPORTED
+    assert _decode(L, q_row_stride=2047) == pa.PA_ERR_INVALID_ARG
+    assert _decode(L, q_row_stride=1024) == pa.PA_ERR_INVALID_ARG
+    assert _decode(L, scale=0.0) == pa.PA_ERR_INVALID_ARG
+    assert _decode(L, batch=5000) == pa.PA_ERR_UNSUPPORTED
+    assert _decode(L, ws=None, wsb=0) == pa.PA_ERR_WORKSPACE
+    assert _decode(L, wsb=100) == pa.PA_ERR_WORKSPACE
+    assert "workspace" in _msg(L)
+    assert _decode(L, k=C.c_void_p(258)) == pa.PA_ERR_INVALID_ARG
+    assert _decode(L, nb=1 << 24) == pa.PA_ERR_UNSUPPORTED       # slots overflow int32
+
+
+def test_slot_mapping_argument_checks(L):
+    p = C.c_void_p(256)
+    assert L.pa_slot_mapping_decode(p, p, 4, p, 0, 256, None) == pa.PA_OK
+    assert L.pa_slot_mapping_decode(None, p, 4, p, 3, 256, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_slot_mapping_decode(p, p, 4, p, 3, 0, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_slot_mapping_prefill(p, p, 4, p, p, 2, 0, 256, None) == pa.PA_OK
+    assert L.pa_slot_mapping_prefill(p, p, 4, p, p, -1, 3, 256, None) == pa.PA_ERR_INVALID_ARG

@@ -1,0 +1,161 @@
+"""GPU parity: pa_decode (after pa_store_kvcache of the decoded token)
+against the float64 oracle, max-abs <= 2e-2 and mean-abs <= 2e-3 on bf16
+outputs.  Small odd shapes span several tiles, chunks and ragged tails; the
+four decode workloads run at full size in the launch configuration the
+benchmark times."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import paged_kv_cache_store_gb300 as pa
+from paged_kv_cache_store_gb300.workloads import decode_config, make_decode
+from gpu_util import assert_close, dev_bf16, dev_i32, host_bits, host_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu_step(inp, max_context_len=0):
+    """store the decoded token's K/V at its slot, then decode; returns (out, caches)."""
+    kc, vc = dev_bf16(inp.k_cache), dev_bf16(inp.v_cache)
+    bt, ctx = dev_i32(inp.block_tables), dev_i32(inp.context_lens)
+    slots = pa.slot_mapping_decode(bt, ctx, inp.block_size)
+    pa.store_kvcache(dev_bf16(inp.new_k), dev_bf16(inp.new_v), kc, vc, slots)
+    out = pa.decode(dev_bf16(inp.q), kc, vc, bt, ctx, inp.scale, max_context_len=max_context_len)
+    code, where = pa.get_device_error()
+    assert code == 0, (code, where)
+    return out, kc, vc
+
+
+def run_oracle_step(inp, rows=None):
+    kc, vc = inp.k_cache.copy(), inp.v_cache.copy()
+    slots = np.array([O.decode_slot(inp.block_tables[b], inp.block_size, int(inp.context_lens[b]))
+                      for b in range(inp.batch)], np.int32)
+    O.store_kvcache(inp.new_k, inp.new_v, kc, vc, slots)
+    return O.decode(inp.q, kc, vc, inp.block_tables, inp.context_lens, inp.scale, rows=rows), kc, vc
+
+
+EDGE_CTX = [1, 2, 15, 16, 17, 63, 64, 65, 255, 256, 257, 511, 512, 513, 1000, 1537]
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8), (8, 8), (64, 8)])
+def test_decode_edge_lengths(hq, hkv):
+    inp = make_decode(f"edge {hq}/{hkv}", 100 + hq, len(EDGE_CTX), hq, hkv, EDGE_CTX)
+    out, kc, vc = run_gpu_step(inp)
+    want, okc, ovc = run_oracle_step(inp)
+    assert np.array_equal(host_bits(kc), okc)
+    assert_close(host_f64(out), want, f"decode {hq}/{hkv}")
+
+
+@pytest.mark.parametrize("B", [16, 32, 48, 64, 128, 256, 512])
+def test_decode_block_sizes(B):
+    ctx = [1, B - 1, B, B + 1, 3 * B + 7, 700]
+    inp = make_decode(f"B={B}", 200 + B, len(ctx), 32, 8, ctx, block_size=B)
+    out, _, _ = run_gpu_step(inp)
+    want, _, _ = run_oracle_step(inp)
+    assert_close(host_f64(out), want, f"block_size {B}")
+
+
+def test_decode_zero_context_rows_and_padded_tables():
+    ctx = [0, 300, 0, 1, 4097]
+    inp = make_decode("zero rows", 7, len(ctx), 16, 8, [max(c, 1) for c in ctx], extra_table_cols=3)
+    inp.context_lens[:] = ctx
+    inp.block_tables[[0, 2], :] = -1
+    kc, vc = dev_bf16(inp.k_cache), dev_bf16(inp.v_cache)
+    out = torch.full((len(ctx), 16, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    pa.decode(dev_bf16(inp.q), kc, vc, dev_i32(inp.block_tables), dev_i32(inp.context_lens), inp.scale, out=out)
+    assert pa.get_device_error() == (0, 0)
+    want = O.decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale)
+    got = host_f64(out)
+    assert np.all(got[[0, 2]] == 0.0)
+    assert_close(got, want, "zero rows")
+
+
+def test_decode_shared_prefix_blocks():
+    ctx = [1025, 1300, 2048, 4000, 1100, 600]
+    inp = make_decode("shared", 8, len(ctx), 32, 8, ctx, shared_prefix_seqs=4, shared_prefix_blocks=4)
+    out, _, _ = run_gpu_step(inp)
+    want, _, _ = run_oracle_step(inp)
+    assert_close(host_f64(out), want, "shared prefix")
+
+
+def test_decode_strided_q_rows():
+    ctx = [100, 2000, 3]
+    inp = make_decode("strided q", 9, 3, 16, 8, ctx)
+    qkv = torch.zeros(3, (16 + 16) * 128, dtype=torch.bfloat16, device="cuda")
+    qkv[:, :16 * 128] = dev_bf16(inp.q).view(3, -1)
+    q = qkv[:, :16 * 128].view(3, 16, 128)
+    out = pa.decode(q, dev_bf16(inp.k_cache), dev_bf16(inp.v_cache), dev_i32(inp.block_tables),
+                    dev_i32(inp.context_lens), inp.scale)
+    want = O.decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale)
+    assert_close(host_f64(out), want, "strided q")
+
+
+def test_decode_split_count_does_not_change_result():
+    """One long sequence: splitting into 256-token chunks (merge of 40 partials)
+    and the same data in a batch where the hint forces the same chunks agree
+    with the unsplit oracle."""
+    ctx = [10000]
+    inp = make_decode("long", 10, 1, 32, 8, ctx)
+    out, _, _ = run_gpu_step(inp)
+    want, _, _ = run_oracle_step(inp)
+    assert_close(host_f64(out), want, "long")
+    out2, _, _ = run_gpu_step(inp, max_context_len=10000)
+    assert torch.equal(out, out2)
+
+
+def test_decode_repeated_calls_reuse_workspace():
+    """The split-merge counters reset themselves: many calls on one workspace."""
+    ctx = [3000, 5000, 257, 1]
+    inp = make_decode("repeat", 11, 4, 16, 8, ctx)
+    kc, vc = dev_bf16(inp.k_cache), dev_bf16(inp.v_cache)
+    q, bt, cl = dev_bf16(inp.q), dev_i32(inp.block_tables), dev_i32(inp.context_lens)
+    ws = pa.decode_workspace(4, 16, 8, 128, 0, inp.max_blocks, 256)
+    outs = [pa.decode(q, kc, vc, bt, cl, inp.scale, workspace=ws) for _ in range(5)]
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    want = O.decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale)
+    assert_close(host_f64(outs[0]), want, "repeat")
+
+
+def test_decode_bad_context_is_recorded():
+    inp = make_decode("bad ctx", 12, 2, 16, 8, [10, 10])
+    cl = inp.context_lens.copy()
+    cl[1] = inp.max_blocks * inp.block_size + 1
+    pa.get_device_error()
+    pa.decode(dev_bf16(inp.q), dev_bf16(inp.k_cache), dev_bf16(inp.v_cache), dev_i32(inp.block_tables),
+              dev_i32(cl), inp.scale)
+    code, where = pa.get_device_error()
+    assert code == pa.PA_DEV_BAD_CONTEXT and where == 1
+
+
+def test_decode_checked_mode_records_bad_block():
+    inp = make_decode("bad block", 13, 2, 16, 8, [300, 10])
+    bt = inp.block_tables.copy()
+    bt[0, 1] = inp.num_blocks + 3
+    pa.get_device_error()
+    pa.set_checked(True)
+    try:
+        out = pa.decode(dev_bf16(inp.q), dev_bf16(inp.k_cache), dev_bf16(inp.v_cache), dev_i32(bt),
+                        dev_i32(inp.context_lens), inp.scale)
+        code, where = pa.get_device_error()
+    finally:
+        pa.set_checked(False)
+    assert code == pa.PA_DEV_BAD_BLOCK and where == 1
+    # Sequence 1 is unaffected.
+    want = O.decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale)
+    assert_close(host_f64(out)[1], want[1], "unaffected row")
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+def test_decode_workloads_full_size(cfg):
+    """The four decode workloads at full size (store + decode, the benchmark's
+    step), every output row against the oracle."""
+    inp = decode_config(cfg)
+    out, kc, vc = run_gpu_step(inp)
+    want, okc, ovc = run_oracle_step(inp)
+    # The store touched exactly the decoded tokens' slots.
+    assert np.array_equal(host_bits(kc), okc) and np.array_equal(host_bits(vc), ovc)
+    assert_close(host_f64(out), want, f"workload {cfg}")
