@@ -159,14 +159,6 @@ PA_API size_t pa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32
                                 int32_t max_blocks_per_seq, int32_t block_size);
 
 /*
- * pa_decode_workspace_init -- zero a workspace (cudaMemsetAsync on stream).
- * The split-merge counters at its start must be zero before a workspace's
- * first pa_decode call; every call that completes leaves them zero again.
- * Re-initialise after a call that reported a device error.
- */
-PA_API pa_status pa_decode_workspace_init(void *workspace, size_t workspace_bytes, pa_stream_t stream);
-
-/*
  * pa_decode -- paged split-KV GQA decode attention, one query per sequence.
  * [NV12 §12.6 flash_attn_with_kvcache; VD §3 paged_attention_v1_kernel]
  *
@@ -176,7 +168,8 @@ PA_API pa_status pa_decode_workspace_init(void *workspace, size_t workspace_byte
  * where slot(b,p) = block_tables[b][p/B]*B + p%B.  The query is the token at
  * position ctx-1 and sees all ctx keys, including its own (store it first).
  * ctx == 0 writes zeros and reads nothing.  Long contexts are split across
- * CTAs (online softmax per split, log-sum-exp merge of the partials).
+ * CTAs (online softmax per split); a second kernel on the same stream merges
+ * the partials (log-sum-exp).
  *
  *   out                bf16 [batch, Hq, D] contiguous.
  *   q                  bf16; row b (Hq*D contiguous values) at q + b*q_row_stride.
@@ -187,10 +180,11 @@ PA_API pa_status pa_decode_workspace_init(void *workspace, size_t workspace_byte
  *   max_context_len    an upper bound on context_lens (sizes the split count);
  *                      <= 0 means max_blocks_per_seq*block_size.
  *   workspace          device scratch of >= pa_decode_workspace_size(...)
- *                      bytes, zeroed once (pa_decode_workspace_init).  One
- *                      workspace must not be used by two calls that may run
- *                      at the same time.
- * batch == 0 is a no-op; batch <= 4096.
+ *                      bytes (fp32 split partials; no initialisation needed;
+ *                      may be NULL when that size is for a single split).
+ *                      One workspace must not be used by two calls that may
+ *                      run at the same time.
+ * batch == 0 is a no-op; batch <= 2048.
  */
 PA_API pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *k_cache,
                     const void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,

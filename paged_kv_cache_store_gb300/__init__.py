@@ -9,7 +9,7 @@ libpa.so has not been built (see build.py).
 
 Entry points (same names as the C ABI without the ``pa_`` prefix):
   store_kvcache, slot_mapping_decode, slot_mapping_prefill,
-  decode_workspace_size, decode_workspace_init, decode, prefill_varlen,
+  decode_workspace_size, decode, prefill_varlen,
   set_checked, get_device_error.
 """
 from __future__ import annotations
@@ -36,7 +36,6 @@ SIGNATURES = {
     "pa_slot_mapping_decode": (C.c_int, [_vp, _vp, _i32, _vp, _i32, _i32, _vp]),
     "pa_slot_mapping_prefill": (C.c_int, [_vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _vp]),
     "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
-    "pa_decode_workspace_init": (C.c_int, [_vp, _sz, _vp]),
     "pa_decode": (C.c_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                             _i32, _f32, _i32, _vp, _sz, _vp]),
     "pa_prefill_varlen": (C.c_int, [_vp, _vp, _i64, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i32,
@@ -164,15 +163,10 @@ def decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_contex
 
 def decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, max_context_len,
                      max_blocks_per_seq, block_size, device="cuda"):
-    """Allocate (with torch) and zero a workspace for pa_decode."""
+    """Allocate (with torch) a workspace for pa_decode."""
     n = decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_context_len,
                               max_blocks_per_seq, block_size)
-    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
-
-
-def decode_workspace_init(workspace, stream=None):
-    _check(lib().pa_decode_workspace_init(_ptr(workspace), workspace.numel(), _stream(stream)),
-           "pa_decode_workspace_init")
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, max_context_len=0,

@@ -107,7 +107,7 @@ def test_decode_split_count_does_not_change_result():
 
 
 def test_decode_repeated_calls_reuse_workspace():
-    """The split-merge counters reset themselves: many calls on one workspace."""
+    """Many calls on one (uninitialised) workspace give identical results."""
     ctx = [3000, 5000, 257, 1]
     inp = make_decode("repeat", 11, 4, 16, 8, ctx)
     kc, vc = dev_bf16(inp.k_cache), dev_bf16(inp.v_cache)
