@@ -194,6 +194,33 @@ PA_API pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const
                     size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_decode_static -- pa_decode for callers that cannot allocate device memory.
+ * (An addition of this library: the source pages have no counterpart.)
+ *
+ * Same arguments and result as pa_decode, minus the workspace.  Some callers
+ * cannot call cudaMalloc or an allocating library: code running inside
+ * another framework's memory pool, plugins that must not touch the
+ * allocator, or hosts that forbid device allocation after start-up.  This
+ * entry point allocates nothing.  The split partials go to a 32 MiB scratch
+ * array compiled into the library; every GPU that loads the library holds
+ * those 32 MiB until the process exits.
+ *   - Shapes whose pa_decode_workspace_size(...) exceeds 32 MiB are rejected
+ *     with PA_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Nothing in it has to start at zero: every partial is written before it
+ *     is read within the same call.  Calls that may overlap on the GPU (other
+ *     streams, other threads) race on it and must be serialised by the caller.
+ */
+PA_API pa_status pa_decode_static(void *out, const void *q, int64_t q_row_stride, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t block_size, int32_t num_blocks, float softmax_scale,
+                                  int32_t max_context_len, pa_stream_t stream);
+
+/*
  * pa_prefill_varlen -- varlen causal attention for prompt (prefill) tokens.
  * [NV12 §12.6 flash_attn_varlen_func and its cu_seqlens example; NV05 prepare_prefill]
  *

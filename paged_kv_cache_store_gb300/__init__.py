@@ -9,7 +9,7 @@ libpa.so has not been built (see build.py).
 
 Entry points (same names as the C ABI without the ``pa_`` prefix):
   store_kvcache, slot_mapping_decode, slot_mapping_prefill,
-  decode_workspace_size, decode, prefill_varlen,
+  decode_workspace_size, decode, decode_static, prefill_varlen,
   set_checked, get_device_error.
 """
 from __future__ import annotations
@@ -38,6 +38,8 @@ SIGNATURES = {
     "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
     "pa_decode": (C.c_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                             _i32, _f32, _i32, _vp, _sz, _vp]),
+    "pa_decode_static": (C.c_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                   _i32, _f32, _i32, _vp]),
     "pa_prefill_varlen": (C.c_int, [_vp, _vp, _i64, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i32,
                                     _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp]),
     "pa_set_checked": (C.c_int, [_i32]),
@@ -195,6 +197,30 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, 
                            float(softmax_scale), int(max_context_len), _ptr(workspace),
                            workspace.numel(), _stream(stream)),
            "pa_decode")
+    return out
+
+
+def decode_static(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, max_context_len=0,
+                  out=None, stream=None):
+    """pa_decode without a workspace: for callers that must not allocate device
+    memory.  The split scratch is a 32 MiB array built into the library (shared
+    by all calls, so calls that may overlap on the GPU must be serialised).
+    Only `out` is allocated here, and only when the caller passes none."""
+    _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    batch, hq, d = q.shape
+    nb, B, hkv, _ = k_cache.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(batch, hq, d, dtype=torch.bfloat16, device=q.device)
+    _check(lib().pa_decode_static(_ptr(out), _ptr(q), _row_stride(q, "q"), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), batch, hq, hkv,
+                                  d, B, nb, float(softmax_scale), int(max_context_len), _stream(stream)),
+           "pa_decode_static")
     return out
 
 

@@ -32,6 +32,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "pa_internal.cuh"
 
@@ -734,3 +735,59 @@ pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// pa_decode_static: decode attention for callers that cannot allocate device
+// memory.  The split partials live in a fixed scratch array that is part of
+// this library's device image instead of a caller-provided workspace.
+// ---------------------------------------------------------------------------
+
+// 32 MiB of split-partial scratch.  It is loaded with the module, so every GPU
+// that loads this library holds it until the process exits.
+static constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char pa_static_scratch[kStaticScratchBytes];
+
+namespace {
+std::mutex g_static_mu;
+void *g_static_scratch_addr[64] = {};  // device address of the array, per device
+}  // namespace
+
+extern "C" pa_status pa_decode_static(void *out, const void *q, int64_t q_row_stride, const void *k_cache,
+                                      const void *v_cache, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
+                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int32_t num_blocks, float softmax_scale,
+                                      int32_t max_context_len, pa_stream_t stream) {
+    using namespace pa;
+    const size_t need = pa_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                                                 max_blocks_per_seq, block_size);
+    if (need == 0)  // batch == 0 or arguments pa_decode rejects: let it report
+        return pa_decode(out, q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                         context_lens, batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                         softmax_scale, max_context_len, nullptr, 0, stream);
+    if (need > kStaticScratchBytes)
+        return fail(PA_ERR_WORKSPACE,
+                    "pa_decode_static: this shape needs %zu bytes of split scratch but the built-in scratch "
+                    "holds %zu; lower max_context_len/batch or call pa_decode with a workspace",
+                    need, kStaticScratchBytes);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    void *scratch = nullptr;
+    {
+        // Set-up, once per device, with that device current: the host-side name
+        // of the array is not a device address, so ask the runtime for it.
+        std::lock_guard<std::mutex> lk(g_static_mu);
+        if (g_static_scratch_addr[dev] == nullptr) {
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, pa_static_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(pa_static_scratch)");
+            g_static_scratch_addr[dev] = p;
+        }
+        scratch = g_static_scratch_addr[dev];
+    }
+    return pa_decode(out, q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                     batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, softmax_scale,
+                     max_context_len, scratch, kStaticScratchBytes, stream);
+}
