@@ -229,24 +229,28 @@ PA_API pa_status pa_decode_static(void *out, const void *q, int64_t q_row_stride
  * c = Lk - Lq keys were cached earlier (prefix-cache hits).  Query i sits at
  * position c + i and, with causal != 0, sees keys 0..c+i (bottom-right
  * alignment); with causal == 0 it sees all Lk keys.  Sequences never
- * interact.
+ * interact.  Tensor cores (tcgen05, bf16 in, fp32 accumulate) compute
+ * Q.K^T and P.V; the softmax runs in fp32 with P rounded to bf16.
  *   out            bf16 [total_q, Hq, D] contiguous.
  *   q              bf16; row t at q + t*q_row_stride, Hq*D contiguous values.
+ *   total_q        rows of q (= cu_seqlens_q[num_seqs]); bounds the q reads.
  *   k, v           block_tables != NULL: the layer's caches (keys of sequence s
  *                  at slot(s, j)); the suffix must already be stored.
  *                  block_tables == NULL: contiguous rows, key j of sequence s
  *                  at k + (cu_seqlens_k[s] + j)*kv_row_stride, Hkv*D values.
  *   kv_row_stride  elements between rows in the contiguous case (ignored otherwise).
- *   max_seqlen_q, max_seqlen_k  upper bounds of Lq and Lk (size the grid).
- *   num_blocks     pool size in blocks (paged case; bounds TMA reads).
+ *   total_k        rows of contiguous k/v (ignored when paged); bounds the reads.
+ *   max_seqlen_q   an upper bound of Lq (sizes the grid); max_seqlen_k of Lk.
+ *   num_blocks     pool size in blocks (paged case).
  */
-PA_API pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_stride, const void *k,
-                            const void *v, int64_t kv_row_stride, const int32_t *block_tables,
-                            int32_t max_blocks_per_seq, const int32_t *cu_seqlens_q,
-                            const int32_t *cu_seqlens_k, int32_t num_seqs, int32_t max_seqlen_q,
-                            int32_t max_seqlen_k, int32_t num_q_heads, int32_t num_kv_heads,
-                            int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                            float softmax_scale, int32_t causal, pa_stream_t stream);
+PA_API pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_stride, int32_t total_q,
+                                   const void *k, const void *v, int64_t kv_row_stride, int32_t total_k,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                   int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t num_blocks, float softmax_scale,
+                                   int32_t causal, pa_stream_t stream);
 
 /*
  * pa_set_checked -- enable (1) or disable (0) extra device checks for calls

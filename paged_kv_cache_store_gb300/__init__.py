@@ -40,8 +40,8 @@ SIGNATURES = {
                             _i32, _f32, _i32, _vp, _sz, _vp]),
     "pa_decode_static": (C.c_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                    _i32, _f32, _i32, _vp]),
-    "pa_prefill_varlen": (C.c_int, [_vp, _vp, _i64, _vp, _vp, _i64, _vp, _i32, _vp, _vp, _i32, _i32,
-                                    _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp]),
+    "pa_prefill_varlen": (C.c_int, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _i32, _vp, _i32, _vp, _vp, _i32,
+                                    _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp]),
     "pa_set_checked": (C.c_int, [_i32]),
     "pa_get_device_error": (C.c_int, [_vp, C.POINTER(_i32), C.POINTER(_i64)]),
 }
@@ -237,15 +237,15 @@ def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen
     if block_tables is not None:
         _need(block_tables, torch.int32, "block_tables")
         nb, B, hkv, _ = k.shape
-        mb, kv_stride = block_tables.shape[1], 0
+        mb, kv_stride, tk = block_tables.shape[1], 0, 0
     else:
-        _, hkv, _ = k.shape
+        tk, hkv, _ = k.shape
         nb, B, mb, kv_stride = 0, 16, 0, _row_stride(k, "k")
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty(tq, hq, d, dtype=torch.bfloat16, device=q.device)
-    _check(lib().pa_prefill_varlen(_ptr(out), _ptr(q), _row_stride(q, "q"), _ptr(k), _ptr(v), kv_stride,
+    _check(lib().pa_prefill_varlen(_ptr(out), _ptr(q), _row_stride(q, "q"), tq, _ptr(k), _ptr(v), kv_stride, tk,
                                    _ptr(block_tables), mb, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
                                    cu_seqlens_q.numel() - 1, int(max_seqlen_q), int(max_seqlen_k), hq, hkv,
                                    d, B, nb, float(softmax_scale), 1 if causal else 0, _stream(stream)),

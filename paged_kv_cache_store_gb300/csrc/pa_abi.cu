@@ -78,32 +78,42 @@ int sm_count() {
 
 bool checked_mode() { return g_checked.load(std::memory_order_relaxed) != 0; }
 
+static pa_status get_encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return PA_OK;
+}
+
+pa_status encode_tensor_map_3d(CUtensorMap *map, const void *base, int64_t dim0, int64_t dim1, int64_t dim2,
+                               int64_t stride1_bytes, int64_t stride2_bytes, int32_t box0, int32_t box2,
+                               bool swizzle128) {
+    pa_status st = get_encoder();
+    if (st != PA_OK) return st;
+    const cuuint64_t dims[3] = {(cuuint64_t)dim0, (cuuint64_t)dim1, (cuuint64_t)dim2};
+    const cuuint64_t strides[2] = {(cuuint64_t)stride1_bytes, (cuuint64_t)stride2_bytes};
+    const cuuint32_t box[3] = {(cuuint32_t)box0, 1u, (cuuint32_t)box2};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for dims %lld x %lld x %lld", (int)r,
+                    (long long)dim0, (long long)dim1, (long long)dim2);
+    return PA_OK;
+}
+
 pa_status encode_kv_tensor_map(CUtensorMap *map, const void *base, int64_t num_slots,
                                int32_t num_kv_heads, int32_t head_dim, int32_t box_rows) {
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (g_encode == nullptr) {
-            void *fn = nullptr;
-            cudaDriverEntryPointQueryResult q;
-            cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                             cudaEnableDefault, &q);
-            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
-                return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
-            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-        }
-    }
-    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)num_slots};
-    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_kv_heads * head_dim * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)head_dim, 1u, (cuuint32_t)box_rows};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-        return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %lld slots x %d heads",
-                    (int)r, (long long)num_slots, num_kv_heads);
-    return PA_OK;
+    return encode_tensor_map_3d(map, base, head_dim, num_kv_heads, num_slots, (int64_t)head_dim * 2,
+                                (int64_t)num_kv_heads * head_dim * 2, head_dim, box_rows, false);
 }
 
 }  // namespace pa
