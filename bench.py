@@ -187,6 +187,74 @@ def run_reference(args):
     return 0
 
 
+def prefill_pairs(p):
+    """Unmasked (query, key) pairs of the causal prefill: query i of a sequence
+    with c cached tokens sees c + i + 1 keys."""
+    tot = 0
+    for s in range(p.num_seqs):
+        c, lq = int(p.seqlens_k[s] - p.seqlens_q[s]), int(p.seqlens_q[s])
+        tot += lq * c + lq * (lq + 1) // 2
+    return tot
+
+
+def measure_prefill(args, dev, stream, flush, bf16_peak):
+    """The varlen prefill workload: slot mapping + store of the uncached suffix,
+    then causal prefill over the paged pool.  Returns a JSON-able dict."""
+    import torch
+    import paged_kv_cache_store_gb300 as pa
+    from paged_kv_cache_store_gb300.workloads import prefill_config
+
+    p = prefill_config(5)
+
+    def to_dev(a, bf=False):
+        if bf:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    kc, vc = to_dev(p.k_cache, True), to_dev(p.v_cache, True)
+    q, nk, nv = to_dev(p.q, True), to_dev(p.new_k, True), to_dev(p.new_v, True)
+    bt, cq, ck = to_dev(p.block_tables), to_dev(p.cu_seqlens_q), to_dev(p.cu_seqlens_k)
+    slots = torch.empty(p.total_q, dtype=torch.int32, device=dev)
+    out = torch.empty(p.total_q, p.num_q_heads, p.head_dim, dtype=torch.bfloat16, device=dev)
+    mq, mk = int(p.seqlens_q.max()), int(p.seqlens_k.max())
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        pa.slot_mapping_prefill(bt, cq, ck, p.block_size, total_q=p.total_q, out=slots)
+        pa.store_kvcache(nk, nv, kc, vc, slots)
+        if ev:
+            ev[1].record(stream)
+        pa.prefill_varlen(q, kc, vc, cq, ck, mq, mk, p.scale, block_tables=bt, out=out)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for e in evs:
+        flush.zero_()
+        step(e)
+    torch.cuda.synchronize()
+    code, where = pa.get_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} at {where}")
+    pre_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / len(evs)
+    store_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)
+    flops = 4 * p.head_dim * p.num_q_heads * prefill_pairs(p)
+    tflops = flops / (pre_ms / 1000.0) / 1e12
+    store_bytes = p.total_q * p.num_kv_heads * p.head_dim * 2 * 4
+    del kc, vc
+    return {"workload": "varlen causal prefill, 16 seqs, 32 q / 8 kv heads, Lk ~ U[128,2048], 0..3 cached "
+                        "blocks per seq, block_size 256 (suffix stored via slot_mapping first)",
+            "total_q": p.total_q, "ms_prefill": pre_ms, "ms_slotmap_store": store_ms,
+            "algorithmic_flops": flops,
+            "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": tflops, "peak": bf16_peak,
+                         "unit": "TFLOP/s", "frac": tflops / bf16_peak, "traffic": None},
+            "store_gbs": store_bytes / (store_ms / 1000.0) / 1e9}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -291,6 +359,11 @@ def run_ours(args):
     code, where = pa.get_device_error()
     if code:
         raise RuntimeError(f"device error {code} at {where}")
+    prefill = None
+    if not args.no_prefill:
+        del kc, vc
+        torch.cuda.empty_cache()
+        prefill = measure_prefill(args, dev, stream, flush, peaks()[1])
 
     if rank == 0:
         hbm, _, peak_kind = peaks()
@@ -313,8 +386,9 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": alg_bytes, "decode_ms": dec_avg,
                          "store_ms": sum(store_ms) / len(store_ms)},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": 4 * args.steps,
             "clocks": clk.summary(),
+            "prefill": prefill,
         }
         if not args.no_cpu_baseline:
             import oracle as O
@@ -337,6 +411,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

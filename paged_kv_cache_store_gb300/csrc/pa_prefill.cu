@@ -29,7 +29,7 @@
 
 #include <algorithm>
 
-#include "pa_internal.cuh"
+#include "pa_tcgen05.cuh"
 
 namespace pa {
 namespace {
