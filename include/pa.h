@@ -83,8 +83,10 @@ enum {
                                   where = sequence index */
     PA_DEV_BAD_BLOCK = 4,      /* checked mode: block id outside [0, num_blocks);
                                   where = sequence*max_blocks_per_seq + logical block */
-    PA_DEV_BAD_SEQLENS = 5     /* prefill: cu_seqlens not monotone or Lq > Lk;
+    PA_DEV_BAD_SEQLENS = 5,    /* prefill: cu_seqlens not monotone or Lq > Lk;
                                   where = sequence index */
+    PA_DEV_SMEM_ALIGN = 6      /* a kernel could not align its shared-memory tiles
+                                  (no work done); where = bytes of padding needed */
 };
 
 /* Library version (major*10000 + minor*100 + patch). */

@@ -24,7 +24,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpa.so")
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_DEVICE_CHECK = range(6)
-PA_DEV_TIMEOUT, PA_DEV_BAD_SLOT, PA_DEV_BAD_CONTEXT, PA_DEV_BAD_BLOCK, PA_DEV_BAD_SEQLENS = 1, 2, 3, 4, 5
+PA_DEV_TIMEOUT, PA_DEV_BAD_SLOT, PA_DEV_BAD_CONTEXT, PA_DEV_BAD_BLOCK, PA_DEV_BAD_SEQLENS, PA_DEV_SMEM_ALIGN = range(1, 7)
 
 # Every symbol include/pa.h declares, with its ctypes signature.
 _i32, _i64, _sz, _f32, _vp = C.c_int32, C.c_int64, C.c_size_t, C.c_float, C.c_void_p

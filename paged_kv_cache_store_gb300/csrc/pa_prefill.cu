@@ -6,9 +6,13 @@
 // all Lk keys when causal == 0), keys read through the block table
 // (prefix cache) or from contiguous rows.
 //
-// How (GB300 design): one CTA per (128-row query tile, sequence, q head).
-//  * warp 0 (one thread) issues TMA copies: the Q tile once, then K and V
-//    tiles of 128 keys into two-stage rings.  Boxes are {64 dims, 1 head,
+// How (GB300 design): persistent CTAs (one per SM) walk work tiles of
+// (128-row query tile, sequence, q head), highest query tiles first; all
+// roles follow one global KV-tile counter, so the next tile's Q/K/V copies
+// overlap the current tile's softmax and epilogue.
+//  * warps 0 and 10 (one thread each) issue TMA copies: warp 0 the Q tile
+//    and the K tiles of 128 keys, warp 10 the V tiles, into separate rings
+//    (Q: 2, K: 3, V: 2 stages) so neither stream waits behind the other.  Boxes are {64 dims, 1 head,
 //    R rows} with 128-byte swizzle (two boxes per 128-dim row); paged boxes
 //    never straddle a block (R = gcd(block_size, 128)).
 //  * warp 1 (one thread) owns the tensor cores: S = Q.K^T (M=N=128, K=128,
@@ -16,15 +20,17 @@
 //    O += P.V with V as an MN-major operand, O accumulating in TMEM.
 //    tcgen05.commit arrives on mbarriers to free K/V stages, publish S and
 //    release the P buffer.
-//  * warps 4..7 (one thread per query row = TMEM lane) read S rows with
-//    tcgen05.ld, apply scale and mask, keep the running max/sum in base 2,
-//    and write P as bf16 into a 128-byte-swizzled shared-memory tile for
-//    the P.V MMA.  O in TMEM is rescaled only when a row's max grows by
+//  * warps 2..9: two warps per TMEM lane quarter, one thread per query row
+//    and 64 of the 128 key columns each, read S with tcgen05.ld, apply scale
+//    and mask, share the row max through shared memory (an mbarrier per
+//    warp pair, double-buffered slots), keep running statistics in base 2, and write
+//    their half of P as bf16 pairs into TMEM, where the P.V MMA takes it as
+//    its A operand (only V is read from shared memory).  O in TMEM is rescaled only when a row's max grows by
 //    more than 2^8 (otherwise the stale max keeps P <= 256, exact enough in
 //    bf16 and fp32); the final 1/l is applied in the epilogue.
 //  * Every mbarrier wait is bounded; a timeout records PA_DEV_TIMEOUT and
 //    the roles skip to the CTA-wide teardown.
-// TMEM: S0 = columns 0..127, S1 = 128..255, O = 256..383 (512 allocated).
+// TMEM: S0 = columns 0..127, S1 = 128..255, O = 256..383, P0/P1 = 384..511.
 #include <math.h>
 
 #include <algorithm>
@@ -39,25 +45,39 @@ constexpr int BM = 128;                   // query rows per tile
 constexpr int BN = 128;                   // keys per tile
 constexpr int TILE_BYTES = BM * D * 2;    // 32 KiB
 constexpr int HALF_BYTES = TILE_BYTES / 2;  // [128 rows][64 dims], 128-byte rows
-constexpr int NTHREADS = 256;
-constexpr int W_TMA = 0, W_MMA = 1, W_SOFT = 4;  // softmax warps 4..7
+constexpr int NTHREADS = 352;
+constexpr int W_TMA = 0, W_MMA = 1, W_SOFT = 2, W_VTMA = 10;  // softmax warps 2..9
+// Softmax warp w reads TMEM lane quarter w % 4 (hardware rule) and key/dim
+// columns [64*h, 64*h + 64) with h = (w - 2) / 4: two warps share each row.
 
+constexpr int QST = 2;  // Q tiles (one per work tile in flight)
+constexpr int KST = 3;  // K ring stages (K is needed first: deepest prefetch)
+constexpr int VST = 2;  // V ring stages (V is needed after the softmax)
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE_BYTES;      // 2 stages
-constexpr int OFF_V = OFF_K + 2 * TILE_BYTES;  // 2 stages
-constexpr int OFF_P = OFF_V + 2 * TILE_BYTES;  // 2 buffers
-constexpr int OFF_BAR = OFF_P + 2 * TILE_BYTES;
-enum { B_Q = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 7, B_SFULL = 9, B_SFREE = 11,
-       B_PFULL = 13, B_PFREE = 15, NBAR = 17 };
+constexpr int OFF_K = OFF_Q + QST * TILE_BYTES;
+constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
+constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
+enum { B_Q = 0, B_QEMPTY = B_Q + QST, B_KFULL = B_QEMPTY + QST, B_KEMPTY = B_KFULL + KST, B_VFULL = B_KEMPTY + KST,
+       B_SFULL = B_VFULL + VST, B_PFULL = B_SFULL + 2, B_PFREE = B_PFULL + 2, B_OFREE = B_PFREE + 2,
+       B_XCH = B_OFREE + 1 /* [4 quarters][2 slots] */, NBAR = B_XCH + 8 };
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int OFF_FLAGS = OFF_TMEM + 8;
-constexpr size_t SMEM_BYTES = OFF_FLAGS + 16 + 1024;
+constexpr int OFF_XCH = OFF_FLAGS + 16;  // row-statistics exchange [4 quarters][2 slots][2 halves][32] f32
+constexpr int OFF_BID = OFF_XCH + 4 * 2 * 2 * 32 * 4;  // block ids of the current work tile, per producer
+constexpr int NBID = 32;
+constexpr int SMEM_USED = OFF_BID + 2 * NBID * 4;
+// Slack for aligning the dynamic shared-memory base to the 1 KiB the swizzled
+// tiles need (the base is normally aligned already; the kernel checks).
+constexpr int SMEM_SLACK = 256;
+constexpr size_t SMEM_BYTES = SMEM_USED + SMEM_SLACK;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(VST == 2, "V stages are released through the two P buffers' barriers");
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_O = 256;
+constexpr uint32_t COL_O = 256;  // O accumulator, 128 fp32 columns
+constexpr uint32_t COL_P = 384;  // two P buffers, 64 columns each (128 keys as bf16 pairs)
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
-constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, false, true);   // P K-major, V MN-major
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, false, true);   // P from TMEM, V MN-major
 constexpr uint32_t SBO = 1024;  // 8 rows x 128 B between core-matrix groups
 constexpr unsigned FULL = 0xffffffffu;
 
@@ -91,38 +111,80 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// Tile coordinates of work tile t: the highest query tiles (the most keys)
+// come first, then sequence, then q head (the heads of one kv group are
+// neighbours, so their K/V tiles are reused from L2).
+struct Tile {
+    int s, h, m0, q0, Lq, k0, Lk, n_kv, key_end, valid;
+};
+
+__device__ __forceinline__ Tile tile_of(const PrefillArgs &a, int t) {
+    Tile T;
+    const int per = a.num_seqs * a.Hq;
+    const int mt = a.mtiles - 1 - t / per;
+    const int rem = t % per;
+    T.s = rem / a.Hq;
+    T.h = rem % a.Hq;
+    T.m0 = mt * BM;
+    T.q0 = __ldg(a.cu_q + T.s);
+    T.Lq = __ldg(a.cu_q + T.s + 1) - T.q0;
+    T.k0 = __ldg(a.cu_k + T.s);
+    T.Lk = __ldg(a.cu_k + T.s + 1) - T.k0;
+    const bool bad = T.Lq < 0 || T.Lk < T.Lq || (a.paged && T.Lk > a.max_blocks * a.block_size);
+    T.valid = !bad && T.m0 < T.Lq;
+    if (bad && mt == 0 && T.h == 0 && threadIdx.x == 0) record_error(a.err, PA_DEV_BAD_SEQLENS, T.s);
+    T.key_end = 0;
+    T.n_kv = 0;
+    if (T.valid) {
+        const int c = T.Lk - T.Lq;
+        const int last_row = min(T.m0 + BM, T.Lq) - 1;
+        T.key_end = a.causal ? min(T.Lk, c + last_row + 1) : T.Lk;
+        T.n_kv = (T.key_end + BN - 1) / BN;
+    }
+    return T;
+}
+
+// First work tile >= t (stepping by gridDim.x) whose query rows exist.  The
+// warp tests 32 candidates per round of loads and takes the first by ballot,
+// so skipping the many empty high query tiles costs one load latency per 32.
+// Every lane must call it; every role gets the same answer.
+__device__ __forceinline__ int next_valid_tile(const PrefillArgs &a, int t, int ntiles, int lane) {
+    const int per = a.num_seqs * a.Hq;
+    for (int base = t; base < ntiles; base += 32 * (int)gridDim.x) {
+        const int tt = base + lane * (int)gridDim.x;
+        bool v = false;
+        if (tt < ntiles) {
+            const int mt = a.mtiles - 1 - tt / per;
+            const int s = (tt % per) / a.Hq;
+            v = mt * BM < __ldg(a.cu_q + s + 1) - __ldg(a.cu_q + s);
+        }
+        const unsigned m = __ballot_sync(FULL, v);
+        if (m) return base + (__ffs(m) - 1) * (int)gridDim.x;
+    }
+    return ntiles;
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+    if (pad > (uint32_t)SMEM_SLACK) {  // cannot align the tiles inside the allocation
+        if (threadIdx.x == 0) record_error(a.err, PA_DEV_SMEM_ALIGN, (long long)pad);
+        return;
+    }
+    uint8_t *smem = smem_raw + pad;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + OFF_FLAGS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // ---- which tile: the highest query tiles (the most keys) come first
-    const int per = a.num_seqs * a.Hq;
-    const int mt = a.mtiles - 1 - (int)(blockIdx.x / per);
-    const int rem = (int)(blockIdx.x % per);
-    const int s = rem / a.Hq, h = rem % a.Hq, kvh = h / a.group;
-    const int q0 = a.cu_q[s], Lq = a.cu_q[s + 1] - q0;
-    const int k0 = a.cu_k[s], Lk = a.cu_k[s + 1] - k0;
-    if (Lq < 0 || Lk < Lq || (a.paged && Lk > a.max_blocks * a.block_size)) {
-        if (threadIdx.x == 0 && mt == 0 && h == 0) record_error(a.err, PA_DEV_BAD_SEQLENS, s);
-        return;
-    }
-    const int m0 = mt * BM;
-    if (m0 >= Lq) return;  // the whole CTA leaves together
-    const int c = Lk - Lq;
-    const int last_row = min(m0 + BM, Lq) - 1;
-    const int key_end = a.causal ? min(Lk, c + last_row + 1) : Lk;  // keys [0, key_end) are needed
-    const int n_kv = (key_end + BN - 1) / BN;
+    const int ntiles = a.mtiles * a.num_seqs * a.Hq;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NBAR; ++i) {
             uint32_t cnt = 1;
-            if ((i >= B_SFREE && i < B_SFREE + 2) || (i >= B_PFULL && i < B_PFULL + 2)) cnt = 4;
+            if ((i >= B_PFULL && i < B_PFULL + 2) || i == B_OFREE) cnt = 8;
+            if (i >= B_XCH) cnt = 64;
             mbar_init(&bar[i], cnt);
         }
         flags[0] = 0;
@@ -137,232 +199,319 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == W_TMA) {
-        // ------------------------------------------------------------ TMA producer
+    // Every role walks the same tiles t = blockIdx.x, +gridDim.x, ... and the
+    // same global KV-tile counter g, so ring stages and barrier phases agree.
+    if (warp == W_TMA || warp == W_VTMA) {
+        // ------------------------------------------------------------ TMA producers
+        // Two independent streams: warp W_TMA loads Q and K, warp W_VTMA loads V,
+        // each as far ahead as its own ring allows (V is needed after the
+        // softmax, K before it, so neither waits behind the other).
+        const bool is_k = warp == W_TMA;
+        const CUtensorMap *tm = is_k ? &tmk : &tmv;
+        const int NS = is_k ? KST : VST;
+        const int off = is_k ? OFF_K : OFF_V;
+        uint64_t *full = &bar[is_k ? B_KFULL : B_VFULL];
+        // A V stage is free once the P.V that read it is complete: with as many V
+        // stages as P buffers, the P_FREE barrier of that P.V serves, and the
+        // producer waits on its phases in order.  The 3-stage K ring has its
+        // own release barriers (one phase per stage use).
+        int *bid = reinterpret_cast<int *>(smem + OFF_BID) + (is_k ? 0 : NBID);
         if (lane == 0) {
-            prefetch_tensormap(&tmq);
-            prefetch_tensormap(&tmk);
-            prefetch_tensormap(&tmv);
-            mbar_arrive_expect_tx(&bar[B_Q], TILE_BYTES);
-            tma_load_3d_plain(smem + OFF_Q, &tmq, 0, h, q0 + m0, &bar[B_Q]);
-            tma_load_3d_plain(smem + OFF_Q + HALF_BYTES, &tmq, 64, h, q0 + m0, &bar[B_Q]);
-            const int R = a.box_rows;
-            const int32_t *bt = a.bt + (int64_t)s * a.max_blocks;
-            int issued = 0;  // K/V tiles whose copies were issued
-            for (int j = 0; j < n_kv; ++j) {
-                const int st = j & 1;
-                const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-                const int kb = j * BN;
-                const int nsub = (min(BN, key_end - kb) + R - 1) / R;
-                const uint32_t bytes = (uint32_t)nsub * R * D * 2;
-                int rows[BN / 16];
-                for (int sub = 0; sub < nsub; ++sub) {
-                    const int key = kb + sub * R;
-                    if (a.paged) {
-                        const int blk = __ldg(bt + key / a.block_size);
-                        if (a.checked && (blk < 0 || blk >= a.num_blocks))
-                            record_error(a.err, PA_DEV_BAD_BLOCK, (long long)s * a.max_blocks + key / a.block_size);
-                        // An invalid block id reads as zeros: TMA fills out-of-range boxes.
-                        rows[sub] = (blk < 0 || blk >= a.num_blocks) ? -2 * R : blk * a.block_size + key % a.block_size;
-                    } else {
-                        rows[sub] = k0 + key;
+            if (is_k) prefetch_tensormap(&tmq);
+            prefetch_tensormap(tm);
+        }
+        const int R = a.box_rows;
+        uint32_t g = 0, tk = 0;  // KV tiles and Q tiles issued by this warp
+        bool ok = true;
+        for (int t = next_valid_tile(a, blockIdx.x, ntiles, lane); ok && t < ntiles;
+             t = next_valid_tile(a, t + gridDim.x, ntiles, lane)) {
+            const Tile T = tile_of(a, t);
+            const int32_t *bt = a.bt + (int64_t)T.s * a.max_blocks;
+            if (T.valid && a.paged) {
+                // The warp fetches the tile's first NBID block ids at once.
+                const int nblk = min((T.key_end - 1) / a.block_size + 1, NBID);
+                for (int b = lane; b < nblk; b += 32) bid[b] = __ldg(bt + b);
+            }
+            __syncwarp();
+            if (lane == 0 && T.valid) {
+                const int kvh = T.h / a.group;
+                if (is_k) {
+                    const uint32_t qs = tk % QST;
+                    ok = wait_or_abort(&bar[B_QEMPTY + qs], ((tk / QST) & 1u) ^ 1u, flags, a.err, 400);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&bar[B_Q + qs], TILE_BYTES);
+                        uint8_t *qd = smem + OFF_Q + qs * TILE_BYTES;
+                        tma_load_3d_plain(qd, &tmq, 0, T.h, T.q0 + T.m0, &bar[B_Q + qs]);
+                        tma_load_3d_plain(qd + HALF_BYTES, &tmq, 64, T.h, T.q0 + T.m0, &bar[B_Q + qs]);
+                        ++tk;
                     }
                 }
-                if (!wait_or_abort(&bar[B_KEMPTY + st], ph ^ 1u, flags, a.err, 400)) break;
-                mbar_arrive_expect_tx(&bar[B_KFULL + st], bytes);
-                uint8_t *kd = smem + OFF_K + st * TILE_BYTES;
-                for (int sub = 0; sub < nsub; ++sub) {
-                    tma_load_3d_plain(kd + sub * R * 128, &tmk, 0, kvh, rows[sub], &bar[B_KFULL + st]);
-                    tma_load_3d_plain(kd + HALF_BYTES + sub * R * 128, &tmk, 64, kvh, rows[sub], &bar[B_KFULL + st]);
+                for (int j = 0; ok && j < T.n_kv; ++j, ++g) {
+                    const int st = g % NS;
+                    const int kb = j * BN;
+                    const int nsub = (min(BN, T.key_end - kb) + R - 1) / R;
+                    if (is_k) {
+                        if (!(ok = wait_or_abort(&bar[B_KEMPTY + st], ((g / KST) & 1u) ^ 1u, flags, a.err, 401))) break;
+                    } else if (g >= (uint32_t)VST) {  // the P.V of tile g - VST read this stage
+                        const uint32_t u = g - VST;
+                        if (!(ok = wait_or_abort(&bar[B_PFREE + (u & 1)], (u >> 1) & 1u, flags, a.err, 402))) break;
+                    }
+                    mbar_arrive_expect_tx(&full[st], (uint32_t)nsub * R * D * 2);
+                    uint8_t *dst = smem + off + st * TILE_BYTES;
+                    for (int sub = 0; sub < nsub; ++sub) {
+                        const int key = kb + sub * R;
+                        int row;
+                        if (a.paged) {
+                            const int lb = key / a.block_size;
+                            const int blk = lb < NBID ? bid[lb] : __ldg(bt + lb);
+                            if (a.checked && is_k && (blk < 0 || blk >= a.num_blocks))
+                                record_error(a.err, PA_DEV_BAD_BLOCK, (long long)T.s * a.max_blocks + lb);
+                            // An invalid block id reads as zeros: TMA fills out-of-range boxes.
+                            row = (blk < 0 || blk >= a.num_blocks) ? -2 * R : blk * a.block_size + key % a.block_size;
+                        } else {
+                            row = T.k0 + key;
+                        }
+                        tma_load_3d_plain(dst + sub * R * 128, tm, 0, kvh, row, &full[st]);
+                        tma_load_3d_plain(dst + HALF_BYTES + sub * R * 128, tm, 64, kvh, row, &full[st]);
+                    }
                 }
-                if (!wait_or_abort(&bar[B_VEMPTY + st], ph ^ 1u, flags, a.err, 401)) {
-                    issued = j + 1;  // K of tile j is in flight
-                    break;
-                }
-                mbar_arrive_expect_tx(&bar[B_VFULL + st], bytes);
-                uint8_t *vd = smem + OFF_V + st * TILE_BYTES;
-                for (int sub = 0; sub < nsub; ++sub) {
-                    tma_load_3d_plain(vd + sub * R * 128, &tmv, 0, kvh, rows[sub], &bar[B_VFULL + st]);
-                    tma_load_3d_plain(vd + HALF_BYTES + sub * R * 128, &tmv, 64, kvh, rows[sub], &bar[B_VFULL + st]);
-                }
-                issued = j + 1;
             }
-            if (flags[0]) {
-                // Let issued copies land before the CTA's shared memory is released.
-                (void)mbar_wait(&bar[B_Q], 0);
-                for (int j = max(0, issued - 2); j < issued; ++j) {
-                    (void)mbar_wait(&bar[B_KFULL + (j & 1)], (uint32_t)(j >> 1) & 1u);
-                    (void)mbar_wait(&bar[B_VFULL + (j & 1)], (uint32_t)(j >> 1) & 1u);
-                }
-            }
+            ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+        }
+        if (lane == 0 && !ok) {
+            // Let issued copies land before the CTA's shared memory is released.
+            for (uint32_t x = (tk >= QST ? tk - QST : 0); x < tk; ++x)
+                (void)mbar_wait(&bar[B_Q + x % QST], (x / QST) & 1u);
+            for (uint32_t x = (g >= (uint32_t)NS ? g - NS : 0); x < g; ++x) (void)mbar_wait(&full[x % NS], (x / NS) & 1u);
         }
     } else if (warp == W_MMA) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t q_addr = smem_addr(smem + OFF_Q);
-            int committed_pv = -1;
-            auto issue_pv = [&](int jj) -> bool {
-                const int pb = jj & 1;
-                const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
-                if (!wait_or_abort(&bar[B_PFULL + pb], ph, flags, a.err, 410)) return false;
-                if (!wait_or_abort(&bar[B_VFULL + pb], ph, flags, a.err, 411)) return false;
+        // The warp walks the tiles together; lane 0 waits and issues.
+        {
+            uint32_t g = 0, tk = 0;
+            int64_t last_pv = -1;  // global index of the last P.V issued
+            bool ok = true;
+            // O += P_gg V_gg; `first` overwrites O (first KV tile of a work tile).
+            auto issue_pv = [&](uint32_t gg, bool first) -> bool {
+                const int pb = gg & 1, vs = gg % VST;
+                if (first && tk > 1 &&
+                    !wait_or_abort(&bar[B_OFREE], (tk - 2) & 1u, flags, a.err, 410))  // previous epilogue read O
+                    return false;
+                // (The softmax publishes P only after V of the same tile has landed.)
+                if (!wait_or_abort(&bar[B_PFULL + pb], (gg >> 1) & 1u, flags, a.err, 411)) return false;
                 tc_fence_after();
-                const uint32_t p_addr = smem_addr(smem + OFF_P + pb * TILE_BYTES);
-                const uint32_t v_addr = smem_addr(smem + OFF_V + pb * TILE_BYTES);
+                // One descriptor per operand; each K=16 step only moves the start
+                // address (low 14 bits, in 16-byte units) by a constant.
+                const uint64_t vdesc = smem_desc_sw128(smem_addr(smem + OFF_V + vs * TILE_BYTES), HALF_BYTES, SBO);
+                const uint32_t pcol = tmem + COL_P + pb * 64;
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    const uint64_t ad = smem_desc_sw128(p_addr + (k >> 2) * HALF_BYTES + (k & 3) * 32, 16, SBO);
-                    const uint64_t bd = smem_desc_sw128(v_addr + k * 16 * 128, HALF_BYTES, SBO);
-                    mma_bf16_ss(tmem + COL_O, ad, bd, IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
-                }
+                for (int k = 0; k < BN / 16; ++k)  // 16 keys per step = 8 TMEM columns of P
+                    mma_bf16_ts(tmem + COL_O, pcol + k * 8, vdesc + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV,
+                                (!first || k > 0) ? 1u : 0u);
                 mma_commit(&bar[B_PFREE + pb]);
-                mma_commit(&bar[B_VEMPTY + pb]);
-                committed_pv = jj;
+                last_pv = gg;
                 return true;
             };
-            bool ok = wait_or_abort(&bar[B_Q], 0, flags, a.err, 412);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int st = j & 1;
-                const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-                ok = wait_or_abort(&bar[B_KFULL + st], ph, flags, a.err, 413);
-                if (ok && j >= 2) ok = wait_or_abort(&bar[B_SFREE + st], ph ^ 1u, flags, a.err, 414);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t k_addr = smem_addr(smem + OFF_K + st * TILE_BYTES);
+            // All MMAs of one work tile (lane 0 only); false on a timeout.
+            auto mma_tile = [&](const Tile &T) -> bool {
+                const uint32_t qs = tk % QST;
+                if (!wait_or_abort(&bar[B_Q + qs], (tk / QST) & 1u, flags, a.err, 413)) return false;
+                const uint64_t qdesc = smem_desc_sw128(smem_addr(smem + OFF_Q + qs * TILE_BYTES), 16, SBO);
+                ++tk;
+                for (int j = 0; j < T.n_kv; ++j, ++g) {
+                    const int st = g & 1, ks = g % KST;
+                    // (S buffer st is free: P of tile g-2 was published, so its S was read.)
+                    if (!wait_or_abort(&bar[B_KFULL + ks], (g / KST) & 1u, flags, a.err, 414)) return false;
+                    tc_fence_after();
+                    const uint64_t kdesc = smem_desc_sw128(smem_addr(smem + OFF_K + ks * TILE_BYTES), 16, SBO);
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint64_t ad = smem_desc_sw128(q_addr + (k >> 2) * HALF_BYTES + (k & 3) * 32, 16, SBO);
-                    const uint64_t bd = smem_desc_sw128(k_addr + (k >> 2) * HALF_BYTES + (k & 3) * 32, 16, SBO);
-                    mma_bf16_ss(tmem + st * BN, ad, bd, IDESC_S, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint64_t off = (uint64_t)(((k >> 2) * HALF_BYTES + (k & 3) * 32) >> 4);
+                        mma_bf16_ss(tmem + st * BN, qdesc + off, kdesc + off, IDESC_S, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bar[B_KEMPTY + ks]);
+                    mma_commit(&bar[B_SFULL + st]);
+                    if (j == T.n_kv - 1) mma_commit(&bar[B_QEMPTY + qs]);  // this Q tile may be reloaded
+                    if (j >= 1 && !issue_pv(g - 1, j == 1)) return false;
                 }
-                mma_commit(&bar[B_KEMPTY + st]);
-                mma_commit(&bar[B_SFULL + st]);
-                if (j >= 1) ok = issue_pv(j - 1);
+                return issue_pv(g - 1, T.n_kv == 1);
+            };
+            for (int t = next_valid_tile(a, blockIdx.x, ntiles, lane); ok && t < ntiles;
+                 t = next_valid_tile(a, t + gridDim.x, ntiles, lane)) {
+                if (lane == 0) {
+                    const Tile T = tile_of(a, t);
+                    if (T.valid) ok = mma_tile(T);
+                }
+                ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
             }
-            if (ok) ok = issue_pv(n_kv - 1);
-            if (!ok && committed_pv >= 0) {
+            if (lane == 0 && !ok && last_pv >= 0) {
                 // Let the issued MMAs finish before TMEM is released.
-                (void)mbar_wait(&bar[B_PFREE + (committed_pv & 1)], (uint32_t)(committed_pv >> 1) & 1u);
+                (void)mbar_wait(&bar[B_PFREE + (last_pv & 1)], (uint32_t)(last_pv >> 1) & 1u);
             }
         }
     } else if (warp >= W_SOFT) {
         // ------------------------------------------------------------ softmax
-        const int wq = warp - W_SOFT;
-        const int row = wq * 32 + lane;  // tile row == TMEM lane
-        const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-        const int i = m0 + row;          // query index in the sequence (>= Lq: padding row)
-        const int pos = c + i;
-        float m_run = -INFINITY, l_run = 0.f;
+        const int quarter = warp & 3, half = (warp - W_SOFT) >> 2;
+        const int row = quarter * 32 + lane;  // tile row == TMEM lane
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t col0 = half * 64;      // this warp's 64 key columns of S and dim columns of O
+        float *xch = reinterpret_cast<float *>(smem + OFF_XCH) + quarter * 128;  // [2 slots][2 halves][32]
+        const float sl = a.scale_log2;
+        uint32_t g = 0, xc = 0;  // KV tiles consumed; exchanges done with the partner warp
         bool ok = true;
-        for (int j = 0; ok && j < n_kv; ++j) {
-            const int sb = j & 1;
-            const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-            // Waits in this role are made warp-uniform: tcgen05.ld/st are warp-collective.
-            if (!(ok = __all_sync(FULL, wait_or_abort(&bar[B_SFULL + sb], ph, flags, a.err, 420)))) break;
-            tc_fence_after();
-            float x[BN];
-#pragma unroll
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(t_lane + sb * BN + cc * 32, r);
+        // Exchange one value per row with the partner warp (same rows, other
+        // half): slots alternate, so one bounded mbarrier wait per exchange.
+        auto exchange = [&](float v, float &partner) -> bool {
+            const uint32_t slot = xc & 1u;
+            float *x2 = xch + slot * 64;
+            x2[half * 32 + lane] = v;
+            mbar_arrive(&bar[B_XCH + quarter * 2 + slot]);
+            const bool done = __all_sync(FULL, wait_or_abort(&bar[B_XCH + quarter * 2 + slot], (xc >> 1) & 1u, flags,
+                                                              a.err, 425));
+            partner = x2[(half ^ 1) * 32 + lane];
+            ++xc;
+            return done;
+        };
+        for (int t = next_valid_tile(a, blockIdx.x, ntiles, lane); ok && t < ntiles;
+             t = next_valid_tile(a, t + gridDim.x, ntiles, lane)) {
+            const Tile T = tile_of(a, t);
+            if (!T.valid) continue;
+            const int i = T.m0 + row;          // query index in the sequence (>= Lq: padding row)
+            const int pos = (T.Lk - T.Lq) + i;
+            const int key_last = (a.causal ? min(pos, T.Lk - 1) : T.Lk - 1);  // last key this row sees
+            float m_run = -INFINITY;           // running max of raw scores (shared with the partner warp)
+            float l_run = 0.f;                 // this half's running sum
+            for (int j = 0; j < T.n_kv; ++j, ++g) {
+                const int sb = g & 1;
+                const uint32_t ph = (g >> 1) & 1u;
+                // Waits in this role are warp-uniform: tcgen05.ld/st are warp-collective.
+                if (!(ok = __all_sync(FULL, wait_or_abort(&bar[B_SFULL + sb], ph, flags, a.err, 420)))) break;
+                tc_fence_after();
+                // Each warp reads its 64 columns of the S row; the row max is
+                // shared with the partner warp (the other 64 columns).
+                uint32_t r[2][32];
+                tmem_ld32(t_lane + sb * BN + col0, r[0]);
+                tmem_ld32(t_lane + sb * BN + col0 + 32, r[1]);
                 tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[cc * 32 + e] = __uint_as_float(r[e]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[B_SFREE + sb]);
 
-            const int kb = j * BN;
-            const int lim = (a.causal ? min(pos, Lk - 1) : Lk - 1) - kb;  // keys kb+k with k <= lim
-            float tmax = -INFINITY;
+                const int kb = j * BN + col0;
+                const int lim = key_last - kb;  // this warp's keys kb+k with k <= lim are visible
+                float x[64];
 #pragma unroll
-            for (int k = 0; k < BN; ++k) {
-                x[k] = (k <= lim) ? x[k] * a.scale_log2 : -INFINITY;
-                tmax = fmaxf(tmax, x[k]);
-            }
-            const bool grow = tmax > m_run + 8.f;
-            const float m_new = grow ? tmax : m_run;
-            const float alpha = grow ? fast_exp2(m_run - m_new) : 1.f;
-            if (__any_sync(FULL, grow) && j > 0) {
-                // O holds sum_{j' < j} P_j' V_j': wait for the last P.V, then rescale.
-                const int pj = j - 1;
-                ok = __all_sync(FULL, wait_or_abort(&bar[B_PFREE + (pj & 1)], (uint32_t)(pj >> 1) & 1u, flags, a.err, 421));
-                if (ok) {
+                for (int e = 0; e < 32; ++e) {
+                    x[e] = __uint_as_float(r[0][e]);
+                    x[32 + e] = __uint_as_float(r[1][e]);
+                }
+                if (__any_sync(FULL, lim < 63)) {
+#pragma unroll
+                    for (int k = 0; k < 64; ++k)
+                        if (k > lim) x[k] = -INFINITY;
+                }
+                float mx[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mx[e] = x[e];
+#pragma unroll
+                for (int k = 8; k < 64; k += 8)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], x[k + e]);
+                float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                float tpart;
+                if (!(ok = exchange(tmax, tpart))) break;
+                tmax = fmaxf(tmax, tpart);
+                // Lazy rescaling: keep the old max unless this tile's max exceeds it
+                // by more than 8 in log2 units (P then stays <= 2^8).
+                const bool grow = (tmax - m_run) * sl > 8.f;
+                const float m_new = grow ? tmax : m_run;
+                const float alpha = grow ? fast_exp2((m_run - m_new) * sl) : 1.f;
+                if (__any_sync(FULL, grow) && j > 0) {
+                    // O holds the previous tiles' P.V: wait for the last one, then
+                    // rescale this warp's 64 columns of O.
+                    const uint32_t pg = g - 1;
+                    ok = __all_sync(FULL, wait_or_abort(&bar[B_PFREE + (pg & 1)], (pg >> 1) & 1u, flags, a.err, 421));
+                    if (!ok) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t r[32];
-                        tmem_ld32(t_lane + COL_O + cc * 32, r);
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld32(t_lane + COL_O + col0 + cc * 32, o);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                        tmem_st32(t_lane + COL_O + cc * 32, r);
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(t_lane + COL_O + col0 + cc * 32, o);
                     }
                     tmem_st_wait();
                 }
-            }
-            l_run *= alpha;
-            m_run = m_new;
-            const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-            if (ok && j >= 2) ok = __all_sync(FULL, wait_or_abort(&bar[B_PFREE + sb], ph ^ 1u, flags, a.err, 422));
-            if (ok) {
-                const uint32_t prow = smem_addr(smem + OFF_P + sb * TILE_BYTES) + row * 128;
-                float rs = 0.f;
+                l_run *= alpha;
+                m_run = m_new;
+                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run * sl;
+                if (g >= 2 && !(ok = __all_sync(FULL, wait_or_abort(&bar[B_PFREE + sb], ph ^ 1u, flags, a.err, 422))))
+                    break;
+                // This warp's 64 keys become 32 TMEM columns of bf16 pairs (the A
+                // operand of the P.V MMA), in this buffer's half `half`.
+                float rs[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[32];
 #pragma unroll
-                for (int kc = 0; kc < BN / 8; ++kc) {
-                    float p[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        p[e] = fast_exp2(x[kc * 8 + e] - m_use);
-                        rs += p[e];
-                    }
-                    const uint32_t addr = prow + (kc >> 3) * HALF_BYTES + (((kc & 7) ^ (row & 7)) << 4);
-                    st_shared_v4(addr, pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
-                                 pack_bf16(p[6], p[7]));
+                for (int k2 = 0; k2 < 32; ++k2) {
+                    const float p0 = fast_exp2(fmaf(x[2 * k2], sl, neg_m));
+                    const float p1 = fast_exp2(fmaf(x[2 * k2 + 1], sl, neg_m));
+                    rs[(2 * k2) & 3] += p0;
+                    rs[(2 * k2 + 1) & 3] += p1;
+                    pk[k2] = pack_bf16(p0, p1);
                 }
-                l_run += rs;
-                if (j == n_kv - 1 && key_end - kb < BN) {
+                tmem_st32(t_lane + COL_P + sb * 64 + half * 32, pk);
+                tmem_st_wait();
+                l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+                const int kend = T.key_end - j * BN;
+                const int vs = g % VST;
+                // V of this tile must have landed before P is published (the MMA
+                // thread then issues P.V without its own wait).
+                if (!(ok = __all_sync(FULL, wait_or_abort(&bar[B_VFULL + vs], (g / VST) & 1u, flags, a.err, 423))))
+                    break;
+                if (j == T.n_kv - 1 && kend < BN) {
                     // Rows past the last needed key hold stale or unloaded data:
-                    // zero them so 0 * garbage cannot reach O.
-                    ok = __all_sync(FULL, wait_or_abort(&bar[B_VFULL + sb], ph, flags, a.err, 423));
-                    if (ok && row >= key_end - kb) {
-                        const uint32_t vrow = smem_addr(smem + OFF_V + sb * TILE_BYTES) + row * 128;
+                    // zero them (this warp: one 64-dim half) so 0 * garbage cannot reach O.
+                    if (row >= kend) {
+                        const uint32_t vrow = smem_addr(smem + OFF_V + vs * TILE_BYTES) + half * HALF_BYTES + row * 128;
 #pragma unroll
-                        for (int q16 = 0; q16 < 8; ++q16) {
-                            st_shared_v4(vrow + q16 * 16, 0, 0, 0, 0);
-                            st_shared_v4(vrow + HALF_BYTES + q16 * 16, 0, 0, 0, 0);
-                        }
+                        for (int q16 = 0; q16 < 8; ++q16) st_shared_v4(vrow + q16 * 16, 0, 0, 0, 0);
                     }
                 }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[B_PFULL + sb]);
             }
-            fence_proxy_async_smem();
+            if (!ok) break;
+            // ---- epilogue: O / l -> bf16; this warp writes its 64 dims of each row
+            const uint32_t pg = g - 1;
+            if (!(ok = __all_sync(FULL, wait_or_abort(&bar[B_PFREE + (pg & 1)], (pg >> 1) & 1u, flags, a.err, 424))))
+                break;
+            tc_fence_after();
+            uint32_t o[2][32];
+            tmem_ld32(t_lane + COL_O + col0, o[0]);
+            tmem_ld32(t_lane + COL_O + col0 + 32, o[1]);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[B_PFULL + sb]);
-        }
-        // ---- epilogue: O / l -> bf16 rows of this tile that exist
-        const int pj = n_kv - 1;
-        if (ok) ok = __all_sync(FULL, wait_or_abort(&bar[B_PFREE + (pj & 1)], (uint32_t)(pj >> 1) & 1u, flags, a.err, 424));
-        if (__all_sync(FULL, ok)) {
-            tc_fence_after();
-            const float inv = 1.f / l_run;
-            const bool valid = i < Lq;
-            __nv_bfloat16 *orow = a.out + ((int64_t)(q0 + i) * a.Hq + h) * D;
+            if (lane == 0) mbar_arrive(&bar[B_OFREE]);  // O may be overwritten by the next tile
+            float lpart;
+            if (!(ok = exchange(l_run, lpart))) break;
+            const float l_tot = l_run + lpart;
+            if (i < T.Lq) {
+                const float inv = 1.f / l_tot;
+                uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((int64_t)(T.q0 + i) * a.Hq + T.h) * D + col0);
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(t_lane + COL_O + cc * 32, r);
-                tmem_ld_wait();
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+                for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_uint4(pack_bf16(__uint_as_float(r[8 * e + 0]) * inv, __uint_as_float(r[8 * e + 1]) * inv),
-                                            pack_bf16(__uint_as_float(r[8 * e + 2]) * inv, __uint_as_float(r[8 * e + 3]) * inv),
-                                            pack_bf16(__uint_as_float(r[8 * e + 4]) * inv, __uint_as_float(r[8 * e + 5]) * inv),
-                                            pack_bf16(__uint_as_float(r[8 * e + 6]) * inv, __uint_as_float(r[8 * e + 7]) * inv));
-                }
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t *v = &o[cc][8 * e];
+                        dst[cc * 4 + e] = make_uint4(
+                            pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                            pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                            pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                            pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+                    }
             }
         }
     }
@@ -447,8 +596,11 @@ extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_s
     A.scale_log2 = softmax_scale * 1.4426950408889634f;
     A.err = device_error_ptr();
 
-    const int64_t grid = (int64_t)A.mtiles * num_seqs * num_q_heads;
-    if (grid > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "grid too large");
+    const int64_t ntiles = (int64_t)A.mtiles * num_seqs * num_q_heads;
+    if (ntiles > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "too many tiles");
+    const int sms = sm_count();
+    if (sms <= 0) return fail(PA_ERR_CUDA, "no CUDA device");
+    const int64_t grid = std::min<int64_t>(ntiles, sms);  // persistent: one CTA per SM
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !g_attr_done[dev]) {
