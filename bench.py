@@ -280,8 +280,7 @@ def run_ours(args):
     bt, ctx = to_dev(inp.block_tables, torch.int32), to_dev(inp.context_lens, torch.int32)
     slots = torch.empty(inp.batch, dtype=torch.int32, device=dev)
     out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
-    wsp = pa.decode_workspace(inp.batch, inp.num_q_heads, inp.num_kv_heads, inp.head_dim, 0,
-                              inp.max_blocks, inp.block_size, dev)
+    wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     L2 = "flushed (256 MiB write) before every timed step; KV pool 621 MiB > L2"

@@ -152,13 +152,11 @@ PA_API pa_status pa_slot_mapping_prefill(int32_t *slot_mapping, const int32_t *b
                                   int32_t block_size, pa_stream_t stream);
 
 /*
- * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
- * this shape when called with the same max_context_len (<= 0: derived from
- * max_blocks_per_seq*block_size).
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode needs.
+ * It depends only on the GQA group (num_q_heads / num_kv_heads) and is at
+ * most about 2.1 MB; 0 for shapes pa_decode does not support.
  */
-PA_API size_t pa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                                int32_t head_dim, int32_t max_context_len,
-                                int32_t max_blocks_per_seq, int32_t block_size);
+PA_API size_t pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim);
 
 /*
  * pa_decode -- paged split-KV GQA decode attention, one query per sequence.
@@ -169,9 +167,10 @@ PA_API size_t pa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32
  *   out[b,h,:] = sum_p softmax(s)_p * V[slot(b,p), g, :]    (bf16, RNE),
  * where slot(b,p) = block_tables[b][p/B]*B + p%B.  The query is the token at
  * position ctx-1 and sees all ctx keys, including its own (store it first).
- * ctx == 0 writes zeros and reads nothing.  Long contexts are split across
- * CTAs (online softmax per split); a second kernel on the same stream merges
- * the partials (log-sum-exp).
+ * ctx == 0 writes zeros and reads nothing.  The tiles of all (sequence, kv
+ * head) pairs are cut into equal contiguous ranges, one per CTA; a pair cut
+ * between CTAs is combined by a second kernel on the same stream
+ * (log-sum-exp of the per-CTA online-softmax partials).
  *
  *   out                bf16 [batch, Hq, D] contiguous.
  *   q                  bf16; row b (Hq*D contiguous values) at q + b*q_row_stride.
@@ -179,21 +178,18 @@ PA_API size_t pa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32
  *   block_tables       int32 [batch, max_blocks_per_seq].
  *   context_lens       int32 [batch], each in [0, max_blocks_per_seq*block_size].
  *   softmax_scale      usually 1/sqrt(head_dim).
- *   max_context_len    an upper bound on context_lens (sizes the split count);
- *                      <= 0 means max_blocks_per_seq*block_size.
  *   workspace          device scratch of >= pa_decode_workspace_size(...)
- *                      bytes (fp32 split partials; no initialisation needed;
- *                      may be NULL when that size is for a single split).
- *                      One workspace must not be used by two calls that may
- *                      run at the same time.
+ *                      bytes, 16-byte aligned (fp32 split partials and merge
+ *                      tasks; no initialisation needed).  One workspace must
+ *                      not be used by two calls that may run at the same time.
  * batch == 0 is a no-op; batch <= 2048.
  */
 PA_API pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *k_cache,
                     const void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
                     const int32_t *context_lens, int32_t batch, int32_t num_q_heads,
                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                    float softmax_scale, int32_t max_context_len, void *workspace,
-                    size_t workspace_bytes, pa_stream_t stream);
+                    float softmax_scale, void *workspace, size_t workspace_bytes,
+                    pa_stream_t stream);
 
 /*
  * pa_decode_static -- pa_decode for callers that cannot allocate device memory.
@@ -203,11 +199,10 @@ PA_API pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const
  * cannot call cudaMalloc or an allocating library: code running inside
  * another framework's memory pool, plugins that must not touch the
  * allocator, or hosts that forbid device allocation after start-up.  This
- * entry point allocates nothing.  The split partials go to a 32 MiB scratch
- * array compiled into the library; every GPU that loads the library holds
- * those 32 MiB until the process exits.
- *   - Shapes whose pa_decode_workspace_size(...) exceeds 32 MiB are rejected
- *     with PA_ERR_WORKSPACE before anything is enqueued.
+ * entry point allocates nothing.  The split partials go to a 4 MiB scratch
+ * array compiled into the library, which holds the workspace of every
+ * supported shape; every GPU that loads the library holds those 4 MiB until
+ * the process exits.
  *   - The first call on a device (with that device current) looks up the
  *     array's device address; make that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents.
@@ -220,7 +215,7 @@ PA_API pa_status pa_decode_static(void *out, const void *q, int64_t q_row_stride
                                   int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t block_size, int32_t num_blocks, float softmax_scale,
-                                  int32_t max_context_len, pa_stream_t stream);
+                                  pa_stream_t stream);
 
 /*
  * pa_prefill_varlen -- varlen causal attention for prompt (prefill) tokens.

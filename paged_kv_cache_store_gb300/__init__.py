@@ -35,11 +35,11 @@ SIGNATURES = {
     "pa_store_kvcache": (C.c_int, [_vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp]),
     "pa_slot_mapping_decode": (C.c_int, [_vp, _vp, _i32, _vp, _i32, _i32, _vp]),
     "pa_slot_mapping_prefill": (C.c_int, [_vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _vp]),
-    "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32]),
     "pa_decode": (C.c_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
-                            _i32, _f32, _i32, _vp, _sz, _vp]),
+                            _i32, _f32, _vp, _sz, _vp]),
     "pa_decode_static": (C.c_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
-                                   _i32, _f32, _i32, _vp]),
+                                   _i32, _f32, _vp]),
     "pa_prefill_varlen": (C.c_int, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _i32, _vp, _i32, _vp, _vp, _i32,
                                     _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp]),
     "pa_set_checked": (C.c_int, [_i32]),
@@ -157,22 +157,19 @@ def slot_mapping_prefill(block_tables, cu_seqlens_q, cu_seqlens_k, block_size, t
     return out
 
 
-def decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_context_len,
-                          max_blocks_per_seq, block_size) -> int:
-    return int(lib().pa_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
-                                              max_context_len, max_blocks_per_seq, block_size))
+def decode_workspace_size(num_q_heads, num_kv_heads, head_dim) -> int:
+    return int(lib().pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim))
 
 
-def decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, max_context_len,
-                     max_blocks_per_seq, block_size, device="cuda"):
-    """Allocate (with torch) a workspace for pa_decode."""
-    n = decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_context_len,
-                              max_blocks_per_seq, block_size)
+def decode_workspace(num_q_heads, num_kv_heads, head_dim, device="cuda"):
+    """Allocate (with torch) a workspace for pa_decode (about 2 MB at most;
+    it depends only on the GQA group)."""
+    n = decode_workspace_size(num_q_heads, num_kv_heads, head_dim)
     return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
 
 
-def decode(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, max_context_len=0,
-           workspace=None, out=None, stream=None):
+def decode(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, workspace=None, out=None,
+           stream=None):
     """Paged decode attention.  q [batch, Hq, D] bf16 (rows may be strided);
     caches [num_blocks, B, Hkv, D]; block_tables int32 [batch, max_blocks];
     context_lens int32 [batch].  Returns out [batch, Hq, D] bf16."""
@@ -189,21 +186,19 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, 
         softmax_scale = 1.0 / math.sqrt(d)
     mb = block_tables.shape[1]
     if workspace is None:
-        workspace = decode_workspace(batch, hq, hkv, d, max_context_len, mb, B, q.device)
+        workspace = decode_workspace(hq, hkv, d, q.device)
     if out is None:
         out = torch.empty(batch, hq, d, dtype=torch.bfloat16, device=q.device)
     _check(lib().pa_decode(_ptr(out), _ptr(q), _row_stride(q, "q"), _ptr(k_cache), _ptr(v_cache),
                            _ptr(block_tables), mb, _ptr(context_lens), batch, hq, hkv, d, B, nb,
-                           float(softmax_scale), int(max_context_len), _ptr(workspace),
-                           workspace.numel(), _stream(stream)),
+                           float(softmax_scale), _ptr(workspace), workspace.numel(), _stream(stream)),
            "pa_decode")
     return out
 
 
-def decode_static(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, max_context_len=0,
-                  out=None, stream=None):
+def decode_static(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, out=None, stream=None):
     """pa_decode without a workspace: for callers that must not allocate device
-    memory.  The split scratch is a 32 MiB array built into the library (shared
+    memory.  The split scratch is a 4 MiB array built into the library (shared
     by all calls, so calls that may overlap on the GPU must be serialised).
     Only `out` is allocated here, and only when the caller passes none."""
     _need(q, torch.bfloat16, "q")
@@ -219,7 +214,7 @@ def decode_static(q, k_cache, v_cache, block_tables, context_lens, softmax_scale
         out = torch.empty(batch, hq, d, dtype=torch.bfloat16, device=q.device)
     _check(lib().pa_decode_static(_ptr(out), _ptr(q), _row_stride(q, "q"), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), batch, hq, hkv,
-                                  d, B, nb, float(softmax_scale), int(max_context_len), _stream(stream)),
+                                  d, B, nb, float(softmax_scale), _stream(stream)),
            "pa_decode_static")
     return out
 

@@ -6,29 +6,32 @@
 // p < context_lens[b], slot(b,p) = block_tables[b][p/B]*B + p%B [PA3 §3].
 //
 // How (GB300 design):
-//  * Work items are (sequence, kv head, chunk of `chunk_tokens` positions).
-//    Every CTA rebuilds the per-sequence chunk prefix sum from context_lens
-//    in shared memory and walks items blockIdx.x, +gridDim.x, ... (a
-//    persistent grid of one CTA per SM).  Items of the 8 kv heads of one
-//    chunk are adjacent, so neighbouring CTAs stream the same 2 KiB token
-//    rows at the same time.
+//  * The work is a flat list of 64-position tiles ordered (sequence, kv head,
+//    tile).  A persistent grid of one CTA per SM cuts that list into equal
+//    contiguous ranges, so every CTA streams the same number of tiles and
+//    walks only a few (sequence, kv head) segments: a range holds whole
+//    segments in its middle and at most one part-segment at each end.
+//    Every CTA rebuilds the per-sequence tile counts from context_lens in
+//    shared memory and finds its first tile with a warp scan.
 //  * One producer warp issues TMA tile loads (cp.async.bulk.tensor, 64 rows x
 //    256 B per K or V tile; a row is one token of one kv head) into a
-//    5-stage shared-memory ring guarded by mbarriers, plus a bulk copy of the
-//    item's G query rows.  Tiles never straddle a block: the TMA box is
-//    gcd(B, 64) rows, and each box is addressed through the block table.
-//  * Four consumer warps each own 16 rows of a tile.  Q.K: 8 lanes per row,
-//    16 dims per lane, the whole GQA group's q (G x 16 values) in registers,
-//    partial sums combined with a shuffle reduce-scatter (each K byte is read
-//    from shared memory once for all G heads).  Online softmax in base 2 per
-//    warp, then P.V with each lane owning 4 output dims of all G heads.
-//  * Item end: the 4 warp states are merged in shared memory.  A one-chunk
-//    sequence writes bf16 output directly; otherwise the chunk's (m, l, o)
-//    partial goes to the workspace and the CTA that finishes the last chunk
-//    partial goes to the workspace and a small merge kernel, queued behind
-//    this one with programmatic dependent launch, combines the partials.
+//    4-stage shared-memory ring guarded by mbarriers, plus a bulk copy of the
+//    segment's G query rows.  Tiles never straddle a block: the TMA box is
+//    gcd(B, 64) rows, and each box is addressed through the block table,
+//    whose entries the producer's lanes prefetch 32 at a time.
+//  * Consumer warps (one or two groups of four; tiles alternate between the
+//    groups) each own 16 rows of a tile.  Q.K: 8 or 16 lanes per row, the
+//    whole GQA group's q in registers, partial sums combined with a shuffle
+//    reduce-scatter (each K byte is read from shared memory once for all G
+//    heads).  Online softmax in base 2 per warp, then P.V with each lane
+//    owning 4 output dims of all G heads.
+//  * Segment end: a merge warp combines the consumer warps' states.  A whole
+//    segment writes bf16 output directly; a part-segment writes its (m, l, o)
+//    partial to the workspace, and the CTA where the segment's sequence/head
+//    pair starts records a merge task.  A small merge kernel, queued behind
+//    this one with programmatic dependent launch, runs the tasks.
 //  * All waits are bounded; a timeout records PA_DEV_TIMEOUT and the warps
-//    finish their loops without waiting, keeping every named barrier paired.
+//    finish their loops without waiting, keeping every barrier paired.
 #include <math.h>
 
 #include <algorithm>
@@ -45,7 +48,7 @@ constexpr int TILE = 64;          // rows per pipeline stage
 constexpr int WPG = 4;            // consumer warps per group
 constexpr int TPW = TILE / WPG;   // rows per consumer warp per tile
 constexpr int kMaxBatch = 2048;
-constexpr int kMaxSplits = 512;
+constexpr int kMaxGrid = 256;     // CTAs of the persistent grid (min(SMs, this))
 constexpr unsigned FULL = 0xffffffffu;
 
 template <int G>
@@ -72,10 +75,10 @@ struct Cfg {
     static constexpr int OFF_SLOT = OFF_S + NCW * TPW * G * 4;  // merge slots [2][SLOT_FLOATS] f32
     static constexpr int OFF_BAR = OFF_SLOT + 2 * SLOT_FLOATS * 4;
     static constexpr int NBAR = 2 * STAGES + 8;  // full, empty, qfull[2], qempty[2], done[2], free[2]
-    static constexpr int OFF_FLAGS = OFF_BAR + NBAR * 8;
-    static constexpr int OFF_BID = OFF_FLAGS + 16;  // producer's block ids [2][32] int
-    static constexpr int OFF_CUM = OFF_BID + 256;   // [batch+1] int, then clamped ctx [batch] int
-    static constexpr size_t smem_bytes(int batch) { return OFF_CUM + 4 * (size_t)(2 * batch + 1) + 1024; }
+    static constexpr int OFF_FLAGS = OFF_BAR + NBAR * 8;  // [0]: abort
+    static constexpr int OFF_START = OFF_FLAGS + 16;      // RangeStart
+    static constexpr int OFF_CTX = OFF_START + 64;        // clamped context_lens [batch] int
+    static constexpr size_t smem_bytes(int batch) { return OFF_CTX + 4 * (size_t)batch + 1024; }
     static_assert(smem_bytes(kMaxBatch) <= 232448, "shared memory budget");
 };
 
@@ -88,11 +91,10 @@ struct DecodeArgs {
     int32_t max_blocks;
     int32_t batch, Hq, Hkv, block_size, box_rows, num_blocks;
     float scale_log2;
-    int32_t chunk_tokens;
-    int32_t max_splits;
-    int32_t ctx_limit;  // min(max_blocks*B, max_splits*chunk_tokens)
-    float *ws_o;        // [batch][Hq][max_splits][D]
-    float2 *ws_ml;      // [batch][Hq][max_splits]  (m, l) in base 2
+    int32_t ctx_limit;  // max_blocks * block_size
+    float *ws_o;        // [2 * kMaxGrid][G][D]     partials: slot 2j is CTA j's first segment, 2j+1 its last
+    float2 *ws_ml;      // [2 * kMaxGrid][G]        (m, l) in base 2
+    int4 *ws_task;      // [kMaxGrid]               {b, g, nsplit, first slot} of the pair that starts in CTA j
     DevError *err;
     int32_t checked;
 };
@@ -106,28 +108,54 @@ __device__ __forceinline__ int clamp_ctx(const DecodeArgs &a, int b, bool report
     return ctx;
 }
 
-struct Item {
-    int b, g, c, nsplit, p_begin, p_end, ntiles;
+// The tiles of pair (b, g) are [Hkv*CT_b + g*nt_b, ... + nt_b) in the flat
+// list, nt_b = ceil(ctx_b / TILE), CT_b = sum_{b' < b} nt_b'.  CTA j owns
+// `base + (j < rem)` tiles starting at j*base + min(j, rem).
+struct RangeStart {
+    int b, g, t, pad;
+    long long pos, len, base, rem;
 };
 
-__device__ __forceinline__ Item decode_item(const DecodeArgs &a, const int *cum, const int *ctx_s, int item) {
-    Item it;
-    const int chunk_id = item / a.Hkv;
-    it.g = item - chunk_id * a.Hkv;
-    int lo = 0, hi = a.batch - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (cum[mid] <= chunk_id) lo = mid; else hi = mid - 1;
-    }
-    it.b = lo;
-    it.c = chunk_id - cum[lo];
-    it.nsplit = cum[lo + 1] - cum[lo];
-    const int ctx = ctx_s[lo];
-    it.p_begin = it.c * a.chunk_tokens;
-    it.p_end = min(ctx, it.p_begin + a.chunk_tokens);
-    it.ntiles = (it.p_end - it.p_begin + TILE - 1) / TILE;
-    return it;
+__device__ __forceinline__ long long owner_cta(long long x, long long base, long long rem) {
+    const long long cut = rem * (base + 1);
+    return x < cut ? x / (base + 1) : rem + (x - cut) / base;
 }
+
+// One (sequence, kv head) part of a CTA's range.
+struct Seg {
+    int b, g, t_begin, t_end, nt, p_begin, p_end;
+    long long pos;  // flat index of tile t_begin
+};
+
+// Walks a CTA's range segment by segment.  Every role of the CTA runs its
+// own copy and sees the same sequence of segments.
+struct Walker {
+    int b, g, t;
+    long long pos, left;
+    __device__ explicit Walker(const RangeStart &st) : b(st.b), g(st.g), t(st.t), pos(st.pos), left(st.len) {}
+    __device__ bool next(const int *ctx_s, int Hkv, int batch, Seg &s) {
+        if (left <= 0) return false;
+        const int ctx = ctx_s[b];
+        const int nt = (ctx + TILE - 1) / TILE;
+        const int take = (int)min((long long)(nt - t), left);
+        s.b = b;
+        s.g = g;
+        s.t_begin = t;
+        s.t_end = t + take;
+        s.nt = nt;
+        s.p_begin = t * TILE;
+        s.p_end = min(ctx, s.t_end * TILE);
+        s.pos = pos;
+        left -= take;
+        pos += take;
+        t = 0;
+        if (++g == Hkv) {
+            g = 0;
+            do ++b; while (b < batch && ctx_s[b] == 0);
+        }
+        return true;
+    }
+};
 
 // Sum over the LPT lanes of a row group of v[h], scattered so that lane li
 // ends with the total of head li / (LPT / G).
@@ -170,8 +198,8 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     // Align to 1 KiB by pointer arithmetic on the __shared__ array, so every
     // pointer below stays in the shared address space (ld/st.shared).
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    int *cum = reinterpret_cast<int *>(smem + C::OFF_CUM);
-    int *ctx_s = cum + a.batch + 1;
+    int *ctx_s = reinterpret_cast<int *>(smem + C::OFF_CTX);
+    RangeStart *rs = reinterpret_cast<RangeStart *>(smem + C::OFF_START);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *empty = full + C::STAGES;
     uint64_t *qfull = empty + C::STAGES;
@@ -199,25 +227,52 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
     }
-    // Chunk prefix sum: cum[b+1] = sum_{b' <= b} ceil(ctx_b' / chunk_tokens).
+    // Per-sequence tile counts, the total, and this CTA's range.
     if (warp == 0) {
-        int run = 0;
-        if (lane == 0) cum[0] = 0;
+        long long total = 0;
         for (int base = 0; base < a.batch; base += 32) {
             const int b = base + lane;
-            int x = 0;
+            int nt = 0;
             if (b < a.batch) {
                 const int ctx = clamp_ctx(a, b, blockIdx.x == 0);
                 ctx_s[b] = ctx;
-                x = (ctx + a.chunk_tokens - 1) / a.chunk_tokens;
+                nt = (ctx + TILE - 1) / TILE;
             }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) nt += __shfl_xor_sync(FULL, nt, o);
+            total += nt;
+        }
+        __syncwarp();
+        const long long T = total * a.Hkv;
+        const long long j = blockIdx.x, base = T / gridDim.x, rem = T % gridDim.x;
+        const long long start = j * base + min(j, rem), len = base + (j < rem ? 1 : 0);
+        if (lane == 0) {
+            rs->pos = start;
+            rs->len = len;
+            rs->base = base;
+            rs->rem = rem;
+        }
+        // Find the pair holding tile `start`: a scan of the tile counts.
+        long long run = 0;
+        for (int cb = 0; len > 0 && cb < a.batch; cb += 32) {
+            const int b = cb + lane;
+            const int nt = b < a.batch ? (ctx_s[b] + TILE - 1) / TILE : 0;
+            int x = nt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(FULL, x, o);
                 if (lane >= o) x += y;
             }
-            if (b < a.batch) cum[b + 1] = run + x;
-            run += __shfl_sync(FULL, x, 31);
+            const long long lo = run + (long long)(x - nt) * a.Hkv;
+            const bool hit = nt > 0 && lo <= start && start < lo + (long long)nt * a.Hkv;
+            if (hit) {
+                const long long off = start - lo;
+                rs->b = b;
+                rs->g = (int)(off / nt);
+                rs->t = (int)(off % nt);
+            }
+            if (__any_sync(FULL, hit)) break;
+            run += (long long)__shfl_sync(FULL, x, 31) * a.Hkv;
         }
     }
     __syncthreads();
@@ -229,74 +284,78 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
             for (int j = threadIdx.x; j < a.Hq * D / 8; j += C::NCW * 32) o[j] = make_uint4(0, 0, 0, 0);
         }
     }
-    __syncthreads();
-    const int total_items = cum[a.batch] * a.Hkv;
     // The split-merge kernel queued behind this grid may be scheduled now; it
     // waits (griddepcontrol.wait) until this grid's results are visible.
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const RangeStart st = *rs;
 
     // ------------------------------------------------------------------ producer
     if (warp == C::PRODUCER) {
-        // Lane j holds the block id of logical block (p_begin / B + j) of an
-        // item; ids of item k+1 are fetched while lane 0 issues item k.
-        int *bid_s = reinterpret_cast<int *>(smem + C::OFF_BID);
-        auto fetch_ids = [&](int item) -> int {
-            if (item >= total_items) return -1;
-            const Item I = decode_item(a, cum, ctx_s, item);
-            const int first = I.p_begin / a.block_size;
-            const int nblk = (I.p_end - 1) / a.block_size - first + 1;
-            return lane < nblk ? __ldg(a.block_tables + (int64_t)I.b * a.max_blocks + first + lane) : -1;
+        // Lane l holds the block id of logical block wbase + l of the current
+        // segment's sequence; the next segment's first window is fetched while
+        // the current one is issued.
+        auto fetch = [&](const Seg &s, int lb) -> int {
+            const int nblk = (s.p_end - 1) / a.block_size + 1;  // logical blocks of the sequence in use
+            return lb + lane < nblk ? __ldg(a.block_tables + (int64_t)s.b * a.max_blocks + lb + lane) : -1;
         };
         const uint64_t pol = policy_evict_first();
-        uint32_t it = 0, k = 0, kq = 0;  // tiles issued, items seen, query copies issued
+        Walker w(st);
+        Seg cur, nxt;
+        bool have = w.next(ctx_s, a.Hkv, a.batch, cur);
+        int wbase = have ? cur.p_begin / a.block_size : 0;
+        int win = have ? fetch(cur, wbase) : -1;
+        bool have_n = have && w.next(ctx_s, a.Hkv, a.batch, nxt);
+        int win_n = have_n ? fetch(nxt, nxt.p_begin / a.block_size) : -1;
+        uint32_t it = 0, k = 0, kq = 0;  // tiles issued, segments seen, query copies issued
         bool ok = true;
-        int ids = fetch_ids(blockIdx.x);
-        for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x, ++k) {
-            bid_s[(k & 1) * 32 + lane] = ids;
-            __syncwarp();
-            ids = fetch_ids(item + gridDim.x);  // consumed next iteration
+        for (; ok && have; ++k) {
             if (lane == 0) {
-                const Item I = decode_item(a, cum, ctx_s, item);
-                const int first = I.p_begin / a.block_size;
-                const int nblk = (I.p_end - 1) / a.block_size - first + 1;
-                const int *bid = bid_s + (k & 1) * 32;
-                if (!wait_or_abort(&qempty[k & 1], ((k >> 1) & 1) ^ 1, flags, a, 100)) ok = false;
+                ok = wait_or_abort(&qempty[k & 1], ((k >> 1) & 1) ^ 1, flags, a, 100);
                 if (ok) {
                     mbar_arrive_expect_tx(&qfull[k & 1], G * ROW_BYTES);
                     bulk_load(smem + C::OFF_Q + (k & 1) * C::Q_BYTES,
-                              a.q + (int64_t)I.b * a.q_row_stride + (int64_t)I.g * G * D, G * ROW_BYTES,
+                              a.q + (int64_t)cur.b * a.q_row_stride + (int64_t)cur.g * G * D, G * ROW_BYTES,
                               &qfull[k & 1]);
                     ++kq;
                 }
-                for (int t = 0; ok && t < I.ntiles; ++t, ++it) {
-                    const int stage = it % C::STAGES;
-                    if (!wait_or_abort(&empty[stage], ((it / C::STAGES) & 1) ^ 1, flags, a, 101)) {
-                        ok = false;
-                        break;
+            }
+            ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+            for (int t = cur.t_begin; ok && t < cur.t_end; ++t, ++it) {
+                const int stage = it % C::STAGES;
+                if (lane == 0) ok = wait_or_abort(&empty[stage], ((it / C::STAGES) & 1) ^ 1, flags, a, 101);
+                ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                const int p0 = t * TILE;
+                const int rows = min(TILE, cur.p_end - p0);
+                const int nsub = (rows + a.box_rows - 1) / a.box_rows;
+                if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)nsub * a.box_rows * ROW_BYTES * 2);
+                uint8_t *ks = smem + stage * C::STAGE_BYTES;
+                uint8_t *vs = ks + TILE * ROW_BYTES;
+                for (int sub = 0; sub < nsub; ++sub) {
+                    const int ps = p0 + sub * a.box_rows;
+                    const int lb = ps / a.block_size;
+                    if (lb - wbase >= 32) {  // warp-uniform; only sequences with > 32 blocks in a segment
+                        wbase = lb;
+                        win = fetch(cur, lb);
                     }
-                    const int p0 = I.p_begin + t * TILE;
-                    const int rows = min(TILE, I.p_end - p0);
-                    const int nsub = (rows + a.box_rows - 1) / a.box_rows;
-                    mbar_arrive_expect_tx(&full[stage], (uint32_t)nsub * a.box_rows * ROW_BYTES * 2);
-                    uint8_t *ks = smem + stage * C::STAGE_BYTES;
-                    uint8_t *vs = ks + TILE * ROW_BYTES;
-                    for (int sub = 0; sub < nsub; ++sub) {
-                        const int ps = p0 + sub * a.box_rows;
-                        const int lb = ps / a.block_size - first;
-                        const int blk = nblk <= 32 ? bid[lb]
-                                                   : __ldg(a.block_tables + (int64_t)I.b * a.max_blocks + first + lb);
+                    const int blk = __shfl_sync(FULL, win, lb - wbase);
+                    if (lane == 0) {
                         if (a.checked && (blk < 0 || blk >= a.num_blocks))
-                            record_error(a.err, PA_DEV_BAD_BLOCK,
-                                         (long long)I.b * a.max_blocks + ps / a.block_size);
+                            record_error(a.err, PA_DEV_BAD_BLOCK, (long long)cur.b * a.max_blocks + lb);
                         long long slot = (long long)blk * a.block_size + ps % a.block_size;
                         // An invalid block id reads as zeros: TMA fills out-of-range boxes.
                         if (blk < 0 || blk >= a.num_blocks) slot = -2LL * a.box_rows;
-                        tma_load_3d(ks + sub * a.box_rows * ROW_BYTES, &tmk, 0, I.g, (int)slot, &full[stage], pol);
-                        tma_load_3d(vs + sub * a.box_rows * ROW_BYTES, &tmv, 0, I.g, (int)slot, &full[stage], pol);
+                        tma_load_3d(ks + sub * a.box_rows * ROW_BYTES, &tmk, 0, cur.g, (int)slot, &full[stage], pol);
+                        tma_load_3d(vs + sub * a.box_rows * ROW_BYTES, &tmv, 0, cur.g, (int)slot, &full[stage], pol);
                     }
                 }
             }
-            ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+            cur = nxt;
+            have = have_n;
+            win = win_n;
+            wbase = have ? cur.p_begin / a.block_size : 0;
+            have_n = have && w.next(ctx_s, a.Hkv, a.batch, nxt);
+            win_n = have_n ? fetch(nxt, nxt.p_begin / a.block_size) : -1;
         }
         if (!ok && lane == 0) {
             // Let the copies already issued land before the CTA's shared memory goes away.
@@ -315,9 +374,10 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     // ------------------------------------------------------------------ merger
     if (warp == C::MERGER) {
         float *slot_base = reinterpret_cast<float *>(smem + C::OFF_SLOT);
-        uint32_t k = 0;
-        for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++k) {
-            const Item I = decode_item(a, cum, ctx_s, item);
+        int4 task = make_int4(0, 0, 0, 0);  // {b, g, nsplit, first slot}; nsplit 0 = none
+        Walker w(st);
+        Seg sg;
+        for (uint32_t k = 0; w.next(ctx_s, a.Hkv, a.batch, sg); ++k) {
             const bool ok = wait_or_abort(&done[k & 1], (k >> 1) & 1, flags, a, 300);
             const float *so = slot_base + (k & 1) * C::SLOT_FLOATS;
             const float *sml = so + C::NCW * G * D;
@@ -326,14 +386,14 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
             for (int h = 0; h < G; ++h) {
                 M[h] = -INFINITY;
 #pragma unroll
-                for (int w = 0; w < C::NCW; ++w) M[h] = fmaxf(M[h], sml[(w * G + h) * 2]);
+                for (int w2 = 0; w2 < C::NCW; ++w2) M[h] = fmaxf(M[h], sml[(w2 * G + h) * 2]);
                 L[h] = 0.f;
                 O[h][0] = O[h][1] = O[h][2] = O[h][3] = 0.f;
 #pragma unroll
-                for (int w = 0; w < C::NCW; ++w) {
-                    const float f = fast_exp2(sml[(w * G + h) * 2] - M[h]);
-                    L[h] = fmaf(sml[(w * G + h) * 2 + 1], f, L[h]);
-                    const float4 v = *reinterpret_cast<const float4 *>(so + (w * G + h) * D + 4 * lane);
+                for (int w2 = 0; w2 < C::NCW; ++w2) {
+                    const float f = fast_exp2(sml[(w2 * G + h) * 2] - M[h]);
+                    L[h] = fmaf(sml[(w2 * G + h) * 2 + 1], f, L[h]);
+                    const float4 v = *reinterpret_cast<const float4 *>(so + (w2 * G + h) * D + 4 * lane);
                     O[h][0] = fmaf(v.x, f, O[h][0]);
                     O[h][1] = fmaf(v.y, f, O[h][1]);
                     O[h][2] = fmaf(v.z, f, O[h][2]);
@@ -343,8 +403,8 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sfree[k & 1]);
             if (!ok) continue;
-            const int64_t bh0 = (int64_t)I.b * a.Hq + (int64_t)I.g * G;  // first q-head row of (b, g)
-            if (I.nsplit == 1) {
+            if (sg.t_begin == 0 && sg.t_end == sg.nt) {  // the whole pair: final output
+                const int64_t bh0 = (int64_t)sg.b * a.Hq + (int64_t)sg.g * G;  // first q-head row of (b, g)
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     const float inv = 1.f / L[h];
@@ -357,14 +417,21 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                 }
                 continue;
             }
+            // A part of the pair: only a range's first and last segments can be.
+            const int slot = 2 * (int)blockIdx.x + (k == 0 ? 0 : 1);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const int64_t pi = (bh0 + h) * a.max_splits + I.c;
-                *reinterpret_cast<float4 *>(a.ws_o + pi * D + 4 * lane) =
+                *reinterpret_cast<float4 *>(a.ws_o + ((int64_t)slot * G + h) * D + 4 * lane) =
                     make_float4(O[h][0], O[h][1], O[h][2], O[h][3]);
-                if (lane == 0) a.ws_ml[pi] = make_float2(M[h], L[h]);
+                if (lane == 0) a.ws_ml[slot * G + h] = make_float2(M[h], L[h]);
+            }
+            if (sg.t_begin == 0) {  // the pair starts here and goes on in the next CTAs
+                const long long last = sg.pos + sg.nt - 1;
+                const int nsplit = (int)(owner_cta(last, st.base, st.rem) - blockIdx.x) + 1;
+                task = make_int4(sg.b, sg.g, nsplit, slot);
             }
         }
+        if (lane == 0) a.ws_task[blockIdx.x] = task;
         return;
     }
 
@@ -377,10 +444,10 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
 
     float qf[G][C::DPL];
     float m_run[G], l_run[G], o[G][4];
-    uint32_t it = 0, k = 0;
-
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++k) {
-        const Item I = decode_item(a, cum, ctx_s, item);
+    uint32_t it = 0;
+    Walker w(st);
+    Seg sg;
+    for (uint32_t k = 0; w.next(ctx_s, a.Hkv, a.batch, sg); ++k) {
         if (wait_or_abort(&qfull[k & 1], (k >> 1) & 1, flags, a, 200 + warp)) {
             const uint32_t qa = smem_addr(smem + C::OFF_Q + (k & 1) * C::Q_BYTES);
 #pragma unroll
@@ -405,13 +472,13 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
             l_run[h] = 0.f;
             o[h][0] = o[h][1] = o[h][2] = o[h][3] = 0.f;
         }
-        for (int t = 0; t < I.ntiles; ++t, ++it) {
+        for (int t = sg.t_begin; t < sg.t_end; ++t, ++it) {
             if ((int)(it % C::NGRP) != grp) continue;
             const int stage = it % C::STAGES;
             if (wait_or_abort(&full[stage], (it / C::STAGES) & 1, flags, a, 210 + warp)) {
                 const uint32_t ks = smem_addr(smem + stage * C::STAGE_BYTES);
                 const uint32_t vsa = ks + TILE * ROW_BYTES;
-                const int nvalid = min(TILE, I.p_end - (I.p_begin + t * TILE));
+                const int nvalid = min(TILE, sg.p_end - t * TILE);
                 // ---- scores for rows wig*TPW + r*RPR + rg
                 uint4 kw[C::ROUNDS][C::DPL / 8];
 #pragma unroll
@@ -527,50 +594,35 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     }
 }
 
-// Log-sum-exp merge of the split partials of one (sequence, q head):
-// M = max_c m_c, L = sum_c l_c 2^(m_c - M), out = sum_c o_c 2^(m_c - M) / L.
-// Launched after decode_kernel on the same stream (programmatic dependent
-// launch: it may start early and waits for the decode grid's results).
-__global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeArgs a) {
-    __shared__ float wts[kMaxSplits];
+// Log-sum-exp merge of a pair split across CTAs j0 .. j0+nsplit-1 (task of
+// CTA j0): M = max_c m_c, L = sum_c l_c 2^(m_c - M), out = sum_c o_c 2^(m_c - M) / L.
+// The pair's partial in CTA j0 is in the task's slot; in every later CTA it
+// is that CTA's first segment, slot 2j.  Launched after decode_kernel on the
+// same stream (programmatic dependent launch: it may start early and waits
+// for the decode grid's results).
+__global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeArgs a, int G) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int bh = blockIdx.x;
-    const int b = bh / a.Hq;
-    const int ctx = clamp_ctx(a, b, false);
-    const int nsplit = (ctx + a.chunk_tokens - 1) / a.chunk_tokens;
-    if (nsplit <= 1) return;  // written directly by decode_kernel
-    const float2 *ml = a.ws_ml + (int64_t)bh * a.max_splits;
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
+    const int4 task = a.ws_task[blockIdx.x];
+    const int nsplit = task.z;
+    if (nsplit <= 1) return;
+    const int j0 = blockIdx.x, d = threadIdx.x;
+    for (int h = 0; h < G; ++h) {
         float M = -INFINITY;
-        for (int c = lane; c < nsplit; c += 32) M = fmaxf(M, ml[c].x);
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
-        float L = 0.f;
-        for (int c = lane; c < nsplit; c += 32) {
-            const float2 v = ml[c];
-            const float f = fast_exp2(v.x - M);
-            wts[c] = f;
-            L = fmaf(v.y, f, L);
+        for (int c = 0; c < nsplit; ++c) {
+            const int slot = c == 0 ? task.w : 2 * (j0 + c);
+            M = fmaxf(M, a.ws_ml[slot * G + h].x);
         }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(FULL, L, off);
-        const float invL = 1.f / L;
-        __syncwarp();
-        for (int c = lane; c < nsplit; c += 32) wts[c] *= invL;
+        float L = 0.f, acc = 0.f;
+        for (int c = 0; c < nsplit; ++c) {
+            const int slot = c == 0 ? task.w : 2 * (j0 + c);
+            const float2 ml = a.ws_ml[slot * G + h];
+            const float f = fast_exp2(ml.x - M);
+            L = fmaf(ml.y, f, L);
+            acc = fmaf(a.ws_o[((int64_t)slot * G + h) * D + d], f, acc);
+        }
+        const int64_t row = (int64_t)task.x * a.Hq + (int64_t)task.y * G + h;
+        a.out[row * D + d] = __float2bfloat16_rn(acc / L);
     }
-    __syncthreads();
-    const float *po = a.ws_o + (int64_t)bh * a.max_splits * D + threadIdx.x;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-    int c = 0;
-    for (; c + 4 <= nsplit; c += 4) {
-        acc0 = fmaf(po[(int64_t)(c + 0) * D], wts[c + 0], acc0);
-        acc1 = fmaf(po[(int64_t)(c + 1) * D], wts[c + 1], acc1);
-        acc2 = fmaf(po[(int64_t)(c + 2) * D], wts[c + 2], acc2);
-        acc3 = fmaf(po[(int64_t)(c + 3) * D], wts[c + 3], acc3);
-    }
-    for (; c < nsplit; ++c) acc0 = fmaf(po[(int64_t)c * D], wts[c], acc0);
-    a.out[(int64_t)bh * D + threadIdx.x] = __float2bfloat16_rn((acc0 + acc1) + (acc2 + acc3));
 }
 
 int g_attr_done[64][4] = {};
@@ -589,9 +641,9 @@ pa_status launch(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &
     }
     decode_kernel<G><<<grid, Cfg<G>::NTHREADS, Cfg<G>::smem_bytes(a.batch), st>>>(tk, tv, a);
     pa_status r = check_launch("decode_kernel");
-    if (r != PA_OK || a.max_splits <= 1) return r;
+    if (r != PA_OK) return r;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.batch * a.Hq));
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(D);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
@@ -600,40 +652,26 @@ pa_status launch(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_merge_kernel, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_merge_kernel, a, G);
     if (e != cudaSuccess) return cuda_fail(e, "decode_merge_kernel");
     return check_launch("decode_merge_kernel");
 }
 
-int chunk_tokens_for(int max_ctx) {
-    int chunk = 4 * TILE;  // 256 positions per work item
-    if (max_ctx > 0 && (max_ctx + chunk - 1) / chunk > kMaxSplits) {
-        chunk = (max_ctx + kMaxSplits - 1) / kMaxSplits;
-        chunk = (chunk + TILE - 1) / TILE * TILE;
-    }
-    return chunk;
-}
-
+// Workspace: (m, l) pairs, then fp32 partials, then merge tasks; two partial
+// slots per CTA of the largest grid.
 struct WsLayout {
-    size_t ml_off, o_off, total;
-    int max_splits, chunk;
+    size_t ml_off, o_off, task_off, total;
 };
 
-WsLayout ws_layout(int batch, int Hq, int max_ctx) {
-    WsLayout L;
-    L.chunk = chunk_tokens_for(max_ctx);
-    L.max_splits = max_ctx > 0 ? (max_ctx + L.chunk - 1) / L.chunk : 1;
+WsLayout ws_layout(int G) {
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t slots = 2 * (size_t)kMaxGrid * G;
+    WsLayout L;
     L.ml_off = 0;
-    L.o_off = up((size_t)batch * Hq * L.max_splits * 8);
-    L.total = L.o_off + (size_t)batch * Hq * L.max_splits * D * 4;
+    L.o_off = up(slots * sizeof(float2));
+    L.task_off = up(L.o_off + slots * D * sizeof(float));
+    L.total = L.task_off + (size_t)kMaxGrid * sizeof(int4);
     return L;
-}
-
-int effective_max_ctx(int32_t max_context_len, int32_t max_blocks, int32_t block_size) {
-    const int64_t cap = (int64_t)max_blocks * block_size;
-    if (max_context_len <= 0 || max_context_len > cap) return (int)cap;
-    return max_context_len;
 }
 
 }  // namespace
@@ -641,24 +679,19 @@ int effective_max_ctx(int32_t max_context_len, int32_t max_blocks, int32_t block
 
 extern "C" {
 
-size_t pa_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                                int32_t head_dim, int32_t max_context_len,
-                                int32_t max_blocks_per_seq, int32_t block_size) {
+size_t pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim) {
     using namespace pa;
-    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim != D || block_size <= 0 ||
-        max_blocks_per_seq <= 0)
-        return 0;
-    (void)num_kv_heads;
-    return ws_layout(batch, num_q_heads, effective_max_ctx(max_context_len, max_blocks_per_seq, block_size))
-        .total;
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads || head_dim != D) return 0;
+    const int G = num_q_heads / num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return 0;
+    return ws_layout(G).total;
 }
 
 pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *k_cache,
                     const void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
                     const int32_t *context_lens, int32_t batch, int32_t num_q_heads,
                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                    float softmax_scale, int32_t max_context_len, void *workspace,
-                    size_t workspace_bytes, pa_stream_t stream) {
+                    float softmax_scale, void *workspace, size_t workspace_bytes, pa_stream_t stream) {
     using namespace pa;
     if (batch < 0) return fail(PA_ERR_INVALID_ARG, "batch < 0");
     if (batch == 0) return PA_OK;
@@ -684,12 +717,11 @@ pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *
         return fail(PA_ERR_INVALID_ARG, "out/q/cache pointers must be 16-byte aligned");
     if (!(softmax_scale > 0.f) || !isfinite(softmax_scale))
         return fail(PA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
-    const int max_ctx = effective_max_ctx(max_context_len, max_blocks_per_seq, block_size);
-    const WsLayout W = ws_layout(batch, num_q_heads, max_ctx);
-    if (W.max_splits > 1 && (!workspace || workspace_bytes < W.total))
+    const WsLayout W = ws_layout(G);
+    if (!workspace || workspace_bytes < W.total)
         return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", W.total,
                     workspace ? workspace_bytes : (size_t)0);
-    if (workspace && !aligned16(workspace)) return fail(PA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    if (!aligned16(workspace)) return fail(PA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
 
     int box = 64;
     while (block_size % box) box >>= 1;  // gcd(block_size, 64) in {16, 32, 64}
@@ -713,17 +745,15 @@ pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *
     A.box_rows = box;
     A.num_blocks = num_blocks;
     A.scale_log2 = softmax_scale * 1.4426950408889634f;
-    A.chunk_tokens = W.chunk;
-    A.max_splits = W.max_splits;
-    A.ctx_limit = (int)std::min<int64_t>((int64_t)max_blocks_per_seq * block_size,
-                                         (int64_t)W.max_splits * W.chunk);
+    A.ctx_limit = max_blocks_per_seq * block_size;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    A.ws_ml = ws ? reinterpret_cast<float2 *>(ws + W.ml_off) : nullptr;
-    A.ws_o = ws ? reinterpret_cast<float *>(ws + W.o_off) : nullptr;
+    A.ws_ml = reinterpret_cast<float2 *>(ws + W.ml_off);
+    A.ws_o = reinterpret_cast<float *>(ws + W.o_off);
+    A.ws_task = reinterpret_cast<int4 *>(ws + W.task_off);
     A.err = device_error_ptr();
     A.checked = checked_mode() ? 1 : 0;
 
-    const int sms = sm_count();
+    const int sms = std::min(sm_count(), kMaxGrid);
     if (sms <= 0) return fail(PA_ERR_CUDA, "no CUDA device");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (G) {
@@ -742,9 +772,10 @@ pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *
 // this library's device image instead of a caller-provided workspace.
 // ---------------------------------------------------------------------------
 
-// 32 MiB of split-partial scratch.  It is loaded with the module, so every GPU
-// that loads this library holds it until the process exits.
-static constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+// Split-partial scratch, enough for every shape (the workspace size depends
+// only on the GQA group).  It is loaded with the module, so every GPU that
+// loads this library holds it until the process exits.
+static constexpr size_t kStaticScratchBytes = size_t(4) << 20;
 static __device__ __align__(256) unsigned char pa_static_scratch[kStaticScratchBytes];
 
 namespace {
@@ -757,19 +788,15 @@ extern "C" pa_status pa_decode_static(void *out, const void *q, int64_t q_row_st
                                       int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
                                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                       int32_t block_size, int32_t num_blocks, float softmax_scale,
-                                      int32_t max_context_len, pa_stream_t stream) {
+                                      pa_stream_t stream) {
     using namespace pa;
-    const size_t need = pa_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_context_len,
-                                                 max_blocks_per_seq, block_size);
-    if (need == 0)  // batch == 0 or arguments pa_decode rejects: let it report
+    static_assert(kStaticScratchBytes >= 2 * (size_t)kMaxGrid * 8 * (D * 4 + 8) + kMaxGrid * 16 + 512,
+                  "the static scratch holds the workspace of the largest GQA group");
+    const size_t need = pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim);
+    if (need == 0 || batch <= 0)  // batch == 0 or arguments pa_decode rejects: let it report
         return pa_decode(out, q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq,
                          context_lens, batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                         softmax_scale, max_context_len, nullptr, 0, stream);
-    if (need > kStaticScratchBytes)
-        return fail(PA_ERR_WORKSPACE,
-                    "pa_decode_static: this shape needs %zu bytes of split scratch but the built-in scratch "
-                    "holds %zu; lower max_context_len/batch or call pa_decode with a workspace",
-                    need, kStaticScratchBytes);
+                         softmax_scale, nullptr, 0, stream);
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -788,6 +815,6 @@ extern "C" pa_status pa_decode_static(void *out, const void *q, int64_t q_row_st
         scratch = g_static_scratch_addr[dev];
     }
     return pa_decode(out, q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                     batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, softmax_scale,
-                     max_context_len, scratch, kStaticScratchBytes, stream);
+                     batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, softmax_scale, scratch,
+                     kStaticScratchBytes, stream);
 }

@@ -46,17 +46,17 @@ def test_status_strings(L):
 
 
 def test_workspace_size_host_math(L):
-    # Short contexts: one chunk per sequence still reserves counters + partials for 1 split.
-    small = L.pa_decode_workspace_size(4, 16, 8, 128, 256, 1, 256)
-    assert small > 0
-    # 64 sequences, 16 q heads, 8 kv heads, up to 4096 tokens in 256-token chunks: 16 splits.
-    n = L.pa_decode_workspace_size(64, 16, 8, 128, 4096, 16, 256)
-    assert n >= 64 * 16 * 16 * (128 * 4 + 8)
-    # Unsupported head_dim gives 0.
-    assert L.pa_decode_workspace_size(64, 16, 8, 64, 4096, 16, 256) == 0
-    # A very long context caps the number of splits (chunks grow instead).
-    big = L.pa_decode_workspace_size(1, 8, 8, 128, 1 << 20, 4096, 256)
-    assert big <= 1 * 8 * 512 * (128 * 4 + 8) + 4096
+    # Two partial slots of G heads per CTA of the largest grid (256 CTAs), plus merge tasks:
+    # independent of batch and context length.
+    for hq, hkv in [(16, 8), (32, 8), (8, 8), (64, 8)]:
+        g = hq // hkv
+        n = L.pa_decode_workspace_size(hq, hkv, 128)
+        assert 2 * 256 * g * (128 * 4 + 8) <= n <= 2 * 256 * g * (128 * 4 + 8) + 256 * 16 + 1024
+    assert L.pa_decode_workspace_size(64, 8, 128) <= 4 << 20       # fits the static scratch
+    # Unsupported shapes give 0.
+    assert L.pa_decode_workspace_size(16, 8, 64) == 0
+    assert L.pa_decode_workspace_size(24, 8, 128) == 0
+    assert L.pa_decode_workspace_size(12, 8, 128) == 0
 
 
 def _msg(L):
@@ -79,10 +79,10 @@ def test_store_argument_checks(L):
 def _decode(L, **kw):
     p = C.c_void_p(256)
     a = dict(out=p, q=p, q_row_stride=2048, k=p, v=p, bt=p, mb=16, ctx=p, batch=4, hq=16, hkv=8, d=128,
-             B=256, nb=64, scale=0.088, maxctx=0, ws=p, wsb=1 << 30, stream=None)
+             B=256, nb=64, scale=0.088, ws=p, wsb=1 << 30, stream=None)
     a.update(kw)
     return L.pa_decode(a["out"], a["q"], a["q_row_stride"], a["k"], a["v"], a["bt"], a["mb"], a["ctx"],
-                       a["batch"], a["hq"], a["hkv"], a["d"], a["B"], a["nb"], a["scale"], a["maxctx"],
+                       a["batch"], a["hq"], a["hkv"], a["d"], a["B"], a["nb"], a["scale"],
                        a["ws"], a["wsb"], a["stream"])
 
 
@@ -101,6 +101,7 @@ def test_decode_argument_checks(L):
     assert _decode(L, wsb=100) == pa.PA_ERR_WORKSPACE
     assert "workspace" in _msg(L)
     assert _decode(L, k=C.c_void_p(258)) == pa.PA_ERR_INVALID_ARG
+    assert _decode(L, ws=C.c_void_p(264)) == pa.PA_ERR_INVALID_ARG      # unaligned workspace
     assert _decode(L, nb=1 << 24) == pa.PA_ERR_UNSUPPORTED       # slots overflow int32
 
 

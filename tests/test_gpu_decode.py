@@ -17,13 +17,13 @@ from gpu_util import assert_close, dev_bf16, dev_i32, host_bits, host_f64
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu_step(inp, max_context_len=0):
+def run_gpu_step(inp):
     """store the decoded token's K/V at its slot, then decode; returns (out, caches)."""
     kc, vc = dev_bf16(inp.k_cache), dev_bf16(inp.v_cache)
     bt, ctx = dev_i32(inp.block_tables), dev_i32(inp.context_lens)
     slots = pa.slot_mapping_decode(bt, ctx, inp.block_size)
     pa.store_kvcache(dev_bf16(inp.new_k), dev_bf16(inp.new_v), kc, vc, slots)
-    out = pa.decode(dev_bf16(inp.q), kc, vc, bt, ctx, inp.scale, max_context_len=max_context_len)
+    out = pa.decode(dev_bf16(inp.q), kc, vc, bt, ctx, inp.scale)
     code, where = pa.get_device_error()
     assert code == 0, (code, where)
     return out, kc, vc
@@ -93,17 +93,24 @@ def test_decode_strided_q_rows():
     assert_close(host_f64(out), want, "strided q")
 
 
-def test_decode_split_count_does_not_change_result():
-    """One long sequence: splitting into 256-token chunks (merge of 40 partials)
-    and the same data in a batch where the hint forces the same chunks agree
-    with the unsplit oracle."""
-    ctx = [10000]
-    inp = make_decode("long", 10, 1, 32, 8, ctx)
+def test_decode_pairs_cut_across_many_ctas():
+    """One long sequence: its 8 (sequence, kv head) pairs of 157 tiles are cut
+    into ranges of ~8 tiles, so every pair is merged from ~20 CTA partials,
+    most of them a CTA's only segment."""
+    inp = make_decode("long", 10, 1, 32, 8, [10000])
     out, _, _ = run_gpu_step(inp)
     want, _, _ = run_oracle_step(inp)
     assert_close(host_f64(out), want, "long")
-    out2, _, _ = run_gpu_step(inp, max_context_len=10000)
-    assert torch.equal(out, out2)
+
+
+def test_decode_fewer_tiles_than_ctas():
+    """Fewer tiles than CTAs: most CTAs get no work, the rest one tile, and a
+    pair of several tiles is merged from one-tile partials."""
+    for hq, hkv, ctx in [(8, 8, [1]), (16, 8, [130, 5]), (8, 1, [64 * 40 + 3])]:
+        inp = make_decode(f"few {hq}/{hkv}", 14, len(ctx), hq, hkv, ctx)
+        out, _, _ = run_gpu_step(inp)
+        want, _, _ = run_oracle_step(inp)
+        assert_close(host_f64(out), want, f"few tiles {hq}/{hkv} {ctx}")
 
 
 def test_decode_repeated_calls_reuse_workspace():
@@ -112,7 +119,7 @@ def test_decode_repeated_calls_reuse_workspace():
     inp = make_decode("repeat", 11, 4, 16, 8, ctx)
     kc, vc = dev_bf16(inp.k_cache), dev_bf16(inp.v_cache)
     q, bt, cl = dev_bf16(inp.q), dev_i32(inp.block_tables), dev_i32(inp.context_lens)
-    ws = pa.decode_workspace(4, 16, 8, 128, 0, inp.max_blocks, 256)
+    ws = pa.decode_workspace(16, 8, 128)
     outs = [pa.decode(q, kc, vc, bt, cl, inp.scale, workspace=ws) for _ in range(5)]
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
