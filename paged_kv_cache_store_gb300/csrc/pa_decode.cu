@@ -13,18 +13,30 @@
 //    segments in its middle and at most one part-segment at each end.
 //    Every CTA rebuilds the per-sequence tile counts from context_lens in
 //    shared memory and finds its first tile with a warp scan.
-//  * One producer warp issues TMA tile loads (cp.async.bulk.tensor, 64 rows x
+//  * Two producer warps issue TMA tile loads (cp.async.bulk.tensor, 64 rows x
 //    256 B per K or V tile; a row is one token of one kv head) into a
-//    4-stage shared-memory ring guarded by mbarriers, plus a bulk copy of the
-//    segment's G query rows.  Tiles never straddle a block: the TMA box is
-//    gcd(B, 64) rows, and each box is addressed through the block table,
-//    whose entries the producer's lanes prefetch 32 at a time.
-//  * Consumer warps (one or two groups of four; tiles alternate between the
-//    groups) each own 16 rows of a tile.  Q.K: 8 or 16 lanes per row, the
-//    whole GQA group's q in registers, partial sums combined with a shuffle
-//    reduce-scatter (each K byte is read from shared memory once for all G
-//    heads).  Online softmax in base 2 per warp, then P.V with each lane
-//    owning 4 output dims of all G heads.
+//    4-stage shared-memory ring guarded by mbarriers: one warp the K tiles
+//    and the segment's G query rows (a bulk copy), the other the V tiles.
+//    Split this way, each warp's issue latency (mbarrier and TMA operations
+//    queue behind the consumers' shared-memory traffic) is paid in parallel.
+//    Tiles never straddle a block: the TMA box is gcd(B, 64) rows, and each
+//    box is addressed through the block table, whose entries the producers'
+//    lanes prefetch 32 at a time.
+//  * K and V tiles land 128-byte swizzled, split into the two 64-dim halves
+//    of each row ([half][row][64]; the tensor map views a pool as
+//    [kv head][half][slot][64]), so that 8 consecutive rows at one 16-byte
+//    column sit in 8 different banks.
+//  * Eight consumer warps in two groups of four; tiles alternate between the
+//    groups and each warp owns 16 keys of a tile.  Q.K and P.V run on the
+//    tensor cores as mma.sync m16n8k16 (bf16 in, fp32 accumulate) with the
+//    GQA group's G query rows as the M side (rows G..15 are zero): the whole
+//    group shares each K and V byte, operands come by ldmatrix, and the S
+//    fragment of Q.K is already the A fragment of P.V.  This is not about
+//    tensor throughput (decode moves ~2 flops per byte) but about issue and
+//    shared-memory traffic: one MMA replaces 64 FMAs and the scores need no
+//    shuffle reduction.  Online softmax in base 2 with a lazy reference max:
+//    the running max only moves (rescaling O and l) when a score exceeds it
+//    by more than 2^8, which a warp vote detects.
 //  * Segment end: a merge warp combines the consumer warps' states.  A whole
 //    segment writes bf16 output directly; a part-segment writes its (m, l, o)
 //    partial to the workspace, and the CTA where the segment's sequence/head
@@ -46,35 +58,33 @@ constexpr int D = 128;
 constexpr int ROW_BYTES = D * 2;  // one token row of one kv head
 constexpr int TILE = 64;          // rows per pipeline stage
 constexpr int WPG = 4;            // consumer warps per group
-constexpr int TPW = TILE / WPG;   // rows per consumer warp per tile
+constexpr int KPW = TILE / WPG;   // keys per consumer warp per tile (one MMA n-pair)
+constexpr float kLazyRescale = 8.f;  // log2 headroom before the running max must move
 constexpr int kMaxBatch = 2048;
 constexpr int kMaxGrid = 256;     // CTAs of the persistent grid (min(SMs, this))
 constexpr unsigned FULL = 0xffffffffu;
 
 template <int G>
 struct Cfg {
-    static constexpr int NGRP = (G <= 4) ? 2 : 1;  // consumer groups; tiles alternate between them
+    static constexpr int NGRP = 2;                 // consumer groups; tiles alternate between them
     static constexpr int NCW = WPG * NGRP;         // consumer warps
-    static constexpr int PRODUCER = NCW;           // warp that issues the TMA copies
-    static constexpr int MERGER = NCW + 1;         // warp that finishes work items
-    static constexpr int NTHREADS = (NCW + 2) * 32;
+    static constexpr int PRODUCER_K = NCW;         // warp that issues the K tile (and q) copies
+    static constexpr int PRODUCER_V = NCW + 1;     // warp that issues the V tile copies
+    static constexpr int MERGER = NCW + 2;         // warp that finishes segments
+    static constexpr int NTHREADS = (NCW + 3) * 32;
     // Stage s only ever holds tiles of group s % NGRP, so each full/empty
     // barrier has waiters of one group only and a parity wait can never see a
     // phase two steps old (another group's pending copy) as its own.
     static constexpr int STAGES = 4;
     static_assert(STAGES % NGRP == 0, "a stage must belong to a single consumer group");
-    static constexpr int LPT = (G <= 4) ? 8 : 16;  // lanes per row in Q.K
-    static constexpr int DPL = D / LPT;            // dims per lane in Q.K
-    static constexpr int RPR = 32 / LPT;           // rows per warp per Q.K round
-    static constexpr int ROUNDS = TPW / RPR;
+    static constexpr int NSLOT = 2;  // merge slots (consumer warps -> merge warp), used round-robin
     static constexpr int STAGE_BYTES = 2 * TILE * ROW_BYTES;
     static constexpr int Q_BYTES = G * ROW_BYTES;
     static constexpr int SLOT_FLOATS = NCW * G * (D + 2);      // o[NCW][G][D], then (m,l)[NCW][G]
     static constexpr int OFF_Q = STAGES * STAGE_BYTES;          // q slots [2][G][D] bf16
-    static constexpr int OFF_S = OFF_Q + 2 * Q_BYTES;           // scores [NCW][TPW][G] f32
-    static constexpr int OFF_SLOT = OFF_S + NCW * TPW * G * 4;  // merge slots [2][SLOT_FLOATS] f32
-    static constexpr int OFF_BAR = OFF_SLOT + 2 * SLOT_FLOATS * 4;
-    static constexpr int NBAR = 2 * STAGES + 8;  // full, empty, qfull[2], qempty[2], done[2], free[2]
+    static constexpr int OFF_SLOT = OFF_Q + 2 * Q_BYTES;        // merge slots [NSLOT][SLOT_FLOATS] f32
+    static constexpr int OFF_BAR = OFF_SLOT + NSLOT * SLOT_FLOATS * 4;
+    static constexpr int NBAR = 3 * STAGES + 8;  // kfull, vfull, empty, qfull[2], qempty[2], done[2], free[2]
     static constexpr int OFF_FLAGS = OFF_BAR + NBAR * 8;  // [0]: abort
     static constexpr int OFF_START = OFF_FLAGS + 16;      // RangeStart
     static constexpr int OFF_CTX = OFF_START + 64;        // clamped context_lens [batch] int
@@ -157,26 +167,42 @@ struct Walker {
     }
 };
 
-// Sum over the LPT lanes of a row group of v[h], scattered so that lane li
-// ends with the total of head li / (LPT / G).
-template <int G, int LPT>
-__device__ __forceinline__ float reduce_scatter(float (&v)[G], int li) {
-#pragma unroll
-    for (int step = 0, off = LPT / 2; off >= 1; ++step, off >>= 1) {
-        if ((G >> step) > 1) {
-            const int half = G >> (step + 1);
-            const bool upper = (li & off) != 0;
-#pragma unroll
-            for (int k = 0; k < half; ++k) {
-                const float send = upper ? v[k] : v[k + half];
-                const float keep = upper ? v[k + half] : v[k];
-                v[k] = keep + __shfl_xor_sync(FULL, send, off);
-            }
-        } else {
-            v[0] += __shfl_xor_sync(FULL, v[0], off);
-        }
-    }
-    return v[0];
+// D += A.B for one m16n8k16 tile: A 16x16 bf16 (row-major fragments),
+// B 16x8 bf16 (column fragments), D 16x8 fp32.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four 8x8 bf16 matrices from shared memory; lanes 8i..8i+7 give the row
+// addresses of matrix i.  The .trans form delivers them transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
 }
 
 // Bounded wait that turns a timeout into a recorded error and a CTA-wide abort.
@@ -200,8 +226,9 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     int *ctx_s = reinterpret_cast<int *>(smem + C::OFF_CTX);
     RangeStart *rs = reinterpret_cast<RangeStart *>(smem + C::OFF_START);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint64_t *empty = full + C::STAGES;
+    uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *vfull = kfull + C::STAGES;
+    uint64_t *empty = vfull + C::STAGES;
     uint64_t *qfull = empty + C::STAGES;
     uint64_t *qempty = qfull + 2;
     uint64_t *done = qempty + 2;
@@ -211,7 +238,8 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&kfull[s], 1);
+            mbar_init(&vfull[s], 1);
             mbar_init(&empty[s], WPG);
         }
         for (int k = 0; k < 2; ++k) {
@@ -223,10 +251,8 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
         flags[0] = 0;
         fence_mbar_init();
     }
-    if (warp == C::PRODUCER && lane == 0) {
-        prefetch_tensormap(&tmk);
-        prefetch_tensormap(&tmv);
-    }
+    if (warp == C::PRODUCER_K && lane == 0) prefetch_tensormap(&tmk);
+    if (warp == C::PRODUCER_V && lane == 0) prefetch_tensormap(&tmv);
     // Per-sequence tile counts, the total, and this CTA's range.
     if (warp == 0) {
         long long total = 0;
@@ -289,8 +315,16 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const RangeStart st = *rs;
 
-    // ------------------------------------------------------------------ producer
-    if (warp == C::PRODUCER) {
+    // ------------------------------------------------------------------ producers
+    // Two warps on different SM sub-partitions: one issues the K tiles (and
+    // the segment's q rows), the other the V tiles, each completing on its own
+    // barrier of the stage.  Both wait on the stage's empty barrier; neither
+    // can fall two phases behind, since a stage is only released again after
+    // both of its copies landed.
+    if (warp == C::PRODUCER_K || warp == C::PRODUCER_V) {
+        const bool isk = warp == C::PRODUCER_K;
+        const CUtensorMap *tm = isk ? &tmk : &tmv;
+        uint64_t *fullb = isk ? kfull : vfull;
         // Lane l holds the block id of logical block wbase + l of the current
         // segment's sequence; the next segment's first window is fetched while
         // the current one is issued.
@@ -309,17 +343,19 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
         uint32_t it = 0, k = 0, kq = 0;  // tiles issued, segments seen, query copies issued
         bool ok = true;
         for (; ok && have; ++k) {
-            if (lane == 0) {
-                ok = wait_or_abort(&qempty[k & 1], ((k >> 1) & 1) ^ 1, flags, a, 100);
-                if (ok) {
-                    mbar_arrive_expect_tx(&qfull[k & 1], G * ROW_BYTES);
-                    bulk_load(smem + C::OFF_Q + (k & 1) * C::Q_BYTES,
-                              a.q + (int64_t)cur.b * a.q_row_stride + (int64_t)cur.g * G * D, G * ROW_BYTES,
-                              &qfull[k & 1]);
-                    ++kq;
+            if (isk) {
+                if (lane == 0) {
+                    ok = wait_or_abort(&qempty[k & 1], ((k >> 1) & 1) ^ 1, flags, a, 100);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&qfull[k & 1], G * ROW_BYTES);
+                        bulk_load(smem + C::OFF_Q + (k & 1) * C::Q_BYTES,
+                                  a.q + (int64_t)cur.b * a.q_row_stride + (int64_t)cur.g * G * D, G * ROW_BYTES,
+                                  &qfull[k & 1]);
+                        ++kq;
+                    }
                 }
+                ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
             }
-            ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
             for (int t = cur.t_begin; ok && t < cur.t_end; ++t, ++it) {
                 const int stage = it % C::STAGES;
                 if (lane == 0) ok = wait_or_abort(&empty[stage], ((it / C::STAGES) & 1) ^ 1, flags, a, 101);
@@ -328,9 +364,8 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                 const int p0 = t * TILE;
                 const int rows = min(TILE, cur.p_end - p0);
                 const int nsub = (rows + a.box_rows - 1) / a.box_rows;
-                if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)nsub * a.box_rows * ROW_BYTES * 2);
-                uint8_t *ks = smem + stage * C::STAGE_BYTES;
-                uint8_t *vs = ks + TILE * ROW_BYTES;
+                if (lane == 0) mbar_arrive_expect_tx(&fullb[stage], (uint32_t)nsub * a.box_rows * ROW_BYTES);
+                uint8_t *dst = smem + stage * C::STAGE_BYTES + (isk ? 0 : TILE * ROW_BYTES);
                 for (int sub = 0; sub < nsub; ++sub) {
                     const int ps = p0 + sub * a.box_rows;
                     const int lb = ps / a.block_size;
@@ -340,13 +375,12 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                     }
                     const int blk = __shfl_sync(FULL, win, lb - wbase);
                     if (lane == 0) {
-                        if (a.checked && (blk < 0 || blk >= a.num_blocks))
+                        if (isk && a.checked && (blk < 0 || blk >= a.num_blocks))
                             record_error(a.err, PA_DEV_BAD_BLOCK, (long long)cur.b * a.max_blocks + lb);
                         long long slot = (long long)blk * a.block_size + ps % a.block_size;
                         // An invalid block id reads as zeros: TMA fills out-of-range boxes.
                         if (blk < 0 || blk >= a.num_blocks) slot = -2LL * a.box_rows;
-                        tma_load_3d(ks + sub * a.box_rows * ROW_BYTES, &tmk, 0, cur.g, (int)slot, &full[stage], pol);
-                        tma_load_3d(vs + sub * a.box_rows * ROW_BYTES, &tmv, 0, cur.g, (int)slot, &full[stage], pol);
+                        tma_load_4d(dst + sub * a.box_rows * ROW_BYTES, tm, 0, (int)slot, 0, cur.g, &fullb[stage], pol);
                     }
                 }
             }
@@ -361,7 +395,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
             // Let the copies already issued land before the CTA's shared memory goes away.
             for (uint32_t j = 0; j < C::STAGES && j < it; ++j) {
                 const uint32_t x = it - 1 - j;
-                (void)mbar_wait(&full[x % C::STAGES], (x / C::STAGES) & 1);
+                (void)mbar_wait(&fullb[x % C::STAGES], (x / C::STAGES) & 1);
             }
             for (uint32_t j = 0; j < 2 && j < kq; ++j) {
                 const uint32_t x = kq - 1 - j;
@@ -378,8 +412,8 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
         Walker w(st);
         Seg sg;
         for (uint32_t k = 0; w.next(ctx_s, a.Hkv, a.batch, sg); ++k) {
-            const bool ok = wait_or_abort(&done[k & 1], (k >> 1) & 1, flags, a, 300);
-            const float *so = slot_base + (k & 1) * C::SLOT_FLOATS;
+            const bool ok = wait_or_abort(&done[k % C::NSLOT], (k / C::NSLOT) & 1, flags, a, 300);
+            const float *so = slot_base + (k % C::NSLOT) * C::SLOT_FLOATS;
             const float *sml = so + C::NCW * G * D;
             float O[G][4], M[G], L[G];
 #pragma unroll
@@ -401,7 +435,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sfree[k & 1]);
+            if (lane == 0) mbar_arrive(&sfree[k % C::NSLOT]);
             if (!ok) continue;
             if (sg.t_begin == 0 && sg.t_end == sg.nt) {  // the whole pair: final output
                 const int64_t bh0 = (int64_t)sg.b * a.Hq + (int64_t)sg.g * G;  // first q-head row of (b, g)
@@ -436,161 +470,138 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     }
 
     // ------------------------------------------------------------------ consumers
+    // Fragment coordinates (m16n8k16): row g4 of A/C is query head g4 of the
+    // group (valid when g4 < G), columns 2*t4, 2*t4+1 (and +8) are keys or
+    // dims.  Each warp owns keys [wig*KPW, wig*KPW + 16) of a tile.
     const int grp = warp / WPG, wig = warp % WPG;
-    const int rg = lane / C::LPT, li = lane % C::LPT;
-    float *sbuf = reinterpret_cast<float *>(smem + C::OFF_S) + warp * TPW * G;  // [TPW][G]
-    const uint32_t sbuf_a = smem_addr(sbuf);
+    const int g4 = lane >> 2, t4 = lane & 3;
+    const bool hvalid = g4 < G;
+    const int mi = lane >> 3, r8 = lane & 7;
+    // Byte offset of key row k inside a K or V tile region: boxes of box_rows
+    // keys, each [2 halves][box_rows][128 B]; 128 B swizzle by (k & 7).
+    const int br = a.box_rows;
+    auto key_off = [&](int kk) -> uint32_t {
+        return (uint32_t)((kk / br) * (br * ROW_BYTES) + (kk % br) * 128);
+    };
+    const uint32_t half_stride = (uint32_t)br * 128;
+    const uint32_t qk_row = key_off(wig * KPW + (mi >> 1) * 8 + r8);  // ldmatrix row of this lane in Q.K
+    const uint32_t pv_row = key_off(wig * KPW + (mi & 1) * 8 + r8);   // ... and in P.V
     float *slot_base = reinterpret_cast<float *>(smem + C::OFF_SLOT);
 
-    float qf[G][C::DPL];
-    float m_run[G], l_run[G], o[G][4];
+    uint32_t qa[8][2];  // A fragments of q: [k step][cols 2*t4.. and 2*t4+8..] of row g4
+    float o[16][4];     // O fragments: [dim tile j] rows g4 (and g4+8, unused), dims 8j + 2*t4, +1
     uint32_t it = 0;
     Walker w(st);
     Seg sg;
     for (uint32_t k = 0; w.next(ctx_s, a.Hkv, a.batch, sg); ++k) {
         if (wait_or_abort(&qfull[k & 1], (k >> 1) & 1, flags, a, 200 + warp)) {
-            const uint32_t qa = smem_addr(smem + C::OFF_Q + (k & 1) * C::Q_BYTES);
+            const uint32_t qrow = smem_addr(smem + C::OFF_Q + (k & 1) * C::Q_BYTES) + g4 * ROW_BYTES + 4 * t4;
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-#pragma unroll
-                for (int part = 0; part < C::DPL / 8; ++part) {
-                    const uint4 w = ld_shared_v4(qa + h * ROW_BYTES + part * 128 + 16 * li);
-                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        qf[h][part * 8 + 2 * e] = bf16lo(ww[e]) * a.scale_log2;
-                        qf[h][part * 8 + 2 * e + 1] = bf16hi(ww[e]) * a.scale_log2;
-                    }
-                }
+            for (int kk = 0; kk < 8; ++kk) {
+                qa[kk][0] = hvalid ? ld_shared_u32(qrow + 32 * kk) : 0u;
+                qa[kk][1] = hvalid ? ld_shared_u32(qrow + 32 * kk + 16) : 0u;
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&qempty[k & 1]);
+        float m_ref = -INFINITY, l_part = 0.f;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            m_run[h] = -INFINITY;
-            l_run[h] = 0.f;
-            o[h][0] = o[h][1] = o[h][2] = o[h][3] = 0.f;
-        }
+        for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+
         for (int t = sg.t_begin; t < sg.t_end; ++t, ++it) {
             if ((int)(it % C::NGRP) != grp) continue;
             const int stage = it % C::STAGES;
-            if (wait_or_abort(&full[stage], (it / C::STAGES) & 1, flags, a, 210 + warp)) {
+            if (wait_or_abort(&kfull[stage], (it / C::STAGES) & 1, flags, a, 210 + warp)) {
                 const uint32_t ks = smem_addr(smem + stage * C::STAGE_BYTES);
-                const uint32_t vsa = ks + TILE * ROW_BYTES;
+                const uint32_t vs = ks + TILE * ROW_BYTES;
                 const int nvalid = min(TILE, sg.p_end - t * TILE);
-                // ---- scores for rows wig*TPW + r*RPR + rg
-                uint4 kw[C::ROUNDS][C::DPL / 8];
+                // ---- S = Q.K^T for this warp's 16 keys: two n-tiles of 8 keys
+                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-                for (int r = 0; r < C::ROUNDS; ++r)
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int chunk = 2 * kk + (mi & 1);  // 16-byte column of the row
+                    const uint32_t ad =
+                        ks + qk_row + (chunk >> 3) * half_stride + ((uint32_t)((chunk & 7) ^ r8) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(ad, b0, b1, b2, b3);
+                    mma16816(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+                    mma16816(sc[1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+                }
+                // ---- online softmax (base 2) with a lazy reference max
+                const int key0 = wig * KPW + 2 * t4;
+                float x[4];
 #pragma unroll
-                    for (int part = 0; part < C::DPL / 8; ++part)
-                        kw[r][part] = ld_shared_v4(ks + (wig * TPW + r * C::RPR + rg) * ROW_BYTES + part * 128 + 16 * li);
+                for (int e = 0; e < 4; ++e) {
+                    const int key = key0 + (e >> 1) * 8 + (e & 1);
+                    x[e] = key < nvalid ? sc[e >> 1][e & 1] * a.scale_log2 : -INFINITY;
+                }
+                float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+                if (__any_sync(FULL, hvalid && mx > m_ref + kLazyRescale)) {
+                    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
+                    const float m_new = fmaxf(m_ref, mx);
+                    const float alpha = m_new == -INFINITY ? 1.f : fast_exp2(m_ref - m_new);
+                    l_part *= alpha;
 #pragma unroll
-                for (int r = 0; r < C::ROUNDS; ++r) {
-                    const int row = wig * TPW + r * C::RPR + rg;
-                    float acc[G];
+                    for (int j = 0; j < 16; ++j) {
+                        o[j][0] *= alpha;
+                        o[j][1] *= alpha;
+                    }
+                    m_ref = m_new;
+                }
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                float p[4];
 #pragma unroll
-                    for (int h = 0; h < G; ++h) acc[h] = 0.f;
-#pragma unroll
-                    for (int part = 0; part < C::DPL / 8; ++part) {
-                        const uint32_t ww[4] = {kw[r][part].x, kw[r][part].y, kw[r][part].z, kw[r][part].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float k0 = bf16lo(ww[e]), k1 = bf16hi(ww[e]);
-#pragma unroll
-                            for (int h = 0; h < G; ++h) {
-                                acc[h] = fmaf(qf[h][part * 8 + 2 * e], k0, acc[h]);
-                                acc[h] = fmaf(qf[h][part * 8 + 2 * e + 1], k1, acc[h]);
-                            }
+                for (int e = 0; e < 4; ++e) p[e] = fast_exp2(x[e] - m_use);
+                l_part += (p[0] + p[1]) + (p[2] + p[3]);
+                const uint32_t pa0 = pack_bf16(p[0], p[1]), pa2 = pack_bf16(p[2], p[3]);
+                // ---- O += P.V once the V tile has landed
+                if (wait_or_abort(&vfull[stage], (it / C::STAGES) & 1, flags, a, 230 + warp)) {
+                    const bool ragged = nvalid < (wig + 1) * KPW;
+                    if (ragged) {
+                        // Rows past the context may hold anything (NaN included): zero
+                        // them so that p = 0 contributes exactly nothing.
+                        for (int c = lane; c < KPW * 16; c += 32) {
+                            const int kk = wig * KPW + (c >> 4);
+                            if (kk >= nvalid)
+                                st_shared_zero16(vs + key_off(kk) + ((c >> 3) & 1) * half_stride + (c & 7) * 16);
                         }
-                    }
-                    float s = reduce_scatter<G, C::LPT>(acc, li);
-                    if (row >= nvalid) s = -INFINITY;
-                    if (li % (C::LPT / G) == 0) sbuf[(r * C::RPR + rg) * G + li / (C::LPT / G)] = s;
-                }
-                __syncwarp();
-                // ---- online softmax over this warp's TPW rows (lanes 16..31 mirror 0..15)
-                float alpha[G];
-                {
-                    const int rr = lane & (TPW - 1);
-                    float sc[G];
-#pragma unroll
-                    for (int h = 0; h < G; ++h) sc[h] = sbuf[rr * G + h];
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        float mx = sc[h];
-#pragma unroll
-                        for (int off = TPW / 2; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
-                        const float m_new = fmaxf(m_run[h], mx);
-                        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                        const float p = fast_exp2(sc[h] - m_use);
-                        alpha[h] = fast_exp2(m_run[h] - m_use);
-                        float ps = p;
-#pragma unroll
-                        for (int off = TPW / 2; off >= 1; off >>= 1) ps += __shfl_xor_sync(FULL, ps, off);
-                        l_run[h] = l_run[h] * alpha[h] + ps;
-                        m_run[h] = m_new;
-                        sc[h] = p;
-                    }
-                    __syncwarp();
-                    if (lane < TPW) {
-#pragma unroll
-                        for (int h = 0; h < G; ++h) sbuf[rr * G + h] = sc[h];
-                    }
-                    __syncwarp();
-                }
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    o[h][0] *= alpha[h];
-                    o[h][1] *= alpha[h];
-                    o[h][2] *= alpha[h];
-                    o[h][3] *= alpha[h];
-                }
-                // ---- P.V over this warp's valid rows
-                const int nv = max(0, min(TPW, nvalid - wig * TPW));
-#pragma unroll 4
-                for (int rr = 0; rr < nv; ++rr) {
-                    const int row = wig * TPW + rr;
-                    const uint2 w = ld_shared_v2(vsa + row * ROW_BYTES + 8 * lane);
-                    const float v0 = bf16lo(w.x), v1 = bf16hi(w.x), v2 = bf16lo(w.y), v3 = bf16hi(w.y);
-                    float p[G];
-                    if constexpr (G == 4) {
-                        const uint4 pp = ld_shared_v4(sbuf_a + rr * G * 4);
-                        p[0] = __uint_as_float(pp.x);
-                        p[1] = __uint_as_float(pp.y);
-                        p[2] = __uint_as_float(pp.z);
-                        p[3] = __uint_as_float(pp.w);
-                    } else {
-#pragma unroll
-                        for (int h = 0; h < G; ++h) p[h] = sbuf[rr * G + h];
+                        __syncwarp();
                     }
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        o[h][0] = fmaf(p[h], v0, o[h][0]);
-                        o[h][1] = fmaf(p[h], v1, o[h][1]);
-                        o[h][2] = fmaf(p[h], v2, o[h][2]);
-                        o[h][3] = fmaf(p[h], v3, o[h][3]);
+                    for (int j = 0; j < 16; j += 2) {
+                        const int chunk = j + (mi >> 1);
+                        const uint32_t ad =
+                            vs + pv_row + (chunk >> 3) * half_stride + ((uint32_t)((chunk & 7) ^ r8) << 4);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(ad, b0, b1, b2, b3);
+                        mma16816(o[j], pa0, 0u, pa2, 0u, b0, b1);
+                        mma16816(o[j + 1], pa0, 0u, pa2, 0u, b2, b3);
                     }
+                    // The zeroed rows are rewritten by the next TMA copy into this
+                    // stage: order the generic-proxy stores before it.
+                    if (ragged) fence_proxy_async_smem();
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
         }
         // ---- publish this warp's (m, l, o) for the merge warp
-        (void)wait_or_abort(&sfree[k & 1], ((k >> 1) & 1) ^ 1, flags, a, 220 + warp);
-        float *so = slot_base + (k & 1) * C::SLOT_FLOATS;
+        l_part += __shfl_xor_sync(FULL, l_part, 1);
+        l_part += __shfl_xor_sync(FULL, l_part, 2);
+        (void)wait_or_abort(&sfree[k % C::NSLOT], ((k / C::NSLOT) & 1) ^ 1, flags, a, 220 + warp);
+        float *so = slot_base + (k % C::NSLOT) * C::SLOT_FLOATS;
+        if (hvalid) {
+            float *row = so + (warp * G + g4) * D + 2 * t4;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            *reinterpret_cast<float4 *>(so + (warp * G + h) * D + 4 * lane) =
-                make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-            if (lane == 0) {
-                so[C::NCW * G * D + (warp * G + h) * 2] = m_run[h];
-                so[C::NCW * G * D + (warp * G + h) * 2 + 1] = l_run[h];
+            for (int j = 0; j < 16; ++j) *reinterpret_cast<float2 *>(row + 8 * j) = make_float2(o[j][0], o[j][1]);
+            if (t4 == 0) {
+                so[C::NCW * G * D + (warp * G + g4) * 2] = m_ref;
+                so[C::NCW * G * D + (warp * G + g4) * 2 + 1] = l_part;
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&done[k & 1]);
+        if (lane == 0) mbar_arrive(&done[k % C::NSLOT]);
     }
 }
 
@@ -726,9 +737,9 @@ pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *
     int box = 64;
     while (block_size % box) box >>= 1;  // gcd(block_size, 64) in {16, 32, 64}
     CUtensorMap tk, tv;
-    pa_status st = encode_kv_tensor_map(&tk, k_cache, (int64_t)num_blocks * block_size, num_kv_heads, D, box);
+    pa_status st = encode_kv_tensor_map_halves(&tk, k_cache, (int64_t)num_blocks * block_size, num_kv_heads, box);
     if (st != PA_OK) return st;
-    st = encode_kv_tensor_map(&tv, v_cache, (int64_t)num_blocks * block_size, num_kv_heads, D, box);
+    st = encode_kv_tensor_map_halves(&tv, v_cache, (int64_t)num_blocks * block_size, num_kv_heads, box);
     if (st != PA_OK) return st;
 
     DecodeArgs A;

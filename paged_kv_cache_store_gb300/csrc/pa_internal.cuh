@@ -112,6 +112,16 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                            uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar)),
+        "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -191,10 +201,13 @@ int sm_count();
 // Whether checked mode is on.
 bool checked_mode();
 
-// Encodes a 3-D bf16 tensor map over a KV pool viewed as
-// [num_slots][num_kv_heads][head_dim] with box {head_dim, 1, box_rows}.
-pa_status encode_kv_tensor_map(CUtensorMap *map, const void *base, int64_t num_slots,
-                               int32_t num_kv_heads, int32_t head_dim, int32_t box_rows);
+// Encodes a 4-D bf16 tensor map over a KV pool [num_slots][num_kv_heads][128]
+// viewed as [kv head][half][slot][64] (the strides need not grow with the
+// dimension), with box {64, box_rows, 2, 1} and 128-byte swizzle: a box of
+// box_rows rows of one kv head lands as [2 halves][box_rows][128 B], so 8
+// consecutive rows at one 16-byte column fall in 8 different banks.
+pa_status encode_kv_tensor_map_halves(CUtensorMap *map, const void *base, int64_t num_slots,
+                                      int32_t num_kv_heads, int32_t box_rows);
 // General 3-D bf16 tensor map: dims {dim0, dim1, dim2} (dim0 contiguous),
 // byte strides of dims 1 and 2, box {box0, 1, box2}, optional 128-byte swizzle.
 pa_status encode_tensor_map_3d(CUtensorMap *map, const void *base, int64_t dim0, int64_t dim1, int64_t dim2,
