@@ -154,7 +154,7 @@ PA_API pa_status pa_slot_mapping_prefill(int32_t *slot_mapping, const int32_t *b
 /*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs.
  * It depends only on the GQA group (num_q_heads / num_kv_heads) and is at
- * most about 2.1 MB; 0 for shapes pa_decode does not support.
+ * most about 6.4 MB; 0 for shapes pa_decode does not support.
  */
 PA_API size_t pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim);
 
@@ -168,9 +168,12 @@ PA_API size_t pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads
  * where slot(b,p) = block_tables[b][p/B]*B + p%B.  The query is the token at
  * position ctx-1 and sees all ctx keys, including its own (store it first).
  * ctx == 0 writes zeros and reads nothing.  The tiles of all (sequence, kv
- * head) pairs are cut into equal contiguous ranges, one per CTA; a pair cut
- * between CTAs is combined by a second kernel on the same stream
- * (log-sum-exp of the per-CTA online-softmax partials).
+ * head) pairs are cut into contiguous ranges (one per CTA, then small chunks
+ * taken dynamically); a pair cut between ranges is combined in the same
+ * kernel by the CTA that finishes its last part (log-sum-exp of the
+ * online-softmax partials).  The kernel is launched as a programmatic
+ * dependent launch and reads its inputs only after the preceding work on
+ * the stream has completed.
  *
  *   out                bf16 [batch, Hq, D] contiguous.
  *   q                  bf16; row b (Hq*D contiguous values) at q + b*q_row_stride.
@@ -179,9 +182,12 @@ PA_API size_t pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads
  *   context_lens       int32 [batch], each in [0, max_blocks_per_seq*block_size].
  *   softmax_scale      usually 1/sqrt(head_dim).
  *   workspace          device scratch of >= pa_decode_workspace_size(...)
- *                      bytes, 16-byte aligned (fp32 split partials and merge
- *                      tasks; no initialisation needed).  One workspace must
- *                      not be used by two calls that may run at the same time.
+ *                      bytes, 16-byte aligned, ZERO-FILLED before its first
+ *                      use (fp32 split partials and work counters).  Every
+ *                      call leaves it zero-filled again, so one memset at
+ *                      allocation is enough; after a call that recorded a
+ *                      device error, zero it again.  One workspace must not be
+ *                      used by two calls that may run at the same time.
  * batch == 0 is a no-op; batch <= 2048.
  */
 PA_API pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *k_cache,
@@ -199,10 +205,10 @@ PA_API pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const
  * cannot call cudaMalloc or an allocating library: code running inside
  * another framework's memory pool, plugins that must not touch the
  * allocator, or hosts that forbid device allocation after start-up.  This
- * entry point allocates nothing.  The split partials go to a 4 MiB scratch
- * array compiled into the library, which holds the workspace of every
- * supported shape; every GPU that loads the library holds those 4 MiB until
- * the process exits.
+ * entry point allocates nothing.  The split partials go to an 8 MiB scratch
+ * array compiled into the library (zero-filled at load, as the workspace
+ * contract asks), which holds the workspace of every supported shape; every
+ * GPU that loads the library holds those 8 MiB until the process exits.
  *   - The first call on a device (with that device current) looks up the
  *     array's device address; make that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents.

@@ -162,10 +162,11 @@ def decode_workspace_size(num_q_heads, num_kv_heads, head_dim) -> int:
 
 
 def decode_workspace(num_q_heads, num_kv_heads, head_dim, device="cuda"):
-    """Allocate (with torch) a workspace for pa_decode (about 2 MB at most;
-    it depends only on the GQA group)."""
+    """Allocate (with torch) a zero-filled workspace for pa_decode (at most
+    about 6.4 MB; it depends only on the GQA group).  pa_decode leaves it
+    zeroed, so it can be reused by any number of calls on one stream."""
     n = decode_workspace_size(num_q_heads, num_kv_heads, head_dim)
-    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, workspace=None, out=None,
@@ -198,7 +199,7 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, 
 
 def decode_static(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, out=None, stream=None):
     """pa_decode without a workspace: for callers that must not allocate device
-    memory.  The split scratch is a 4 MiB array built into the library (shared
+    memory.  The split scratch is an 8 MiB array built into the library (shared
     by all calls, so calls that may overlap on the GPU must be serialised).
     Only `out` is allocated here, and only when the caller passes none."""
     _need(q, torch.bfloat16, "q")

@@ -6,22 +6,23 @@
 // p < context_lens[b], slot(b,p) = block_tables[b][p/B]*B + p%B [PA3 §3].
 //
 // How (GB300 design):
-//  * The work is a flat list of 64-position tiles ordered (sequence, kv head,
-//    tile).  A persistent grid of one CTA per SM cuts that list into equal
-//    contiguous ranges, so every CTA streams the same number of tiles and
-//    walks only a few (sequence, kv head) segments: a range holds whole
-//    segments in its middle and at most one part-segment at each end.
-//    Every CTA rebuilds the per-sequence tile counts from context_lens in
-//    shared memory and finds its first tile with a warp scan.
+//  * Work is a flat list of 64-position tiles ordered (sequence, kv head,
+//    tile).  Its first 7/8 is cut into one contiguous range per CTA of a
+//    persistent grid (one CTA per SM); the last 1/8 into small chunk ranges
+//    that CTAs take from an atomic counter once their own range is done, so
+//    the CTAs that stream faster absorb the tail.  A range holds whole
+//    (sequence, kv head) segments in its middle and at most one part-segment
+//    at each end.  Every CTA rebuilds the per-sequence tile counts and their
+//    prefix sum from context_lens in shared memory.
 //  * Two producer warps issue TMA tile loads (cp.async.bulk.tensor, 64 rows x
 //    256 B per K or V tile; a row is one token of one kv head) into a
 //    4-stage shared-memory ring guarded by mbarriers: one warp the K tiles
 //    and the segment's G query rows (a bulk copy), the other the V tiles.
-//    Split this way, each warp's issue latency (mbarrier and TMA operations
-//    queue behind the consumers' shared-memory traffic) is paid in parallel.
-//    Tiles never straddle a block: the TMA box is gcd(B, 64) rows, and each
-//    box is addressed through the block table, whose entries the producers'
-//    lanes prefetch 32 at a time.
+//    Split this way, each warp's issue latency is paid in parallel.  The K
+//    warp also takes the chunk ranges and hands each range to the other
+//    warps through a small ring of tickets.  Tiles never straddle a block:
+//    the TMA box is gcd(B, 64) rows, and each box is addressed through the
+//    block table, whose entries the producers' lanes prefetch 32 at a time.
 //  * K and V tiles land 128-byte swizzled, split into the two 64-dim halves
 //    of each row ([half][row][64]; the tensor map views a pool as
 //    [kv head][half][slot][64]), so that 8 consecutive rows at one 16-byte
@@ -38,10 +39,13 @@
 //    the running max only moves (rescaling O and l) when a score exceeds it
 //    by more than 2^8, which a warp vote detects.
 //  * Segment end: a merge warp combines the consumer warps' states.  A whole
-//    segment writes bf16 output directly; a part-segment writes its (m, l, o)
-//    partial to the workspace, and the CTA where the segment's sequence/head
-//    pair starts records a merge task.  A small merge kernel, queued behind
-//    this one with programmatic dependent launch, runs the tasks.
+//    segment writes bf16 output directly.  A part-segment writes its (m, l, o)
+//    partial to the workspace and counts itself on the pair's arrival
+//    counter; the CTA whose count completes the pair merges the parts
+//    (log-sum-exp) and resets the counter.
+//  * Every global read or write comes after griddepcontrol.wait, so the
+//    kernel can be launched early behind the kernel that produces its inputs
+//    (programmatic dependent launch).
 //  * All waits are bounded; a timeout records PA_DEV_TIMEOUT and the warps
 //    finish their loops without waiting, keeping every barrier paired.
 #include <math.h>
@@ -62,6 +66,9 @@ constexpr int KPW = TILE / WPG;   // keys per consumer warp per tile (one MMA n-
 constexpr float kLazyRescale = 8.f;  // log2 headroom before the running max must move
 constexpr int kMaxBatch = 2048;
 constexpr int kMaxGrid = 256;     // CTAs of the persistent grid (min(SMs, this))
+constexpr int kMaxRanges = 2 * kMaxGrid;  // a head and a tail range per CTA
+constexpr int kTailShift = 3;  // a CTA's tail range is 1/8 of its share
+constexpr int NTK = 4;            // tickets in flight (ranges handed from the K warp to the others)
 constexpr unsigned FULL = 0xffffffffu;
 
 template <int G>
@@ -71,12 +78,18 @@ struct Cfg {
     static constexpr int PRODUCER_K = NCW;         // warp that issues the K tile (and q) copies
     static constexpr int PRODUCER_V = NCW + 1;     // warp that issues the V tile copies
     static constexpr int MERGER = NCW + 2;         // warp that finishes segments
-    static constexpr int NTHREADS = (NCW + 3) * 32;
-    // Stage s only ever holds tiles of group s % NGRP, so each full/empty
-    // barrier has waiters of one group only and a parity wait can never see a
-    // phase two steps old (another group's pending copy) as its own.
+    static constexpr int NWARPS = NCW + 3;
+    static constexpr int NTHREADS = NWARPS * 32;
+    // Tile x of the flat list goes to consumer group x % NGRP, so the split of
+    // a segment between the groups (and the summation order) does not depend
+    // on which CTA runs it.  Group g uses stages g, g + NGRP, ... in turn,
+    // counted by its own tile counter; each full/empty barrier therefore has
+    // waiters of one group only and a parity wait can never see a phase two
+    // steps old as its own.
     static constexpr int STAGES = 4;
     static_assert(STAGES % NGRP == 0, "a stage must belong to a single consumer group");
+    static constexpr int SPG = STAGES / NGRP;  // stages per group
+    static_assert(NGRP == 2, "the producers keep one tile counter per group");
     static constexpr int NSLOT = 2;  // merge slots (consumer warps -> merge warp), used round-robin
     static constexpr int STAGE_BYTES = 2 * TILE * ROW_BYTES;
     static constexpr int Q_BYTES = G * ROW_BYTES;
@@ -84,11 +97,14 @@ struct Cfg {
     static constexpr int OFF_Q = STAGES * STAGE_BYTES;          // q slots [2][G][D] bf16
     static constexpr int OFF_SLOT = OFF_Q + 2 * Q_BYTES;        // merge slots [NSLOT][SLOT_FLOATS] f32
     static constexpr int OFF_BAR = OFF_SLOT + NSLOT * SLOT_FLOATS * 4;
-    static constexpr int NBAR = 3 * STAGES + 8;  // kfull, vfull, empty, qfull[2], qempty[2], done[2], free[2]
-    static constexpr int OFF_FLAGS = OFF_BAR + NBAR * 8;  // [0]: abort
-    static constexpr int OFF_START = OFF_FLAGS + 16;      // RangeStart
-    static constexpr int OFF_CTX = OFF_START + 64;        // clamped context_lens [batch] int
-    static constexpr size_t smem_bytes(int batch) { return OFF_CTX + 4 * (size_t)batch + 1024; }
+    // kfull, vfull, empty [STAGES]; qfull, qempty, done, sfree [2]; tfull, tempty [NTK]
+    static constexpr int NBAR = 3 * STAGES + 8 + 2 * NTK;
+    static constexpr int OFF_FLAGS = OFF_BAR + NBAR * 8;   // [0]: abort
+    static constexpr int OFF_TK = OFF_FLAGS + 16;          // Ticket [NTK]
+    static constexpr int OFF_WSUM = OFF_TK + NTK * 32;     // scan scratch [NWARPS] uint32
+    static constexpr int OFF_CUM = OFF_WSUM + 64;          // per-head tile prefix sum [batch + 1] uint32
+    __host__ __device__ static constexpr size_t off_ctx(int batch) { return OFF_CUM + 4 * (size_t)(batch + 1); }  // [batch] int
+    __host__ __device__ static constexpr size_t smem_bytes(int batch) { return off_ctx(batch) + 4 * (size_t)batch + 1024; }
     static_assert(smem_bytes(kMaxBatch) <= 232448, "shared memory budget");
 };
 
@@ -102,9 +118,10 @@ struct DecodeArgs {
     int32_t batch, Hq, Hkv, block_size, box_rows, num_blocks;
     float scale_log2;
     int32_t ctx_limit;  // max_blocks * block_size
-    float *ws_o;        // [2 * kMaxGrid][G][D]     partials: slot 2j is CTA j's first segment, 2j+1 its last
-    float2 *ws_ml;      // [2 * kMaxGrid][G]        (m, l) in base 2
-    int4 *ws_task;      // [kMaxGrid]               {b, g, nsplit, first slot} of the pair that starts in CTA j
+    float *ws_o;        // [2 * kMaxRanges][G][D]  partials: slot 2r is range r's first segment, 2r+1 its last
+    float2 *ws_ml;      // [2 * kMaxRanges][G]     (m, l) in base 2
+    int *ws_cnt;        // [kMaxRanges]            arrivals of the parts of the pair that starts in range r
+    int *ws_ctr;        // [2]                     chunk ranges taken, CTAs done taking
     DevError *err;
     int32_t checked;
 };
@@ -119,30 +136,58 @@ __device__ __forceinline__ int clamp_ctx(const DecodeArgs &a, int b, bool report
 }
 
 // The tiles of pair (b, g) are [Hkv*CT_b + g*nt_b, ... + nt_b) in the flat
-// list, nt_b = ceil(ctx_b / TILE), CT_b = sum_{b' < b} nt_b'.  CTA j owns
-// `base + (j < rem)` tiles starting at j*base + min(j, rem).
-struct RangeStart {
-    int b, g, t, pad;
-    long long pos, len, base, rem;
+// list, nt_b = ceil(ctx_b / TILE), CT_b = sum_{b' < b} nt_b'.  CTA j's share
+// is base + (j < rem) tiles from j*base + min(j, rem); its last 1/8 (the
+// tail) is a separate range that any CTA may take from the tail counter once
+// its own head range is done.  Range 2j is CTA j's head, 2j+1 its tail, so
+// range indices follow the flat order (a range may be empty).
+struct Split {
+    long long base, rem;
+    int grid;
+    __device__ void init(long long total, int grid_) {
+        grid = grid_;
+        base = total / grid;
+        rem = total % grid;
+    }
+    __device__ long long cta_start(int j) const { return (long long)j * base + min((long long)j, rem); }
+    __device__ long long cta_len(int j) const { return base + (j < rem ? 1 : 0); }
+    __device__ long long tail_len(int j) const { return cta_len(j) >> kTailShift; }
+    __device__ long long start(int r) const {
+        const int j = r >> 1;
+        return cta_start(j) + ((r & 1) ? cta_len(j) - tail_len(j) : 0);
+    }
+    __device__ long long len(int r) const {
+        const int j = r >> 1;
+        return (r & 1) ? tail_len(j) : cta_len(j) - tail_len(j);
+    }
+    __device__ int owner(long long x) const {  // the (non-empty) range holding tile x
+        const long long cut = rem * (base + 1);
+        const int j = (int)(x < cut ? x / (base + 1) : rem + (x - cut) / base);
+        return 2 * j + (x >= cta_start(j) + cta_len(j) - tail_len(j) ? 1 : 0);
+    }
 };
 
-__device__ __forceinline__ long long owner_cta(long long x, long long base, long long rem) {
-    const long long cut = rem * (base + 1);
-    return x < cut ? x / (base + 1) : rem + (x - cut) / base;
-}
+// A range handed from the K producer warp to the other warps.
+struct Ticket {
+    long long pos;  // flat index of the first tile
+    int len;        // tiles; 0 ends the CTA's work
+    int r;          // range index
+    int b, g, t;    // (sequence, kv head, tile) of tile pos
+    int pad;
+};
 
-// One (sequence, kv head) part of a CTA's range.
+// One (sequence, kv head) part of a range.
 struct Seg {
     int b, g, t_begin, t_end, nt, p_begin, p_end;
     long long pos;  // flat index of tile t_begin
 };
 
-// Walks a CTA's range segment by segment.  Every role of the CTA runs its
-// own copy and sees the same sequence of segments.
+// Walks a range segment by segment.  Every role of the CTA runs its own copy
+// and sees the same sequence of segments.
 struct Walker {
     int b, g, t;
     long long pos, left;
-    __device__ explicit Walker(const RangeStart &st) : b(st.b), g(st.g), t(st.t), pos(st.pos), left(st.len) {}
+    __device__ explicit Walker(const Ticket &k) : b(k.b), g(k.g), t(k.t), pos(k.pos), left(k.len) {}
     __device__ bool next(const int *ctx_s, int Hkv, int batch, Seg &s) {
         if (left <= 0) return false;
         const int ctx = ctx_s[b];
@@ -224,8 +269,10 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     // Align to 1 KiB by pointer arithmetic on the __shared__ array, so every
     // pointer below stays in the shared address space (ld/st.shared).
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    int *ctx_s = reinterpret_cast<int *>(smem + C::OFF_CTX);
-    RangeStart *rs = reinterpret_cast<RangeStart *>(smem + C::OFF_START);
+    uint32_t *cum = reinterpret_cast<uint32_t *>(smem + C::OFF_CUM);
+    int *ctx_s = reinterpret_cast<int *>(smem + C::off_ctx(a.batch));
+    uint32_t *wsum = reinterpret_cast<uint32_t *>(smem + C::OFF_WSUM);
+    Ticket *tks = reinterpret_cast<Ticket *>(smem + C::OFF_TK);
     uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *vfull = kfull + C::STAGES;
     uint64_t *empty = vfull + C::STAGES;
@@ -233,6 +280,8 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     uint64_t *qempty = qfull + 2;
     uint64_t *done = qempty + 2;
     uint64_t *sfree = done + 2;
+    uint64_t *tfull = sfree + 2;
+    uint64_t *tempty = tfull + NTK;
     volatile int *flags = reinterpret_cast<volatile int *>(smem + C::OFF_FLAGS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -248,60 +297,49 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
             mbar_init(&done[k], C::NCW);
             mbar_init(&sfree[k], 1);
         }
+        for (int k = 0; k < NTK; ++k) {
+            mbar_init(&tfull[k], 1);
+            mbar_init(&tempty[k], C::NWARPS - 1);  // every warp but the K producer reads a ticket
+        }
         flags[0] = 0;
         fence_mbar_init();
     }
     if (warp == C::PRODUCER_K && lane == 0) prefetch_tensormap(&tmk);
     if (warp == C::PRODUCER_V && lane == 0) prefetch_tensormap(&tmv);
-    // Per-sequence tile counts, the total, and this CTA's range.
-    if (warp == 0) {
-        long long total = 0;
-        for (int base = 0; base < a.batch; base += 32) {
-            const int b = base + lane;
-            int nt = 0;
-            if (b < a.batch) {
-                const int ctx = clamp_ctx(a, b, blockIdx.x == 0);
-                ctx_s[b] = ctx;
-                nt = (ctx + TILE - 1) / TILE;
-            }
+    // Inputs may come from the kernel this one was launched behind.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // Per-sequence tile counts and their exclusive prefix sum: each thread
+    // takes a run of `per` sequences, then a block-wide scan of the run sums.
+    {
+        const int per = (a.batch + C::NTHREADS - 1) / C::NTHREADS;
+        const int b0 = threadIdx.x * per, b1 = min(a.batch, b0 + per);
+        uint32_t run = 0;
+        for (int b = b0; b < b1; ++b) {
+            const int ctx = clamp_ctx(a, b, blockIdx.x == 0);
+            ctx_s[b] = ctx;
+            run += (uint32_t)((ctx + TILE - 1) / TILE);
+        }
+        uint32_t x = run;
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) nt += __shfl_xor_sync(FULL, nt, o);
-            total += nt;
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(FULL, x, o);
+            if (lane >= o) x += y;
         }
-        __syncwarp();
-        const long long T = total * a.Hkv;
-        const long long j = blockIdx.x, base = T / gridDim.x, rem = T % gridDim.x;
-        const long long start = j * base + min(j, rem), len = base + (j < rem ? 1 : 0);
-        if (lane == 0) {
-            rs->pos = start;
-            rs->len = len;
-            rs->base = base;
-            rs->rem = rem;
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        uint32_t before = 0;
+        for (int w2 = 0; w2 < warp; ++w2) before += wsum[w2];
+        uint32_t excl = before + x - run;
+        for (int b = b0; b < b1; ++b) {
+            cum[b] = excl;
+            excl += (uint32_t)((ctx_s[b] + TILE - 1) / TILE);
         }
-        // Find the pair holding tile `start`: a scan of the tile counts.
-        long long run = 0;
-        for (int cb = 0; len > 0 && cb < a.batch; cb += 32) {
-            const int b = cb + lane;
-            const int nt = b < a.batch ? (ctx_s[b] + TILE - 1) / TILE : 0;
-            int x = nt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(FULL, x, o);
-                if (lane >= o) x += y;
-            }
-            const long long lo = run + (long long)(x - nt) * a.Hkv;
-            const bool hit = nt > 0 && lo <= start && start < lo + (long long)nt * a.Hkv;
-            if (hit) {
-                const long long off = start - lo;
-                rs->b = b;
-                rs->g = (int)(off / nt);
-                rs->t = (int)(off % nt);
-            }
-            if (__any_sync(FULL, hit)) break;
-            run += (long long)__shfl_sync(FULL, x, 31) * a.Hkv;
-        }
+        if (threadIdx.x == C::NTHREADS - 1) cum[a.batch] = before + x;
     }
     __syncthreads();
+    Split sp;
+    sp.init((long long)cum[a.batch] * a.Hkv, gridDim.x);
     // Sequences with no context produce zeros.
     if (warp < C::NCW) {
         for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
@@ -310,10 +348,16 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
             for (int j = threadIdx.x; j < a.Hq * D / 8; j += C::NCW * 32) o[j] = make_uint4(0, 0, 0, 0);
         }
     }
-    // The split-merge kernel queued behind this grid may be scheduled now; it
-    // waits (griddepcontrol.wait) until this grid's results are visible.
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const RangeStart st = *rs;
+
+    // Ticket i is read by every warp but the K producer; parities follow i / NTK.
+    auto take_ticket = [&](uint32_t i, Ticket &k) -> bool {
+        const bool ok = wait_or_abort(&tfull[i % NTK], (i / NTK) & 1, flags, a, 400 + warp);
+        k = tks[i % NTK];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[i % NTK]);
+        return ok && k.len > 0;
+    };
 
     // ------------------------------------------------------------------ producers
     // Two warps on different SM sub-partitions: one issues the K tiles (and
@@ -325,77 +369,156 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
         const bool isk = warp == C::PRODUCER_K;
         const CUtensorMap *tm = isk ? &tmk : &tmv;
         uint64_t *fullb = isk ? kfull : vfull;
-        // Lane l holds the block id of logical block wbase + l of the current
-        // segment's sequence; the next segment's first window is fetched while
-        // the current one is issued.
-        auto fetch = [&](const Seg &s, int lb) -> int {
-            const int nblk = (s.p_end - 1) / a.block_size + 1;  // logical blocks of the sequence in use
-            return lb + lane < nblk ? __ldg(a.block_tables + (int64_t)s.b * a.max_blocks + lb + lane) : -1;
-        };
         const uint64_t pol = policy_evict_first();
-        Walker w(st);
-        Seg cur, nxt;
-        bool have = w.next(ctx_s, a.Hkv, a.batch, cur);
-        int wbase = have ? cur.p_begin / a.block_size : 0;
-        int win = have ? fetch(cur, wbase) : -1;
-        bool have_n = have && w.next(ctx_s, a.Hkv, a.batch, nxt);
-        int win_n = have_n ? fetch(nxt, nxt.p_begin / a.block_size) : -1;
-        uint32_t it = 0, k = 0, kq = 0;  // tiles issued, segments seen, query copies issued
+        uint32_t n0 = 0, n1 = 0, k = 0, kq = 0, ti = 0;  // tiles issued per group, segments, q copies, tickets
         bool ok = true;
-        for (; ok && have; ++k) {
+        // The K warp's lane 0 picks the ranges: its own head range, then tail
+        // ranges from the counter.  The next tail is taken two tiles before
+        // the current range ends, so the atomic's latency is hidden.
+        int next_tail = -1;
+        bool taken = false;
+        bool first = true;
+        while (ok) {
+            Ticket tk;
             if (isk) {
+                int r = -1;
                 if (lane == 0) {
-                    ok = wait_or_abort(&qempty[k & 1], ((k >> 1) & 1) ^ 1, flags, a, 100);
+                    if (first && sp.len(2 * (int)blockIdx.x) > 0) {
+                        r = 2 * (int)blockIdx.x;
+                    } else {
+                        if (!taken) next_tail = atomicAdd(&a.ws_ctr[0], 1);
+                        taken = false;
+                        while (next_tail < sp.grid && sp.len(2 * next_tail + 1) == 0)
+                            next_tail = atomicAdd(&a.ws_ctr[0], 1);
+                        if (next_tail < sp.grid) r = 2 * next_tail + 1;
+                    }
+                    tk.len = 0;
+                    tk.r = r;
+                    if (r >= 0) {
+                        tk.pos = sp.start(r);
+                        tk.len = (int)sp.len(r);
+                        // Locate tile pos: the last sequence with Hkv * cum[b] <= pos.
+                        const uint32_t qv = (uint32_t)(tk.pos / a.Hkv);
+                        int lo = 0, hi = a.batch - 1;
+                        while (lo < hi) {
+                            const int mid = (lo + hi + 1) >> 1;
+                            if (cum[mid] <= qv) lo = mid; else hi = mid - 1;
+                        }
+                        const long long off = tk.pos - (long long)a.Hkv * cum[lo];
+                        const int nt = (int)(cum[lo + 1] - cum[lo]);
+                        tk.b = lo;
+                        tk.g = (int)(off / nt);
+                        tk.t = (int)(off % nt);
+                    }
+                    ok = wait_or_abort(&tempty[ti % NTK], ((ti / NTK) & 1) ^ 1, flags, a, 102);
                     if (ok) {
-                        mbar_arrive_expect_tx(&qfull[k & 1], G * ROW_BYTES);
-                        bulk_load(smem + C::OFF_Q + (k & 1) * C::Q_BYTES,
-                                  a.q + (int64_t)cur.b * a.q_row_stride + (int64_t)cur.g * G * D, G * ROW_BYTES,
-                                  &qfull[k & 1]);
-                        ++kq;
+                        tks[ti % NTK] = tk;
+                        mbar_arrive(&tfull[ti % NTK]);  // release: the ticket is visible to its readers
                     }
                 }
+                first = false;
+                ++ti;
                 ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+                tk.len = __shfl_sync(FULL, tk.len, 0);
+                tk.pos = __shfl_sync(FULL, tk.pos, 0);
+                tk.b = __shfl_sync(FULL, tk.b, 0);
+                tk.g = __shfl_sync(FULL, tk.g, 0);
+                tk.t = __shfl_sync(FULL, tk.t, 0);
+                if (!ok || tk.len <= 0) break;
+            } else {
+                const bool got = take_ticket(ti++, tk);
+                if (!got) break;
             }
-            for (int t = cur.t_begin; ok && t < cur.t_end; ++t, ++it) {
-                const int stage = it % C::STAGES;
-                if (lane == 0) ok = wait_or_abort(&empty[stage], ((it / C::STAGES) & 1) ^ 1, flags, a, 101);
-                ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
-                if (!ok) break;
-                const int p0 = t * TILE;
-                const int rows = min(TILE, cur.p_end - p0);
-                const int nsub = (rows + a.box_rows - 1) / a.box_rows;
-                if (lane == 0) mbar_arrive_expect_tx(&fullb[stage], (uint32_t)nsub * a.box_rows * ROW_BYTES);
-                uint8_t *dst = smem + stage * C::STAGE_BYTES + (isk ? 0 : TILE * ROW_BYTES);
-                for (int sub = 0; sub < nsub; ++sub) {
-                    const int ps = p0 + sub * a.box_rows;
-                    const int lb = ps / a.block_size;
-                    if (lb - wbase >= 32) {  // warp-uniform; only sequences with > 32 blocks in a segment
-                        wbase = lb;
-                        win = fetch(cur, lb);
-                    }
-                    const int blk = __shfl_sync(FULL, win, lb - wbase);
+            // Lane l holds the block id of logical block wbase + l of the current
+            // segment's sequence; the next segment's first window is fetched while
+            // the current one is issued.
+            auto fetch = [&](const Seg &s, int lb) -> int {
+                const int nblk = (s.p_end - 1) / a.block_size + 1;  // logical blocks of the sequence in use
+                return lb + lane < nblk ? __ldg(a.block_tables + (int64_t)s.b * a.max_blocks + lb + lane) : -1;
+            };
+            Walker w(tk);
+            int range_left = tk.len;  // tiles of this range not yet issued
+            Seg cur, nxt;
+            bool have = w.next(ctx_s, a.Hkv, a.batch, cur);
+            int wbase = have ? cur.p_begin / a.block_size : 0;
+            int win = have ? fetch(cur, wbase) : -1;
+            bool have_n = have && w.next(ctx_s, a.Hkv, a.batch, nxt);
+            int win_n = have_n ? fetch(nxt, nxt.p_begin / a.block_size) : -1;
+            for (; ok && have; ++k) {
+                if (isk) {
                     if (lane == 0) {
-                        if (isk && a.checked && (blk < 0 || blk >= a.num_blocks))
-                            record_error(a.err, PA_DEV_BAD_BLOCK, (long long)cur.b * a.max_blocks + lb);
-                        long long slot = (long long)blk * a.block_size + ps % a.block_size;
-                        // An invalid block id reads as zeros: TMA fills out-of-range boxes.
-                        if (blk < 0 || blk >= a.num_blocks) slot = -2LL * a.box_rows;
-                        tma_load_4d(dst + sub * a.box_rows * ROW_BYTES, tm, 0, (int)slot, 0, cur.g, &fullb[stage], pol);
+                        ok = wait_or_abort(&qempty[k & 1], ((k >> 1) & 1) ^ 1, flags, a, 100);
+                        if (ok) {
+                            mbar_arrive_expect_tx(&qfull[k & 1], G * ROW_BYTES);
+                            bulk_load(smem + C::OFF_Q + (k & 1) * C::Q_BYTES,
+                                      a.q + (int64_t)cur.b * a.q_row_stride + (int64_t)cur.g * G * D,
+                                      G * ROW_BYTES, &qfull[k & 1]);
+                            ++kq;
+                        }
+                    }
+                    ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+                }
+                for (int t = cur.t_begin; ok && t < cur.t_end; ++t) {
+                    const int tg = (int)((cur.pos + (t - cur.t_begin)) % C::NGRP);  // consumer group of the tile
+                    const uint32_t n = tg ? n1++ : n0++;
+                    const int stage = tg + C::NGRP * (int)(n % C::SPG);
+                    if (lane == 0) ok = wait_or_abort(&empty[stage], ((n / C::SPG) & 1) ^ 1, flags, a, 101);
+                    ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+                    if (!ok) break;
+                    if (isk && lane == 0 && !taken && range_left <= 2) {
+                        next_tail = atomicAdd(&a.ws_ctr[0], 1);
+                        taken = true;
+                    }
+                    --range_left;
+                    const int p0 = t * TILE;
+                    const int rows = min(TILE, cur.p_end - p0);
+                    const int nsub = (rows + a.box_rows - 1) / a.box_rows;
+                    if (lane == 0) mbar_arrive_expect_tx(&fullb[stage], (uint32_t)nsub * a.box_rows * ROW_BYTES);
+                    uint8_t *dst = smem + stage * C::STAGE_BYTES + (isk ? 0 : TILE * ROW_BYTES);
+                    for (int sub = 0; sub < nsub; ++sub) {
+                        const int ps = p0 + sub * a.box_rows;
+                        const int lb = ps / a.block_size;
+                        if (lb - wbase >= 32) {  // warp-uniform; only sequences with > 32 blocks in a segment
+                            wbase = lb;
+                            win = fetch(cur, lb);
+                        }
+                        const int blk = __shfl_sync(FULL, win, lb - wbase);
+                        if (lane == 0) {
+                            if (isk && a.checked && (blk < 0 || blk >= a.num_blocks))
+                                record_error(a.err, PA_DEV_BAD_BLOCK, (long long)cur.b * a.max_blocks + lb);
+                            long long slot = (long long)blk * a.block_size + ps % a.block_size;
+                            // An invalid block id reads as zeros: TMA fills out-of-range boxes.
+                            if (blk < 0 || blk >= a.num_blocks) slot = -2LL * a.box_rows;
+                            tma_load_4d(dst + sub * a.box_rows * ROW_BYTES, tm, 0, (int)slot, 0, cur.g, &fullb[stage],
+                                        pol);
+                        }
                     }
                 }
+                cur = nxt;
+                have = have_n;
+                win = win_n;
+                wbase = have ? cur.p_begin / a.block_size : 0;
+                have_n = have && w.next(ctx_s, a.Hkv, a.batch, nxt);
+                win_n = have_n ? fetch(nxt, nxt.p_begin / a.block_size) : -1;
             }
-            cur = nxt;
-            have = have_n;
-            win = win_n;
-            wbase = have ? cur.p_begin / a.block_size : 0;
-            have_n = have && w.next(ctx_s, a.Hkv, a.batch, nxt);
-            win_n = have_n ? fetch(nxt, nxt.p_begin / a.block_size) : -1;
+        }
+        if (isk && lane == 0) {
+            // This CTA takes no more tail ranges.  The last CTA to get here
+            // resets both counters for the next launch.
+            __threadfence();
+            if (atomicAdd(&a.ws_ctr[1], 1) == (int)gridDim.x - 1) {
+                a.ws_ctr[0] = 0;
+                a.ws_ctr[1] = 0;
+            }
         }
         if (!ok && lane == 0) {
             // Let the copies already issued land before the CTA's shared memory goes away.
-            for (uint32_t j = 0; j < C::STAGES && j < it; ++j) {
-                const uint32_t x = it - 1 - j;
-                (void)mbar_wait(&fullb[x % C::STAGES], (x / C::STAGES) & 1);
+            for (int g2 = 0; g2 < C::NGRP; ++g2) {
+                const uint32_t n = g2 ? n1 : n0;
+                for (uint32_t j = 0; j < C::SPG && j < n; ++j) {
+                    const uint32_t x = n - 1 - j;
+                    (void)mbar_wait(&fullb[g2 + C::NGRP * (x % C::SPG)], (x / C::SPG) & 1);
+                }
             }
             for (uint32_t j = 0; j < 2 && j < kq; ++j) {
                 const uint32_t x = kq - 1 - j;
@@ -408,64 +531,153 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     // ------------------------------------------------------------------ merger
     if (warp == C::MERGER) {
         float *slot_base = reinterpret_cast<float *>(smem + C::OFF_SLOT);
-        int4 task = make_int4(0, 0, 0, 0);  // {b, g, nsplit, first slot}; nsplit 0 = none
-        Walker w(st);
-        Seg sg;
-        for (uint32_t k = 0; w.next(ctx_s, a.Hkv, a.batch, sg); ++k) {
-            const bool ok = wait_or_abort(&done[k % C::NSLOT], (k / C::NSLOT) & 1, flags, a, 300);
-            const float *so = slot_base + (k % C::NSLOT) * C::SLOT_FLOATS;
-            const float *sml = so + C::NCW * G * D;
-            float O[G][4], M[G], L[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                M[h] = -INFINITY;
-#pragma unroll
-                for (int w2 = 0; w2 < C::NCW; ++w2) M[h] = fmaxf(M[h], sml[(w2 * G + h) * 2]);
-                L[h] = 0.f;
-                O[h][0] = O[h][1] = O[h][2] = O[h][3] = 0.f;
-#pragma unroll
-                for (int w2 = 0; w2 < C::NCW; ++w2) {
-                    const float f = fast_exp2(sml[(w2 * G + h) * 2] - M[h]);
-                    L[h] = fmaf(sml[(w2 * G + h) * 2 + 1], f, L[h]);
-                    const float4 v = *reinterpret_cast<const float4 *>(so + (w2 * G + h) * D + 4 * lane);
-                    O[h][0] = fmaf(v.x, f, O[h][0]);
-                    O[h][1] = fmaf(v.y, f, O[h][1]);
-                    O[h][2] = fmaf(v.z, f, O[h][2]);
-                    O[h][3] = fmaf(v.w, f, O[h][3]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sfree[k % C::NSLOT]);
-            if (!ok) continue;
-            if (sg.t_begin == 0 && sg.t_end == sg.nt) {  // the whole pair: final output
-                const int64_t bh0 = (int64_t)sg.b * a.Hq + (int64_t)sg.g * G;  // first q-head row of (b, g)
+        uint32_t k = 0, ti = 0;
+        Ticket tk;
+        while (take_ticket(ti++, tk)) {
+            Walker w(tk);
+            Seg sg;
+            for (int si = 0; w.next(ctx_s, a.Hkv, a.batch, sg); ++si, ++k) {
+                const bool ok = wait_or_abort(&done[k % C::NSLOT], (k / C::NSLOT) & 1, flags, a, 300);
+                const float *so = slot_base + (k % C::NSLOT) * C::SLOT_FLOATS;
+                const float *sml = so + C::NCW * G * D;
+                float O[G][4], M[G], L[G];
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    const float inv = 1.f / L[h];
-                    __nv_bfloat162 lo = __floats2bfloat162_rn(O[h][0] * inv, O[h][1] * inv);
-                    __nv_bfloat162 hi = __floats2bfloat162_rn(O[h][2] * inv, O[h][3] * inv);
+                    M[h] = -INFINITY;
+#pragma unroll
+                    for (int w2 = 0; w2 < C::NCW; ++w2) M[h] = fmaxf(M[h], sml[(w2 * G + h) * 2]);
+                    L[h] = 0.f;
+                    O[h][0] = O[h][1] = O[h][2] = O[h][3] = 0.f;
+#pragma unroll
+                    for (int w2 = 0; w2 < C::NCW; ++w2) {
+                        const float f = fast_exp2(sml[(w2 * G + h) * 2] - M[h]);
+                        L[h] = fmaf(sml[(w2 * G + h) * 2 + 1], f, L[h]);
+                        const float4 v = *reinterpret_cast<const float4 *>(so + (w2 * G + h) * D + 4 * lane);
+                        O[h][0] = fmaf(v.x, f, O[h][0]);
+                        O[h][1] = fmaf(v.y, f, O[h][1]);
+                        O[h][2] = fmaf(v.z, f, O[h][2]);
+                        O[h][3] = fmaf(v.w, f, O[h][3]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sfree[k % C::NSLOT]);
+                const int64_t bh0 = (int64_t)sg.b * a.Hq + (int64_t)sg.g * G;  // first q-head row of (b, g)
+                if (sg.t_begin == 0 && sg.t_end == sg.nt) {  // the whole pair: final output
+                    if (!ok) continue;
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float inv = 1.f / L[h];
+                        uint2 pk;
+                        pk.x = pack_bf16(O[h][0] * inv, O[h][1] * inv);
+                        pk.y = pack_bf16(O[h][2] * inv, O[h][3] * inv);
+                        *reinterpret_cast<uint2 *>(a.out + (bh0 + h) * D + 4 * lane) = pk;
+                    }
+                    continue;
+                }
+                // A part of the pair (only a range's first and last segments can be):
+                // write the partial, then count it on the pair's arrival counter.
+                const int slot = 2 * tk.r + (si == 0 ? 0 : 1);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    *reinterpret_cast<float4 *>(a.ws_o + ((int64_t)slot * G + h) * D + 4 * lane) =
+                        make_float4(O[h][0], O[h][1], O[h][2], O[h][3]);
+                    if (lane == 0) a.ws_ml[slot * G + h] = make_float2(M[h], L[h]);
+                }
+                const long long p0 = sg.pos - sg.t_begin;  // the pair's first tile
+                const int r0 = sp.owner(p0), r1 = sp.owner(p0 + sg.nt - 1);
+                // The pair's parts: the non-empty ranges r0..r1.
+                int nparts = 0;
+                for (int r = r0 + lane; r <= r1; r += 32) nparts += sp.len(r) > 0 ? 1 : 0;
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) nparts += __shfl_xor_sync(FULL, nparts, off);
+                __threadfence();
+                __syncwarp();
+                int arrived = 0;
+                if (lane == 0) arrived = atomicAdd(&a.ws_cnt[r0], 1);
+                arrived = __shfl_sync(FULL, arrived, 0);
+                if (arrived != nparts - 1) continue;
+                // Every part has landed: merge them.  The pair's part in range r0
+                // is that range's first segment when the pair starts the range,
+                // else its last; in each later range it is the first segment.
+                __threadfence();
+                const int slot0 = 2 * r0 + (p0 == sp.start(r0) ? 0 : 1);
+                auto part_slot = [&](int r) { return r == r0 ? slot0 : 2 * r; };
+                // (m, l) of up to 32 ranges at a time, one range per lane.
+                float Mx[G], Lx[G], acc[G][4];
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    Mx[h] = -INFINITY;
+                    Lx[h] = 0.f;
+                    acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
+                }
+                for (int rb = r0; rb <= r1; rb += 32) {
+                    const int r = rb + lane;
+                    if (r <= r1 && sp.len(r) > 0) {
+#pragma unroll
+                        for (int h = 0; h < G; ++h) Mx[h] = fmaxf(Mx[h], __ldcg(&a.ws_ml[part_slot(r) * G + h]).x);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) Mx[h] = fmaxf(Mx[h], __shfl_xor_sync(FULL, Mx[h], off));
+                constexpr int PB = G >= 8 ? 1 : 8 / G;  // parts whose loads are in flight together
+                for (int rb = r0; rb <= r1; rb += 32) {
+                    const int r = rb + lane;
+                    const bool valid = r <= r1 && sp.len(r) > 0;
+                    float f[G];
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        f[h] = 0.f;
+                        if (valid) {
+                            const float2 ml = __ldcg(&a.ws_ml[part_slot(r) * G + h]);
+                            f[h] = fast_exp2(ml.x - Mx[h]);
+                            Lx[h] = fmaf(ml.y, f[h], Lx[h]);
+                        }
+                    }
+                    unsigned mask = __ballot_sync(FULL, valid);
+                    while (mask) {
+                        int c[PB];
+#pragma unroll
+                        for (int q = 0; q < PB; ++q) {
+                            c[q] = mask ? __ffs(mask) - 1 : -1;
+                            mask &= mask - 1;
+                        }
+                        float4 v[PB][G];
+#pragma unroll
+                        for (int q = 0; q < PB; ++q)
+#pragma unroll
+                            for (int h = 0; h < G; ++h)
+                                if (c[q] >= 0)
+                                    v[q][h] = __ldcg(reinterpret_cast<const float4 *>(
+                                                         a.ws_o + ((int64_t)part_slot(rb + c[q]) * G + h) * D) +
+                                                     lane);
+#pragma unroll
+                        for (int q = 0; q < PB; ++q)
+#pragma unroll
+                            for (int h = 0; h < G; ++h) {
+                                if (c[q] < 0) continue;
+                                const float fc = __shfl_sync(FULL, f[h], c[q]);
+                                acc[h][0] = fmaf(v[q][h].x, fc, acc[h][0]);
+                                acc[h][1] = fmaf(v[q][h].y, fc, acc[h][1]);
+                                acc[h][2] = fmaf(v[q][h].z, fc, acc[h][2]);
+                                acc[h][3] = fmaf(v[q][h].w, fc, acc[h][3]);
+                            }
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) Lx[h] += __shfl_xor_sync(FULL, Lx[h], off);
+                    const float inv = 1.f / Lx[h];
                     uint2 pk;
-                    pk.x = *reinterpret_cast<uint32_t *>(&lo);
-                    pk.y = *reinterpret_cast<uint32_t *>(&hi);
+                    pk.x = pack_bf16(acc[h][0] * inv, acc[h][1] * inv);
+                    pk.y = pack_bf16(acc[h][2] * inv, acc[h][3] * inv);
                     *reinterpret_cast<uint2 *>(a.out + (bh0 + h) * D + 4 * lane) = pk;
                 }
-                continue;
-            }
-            // A part of the pair: only a range's first and last segments can be.
-            const int slot = 2 * (int)blockIdx.x + (k == 0 ? 0 : 1);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                *reinterpret_cast<float4 *>(a.ws_o + ((int64_t)slot * G + h) * D + 4 * lane) =
-                    make_float4(O[h][0], O[h][1], O[h][2], O[h][3]);
-                if (lane == 0) a.ws_ml[slot * G + h] = make_float2(M[h], L[h]);
-            }
-            if (sg.t_begin == 0) {  // the pair starts here and goes on in the next CTAs
-                const long long last = sg.pos + sg.nt - 1;
-                const int nsplit = (int)(owner_cta(last, st.base, st.rem) - blockIdx.x) + 1;
-                task = make_int4(sg.b, sg.g, nsplit, slot);
+                if (lane == 0) a.ws_cnt[r0] = 0;  // ready for the next launch
             }
         }
-        if (lane == 0) a.ws_task[blockIdx.x] = task;
         return;
     }
 
@@ -490,149 +702,124 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
 
     uint32_t qa[8][2];  // A fragments of q: [k step][cols 2*t4.. and 2*t4+8..] of row g4
     float o[16][4];     // O fragments: [dim tile j] rows g4 (and g4+8, unused), dims 8j + 2*t4, +1
-    uint32_t it = 0;
-    Walker w(st);
-    Seg sg;
-    for (uint32_t k = 0; w.next(ctx_s, a.Hkv, a.batch, sg); ++k) {
-        if (wait_or_abort(&qfull[k & 1], (k >> 1) & 1, flags, a, 200 + warp)) {
-            const uint32_t qrow = smem_addr(smem + C::OFF_Q + (k & 1) * C::Q_BYTES) + g4 * ROW_BYTES + 4 * t4;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                qa[kk][0] = hvalid ? ld_shared_u32(qrow + 32 * kk) : 0u;
-                qa[kk][1] = hvalid ? ld_shared_u32(qrow + 32 * kk + 16) : 0u;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&qempty[k & 1]);
-        float m_ref = -INFINITY, l_part = 0.f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-
-        for (int t = sg.t_begin; t < sg.t_end; ++t, ++it) {
-            if ((int)(it % C::NGRP) != grp) continue;
-            const int stage = it % C::STAGES;
-            if (wait_or_abort(&kfull[stage], (it / C::STAGES) & 1, flags, a, 210 + warp)) {
-                const uint32_t ks = smem_addr(smem + stage * C::STAGE_BYTES);
-                const uint32_t vs = ks + TILE * ROW_BYTES;
-                const int nvalid = min(TILE, sg.p_end - t * TILE);
-                // ---- S = Q.K^T for this warp's 16 keys: two n-tiles of 8 keys
-                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    uint32_t nt_mine = 0, k = 0, ti = 0;  // tiles of this warp's group, segments, tickets
+    Ticket tk;
+    while (take_ticket(ti++, tk)) {
+        Walker w(tk);
+        Seg sg;
+        for (; w.next(ctx_s, a.Hkv, a.batch, sg); ++k) {
+            if (wait_or_abort(&qfull[k & 1], (k >> 1) & 1, flags, a, 200 + warp)) {
+                const uint32_t qrow = smem_addr(smem + C::OFF_Q + (k & 1) * C::Q_BYTES) + g4 * ROW_BYTES + 4 * t4;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const int chunk = 2 * kk + (mi & 1);  // 16-byte column of the row
-                    const uint32_t ad =
-                        ks + qk_row + (chunk >> 3) * half_stride + ((uint32_t)((chunk & 7) ^ r8) << 4);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(ad, b0, b1, b2, b3);
-                    mma16816(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-                    mma16816(sc[1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
-                }
-                // ---- online softmax (base 2) with a lazy reference max
-                const int key0 = wig * KPW + 2 * t4;
-                float x[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int key = key0 + (e >> 1) * 8 + (e & 1);
-                    x[e] = key < nvalid ? sc[e >> 1][e & 1] * a.scale_log2 : -INFINITY;
-                }
-                float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-                if (__any_sync(FULL, hvalid && mx > m_ref + kLazyRescale)) {
-                    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
-                    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
-                    const float m_new = fmaxf(m_ref, mx);
-                    const float alpha = m_new == -INFINITY ? 1.f : fast_exp2(m_ref - m_new);
-                    l_part *= alpha;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        o[j][0] *= alpha;
-                        o[j][1] *= alpha;
-                    }
-                    m_ref = m_new;
-                }
-                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                float p[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) p[e] = fast_exp2(x[e] - m_use);
-                l_part += (p[0] + p[1]) + (p[2] + p[3]);
-                const uint32_t pa0 = pack_bf16(p[0], p[1]), pa2 = pack_bf16(p[2], p[3]);
-                // ---- O += P.V once the V tile has landed
-                if (wait_or_abort(&vfull[stage], (it / C::STAGES) & 1, flags, a, 230 + warp)) {
-                    const bool ragged = nvalid < (wig + 1) * KPW;
-                    if (ragged) {
-                        // Rows past the context may hold anything (NaN included): zero
-                        // them so that p = 0 contributes exactly nothing.
-                        for (int c = lane; c < KPW * 16; c += 32) {
-                            const int kk = wig * KPW + (c >> 4);
-                            if (kk >= nvalid)
-                                st_shared_zero16(vs + key_off(kk) + ((c >> 3) & 1) * half_stride + (c & 7) * 16);
-                        }
-                        __syncwarp();
-                    }
-#pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const int chunk = j + (mi >> 1);
-                        const uint32_t ad =
-                            vs + pv_row + (chunk >> 3) * half_stride + ((uint32_t)((chunk & 7) ^ r8) << 4);
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(ad, b0, b1, b2, b3);
-                        mma16816(o[j], pa0, 0u, pa2, 0u, b0, b1);
-                        mma16816(o[j + 1], pa0, 0u, pa2, 0u, b2, b3);
-                    }
-                    // The zeroed rows are rewritten by the next TMA copy into this
-                    // stage: order the generic-proxy stores before it.
-                    if (ragged) fence_proxy_async_smem();
+                    qa[kk][0] = hvalid ? ld_shared_u32(qrow + 32 * kk) : 0u;
+                    qa[kk][1] = hvalid ? ld_shared_u32(qrow + 32 * kk + 16) : 0u;
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
-        }
-        // ---- publish this warp's (m, l, o) for the merge warp
-        l_part += __shfl_xor_sync(FULL, l_part, 1);
-        l_part += __shfl_xor_sync(FULL, l_part, 2);
-        (void)wait_or_abort(&sfree[k % C::NSLOT], ((k / C::NSLOT) & 1) ^ 1, flags, a, 220 + warp);
-        float *so = slot_base + (k % C::NSLOT) * C::SLOT_FLOATS;
-        if (hvalid) {
-            float *row = so + (warp * G + g4) * D + 2 * t4;
+            if (lane == 0) mbar_arrive(&qempty[k & 1]);
+            float m_ref = -INFINITY, l_part = 0.f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) *reinterpret_cast<float2 *>(row + 8 * j) = make_float2(o[j][0], o[j][1]);
-            if (t4 == 0) {
-                so[C::NCW * G * D + (warp * G + g4) * 2] = m_ref;
-                so[C::NCW * G * D + (warp * G + g4) * 2 + 1] = l_part;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&done[k % C::NSLOT]);
-    }
-}
+            for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
-// Log-sum-exp merge of a pair split across CTAs j0 .. j0+nsplit-1 (task of
-// CTA j0): M = max_c m_c, L = sum_c l_c 2^(m_c - M), out = sum_c o_c 2^(m_c - M) / L.
-// The pair's partial in CTA j0 is in the task's slot; in every later CTA it
-// is that CTA's first segment, slot 2j.  Launched after decode_kernel on the
-// same stream (programmatic dependent launch: it may start early and waits
-// for the decode grid's results).
-__global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeArgs a, int G) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int4 task = a.ws_task[blockIdx.x];
-    const int nsplit = task.z;
-    if (nsplit <= 1) return;
-    const int j0 = blockIdx.x, d = threadIdx.x;
-    for (int h = 0; h < G; ++h) {
-        float M = -INFINITY;
-        for (int c = 0; c < nsplit; ++c) {
-            const int slot = c == 0 ? task.w : 2 * (j0 + c);
-            M = fmaxf(M, a.ws_ml[slot * G + h].x);
+            for (int t = sg.t_begin; t < sg.t_end; ++t) {
+                if ((int)((sg.pos + (t - sg.t_begin)) % C::NGRP) != grp) continue;
+                const uint32_t n = nt_mine++;
+                const int stage = grp + C::NGRP * (int)(n % C::SPG);
+                const uint32_t ph = (n / C::SPG) & 1;
+                if (wait_or_abort(&kfull[stage], ph, flags, a, 210 + warp)) {
+                    const uint32_t ks = smem_addr(smem + stage * C::STAGE_BYTES);
+                    const uint32_t vs = ks + TILE * ROW_BYTES;
+                    const int nvalid = min(TILE, sg.p_end - t * TILE);
+                    // ---- S = Q.K^T for this warp's 16 keys: two n-tiles of 8 keys
+                    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    #pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const int chunk = 2 * kk + (mi & 1);  // 16-byte column of the row
+                        const uint32_t ad =
+                            ks + qk_row + (chunk >> 3) * half_stride + ((uint32_t)((chunk & 7) ^ r8) << 4);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(ad, b0, b1, b2, b3);
+                        mma16816(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+                        mma16816(sc[1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+                    }
+                    // ---- online softmax (base 2) with a lazy reference max
+                    const int key0 = wig * KPW + 2 * t4;
+                    float x[4];
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = key0 + (e >> 1) * 8 + (e & 1);
+                        x[e] = key < nvalid ? sc[e >> 1][e & 1] * a.scale_log2 : -INFINITY;
+                    }
+                    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+                    if (__any_sync(FULL, hvalid && mx > m_ref + kLazyRescale)) {
+                        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+                        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
+                        const float m_new = fmaxf(m_ref, mx);
+                        const float alpha = m_new == -INFINITY ? 1.f : fast_exp2(m_ref - m_new);
+                        l_part *= alpha;
+    #pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            o[j][0] *= alpha;
+                            o[j][1] *= alpha;
+                        }
+                        m_ref = m_new;
+                    }
+                    const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                    float p[4];
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) p[e] = fast_exp2(x[e] - m_use);
+                    l_part += (p[0] + p[1]) + (p[2] + p[3]);
+                    const uint32_t pa0 = pack_bf16(p[0], p[1]), pa2 = pack_bf16(p[2], p[3]);
+                    // ---- O += P.V once the V tile has landed
+                    if (wait_or_abort(&vfull[stage], ph, flags, a, 230 + warp)) {
+                        const bool ragged = nvalid < (wig + 1) * KPW;
+                        if (ragged) {
+                            // Rows past the context may hold anything (NaN included): zero
+                            // them so that p = 0 contributes exactly nothing.
+                            for (int c = lane; c < KPW * 16; c += 32) {
+                                const int kk = wig * KPW + (c >> 4);
+                                if (kk >= nvalid)
+                                    st_shared_zero16(vs + key_off(kk) + ((c >> 3) & 1) * half_stride + (c & 7) * 16);
+                            }
+                            __syncwarp();
+                        }
+    #pragma unroll
+                        for (int j = 0; j < 16; j += 2) {
+                            const int chunk = j + (mi >> 1);
+                            const uint32_t ad =
+                                vs + pv_row + (chunk >> 3) * half_stride + ((uint32_t)((chunk & 7) ^ r8) << 4);
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4_t(ad, b0, b1, b2, b3);
+                            mma16816(o[j], pa0, 0u, pa2, 0u, b0, b1);
+                            mma16816(o[j + 1], pa0, 0u, pa2, 0u, b2, b3);
+                        }
+                        // The zeroed rows are rewritten by the next TMA copy into this
+                        // stage: order the generic-proxy stores before it.
+                        if (ragged) fence_proxy_async_smem();
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+            }
+            // ---- publish this warp's (m, l, o) for the merge warp
+            l_part += __shfl_xor_sync(FULL, l_part, 1);
+            l_part += __shfl_xor_sync(FULL, l_part, 2);
+            (void)wait_or_abort(&sfree[k % C::NSLOT], ((k / C::NSLOT) & 1) ^ 1, flags, a, 220 + warp);
+            float *so = slot_base + (k % C::NSLOT) * C::SLOT_FLOATS;
+            if (hvalid) {
+                float *row = so + (warp * G + g4) * D + 2 * t4;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    *reinterpret_cast<float2 *>(row + 8 * j) = make_float2(o[j][0], o[j][1]);
+                if (t4 == 0) {
+                    so[C::NCW * G * D + (warp * G + g4) * 2] = m_ref;
+                    so[C::NCW * G * D + (warp * G + g4) * 2 + 1] = l_part;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&done[k % C::NSLOT]);
         }
-        float L = 0.f, acc = 0.f;
-        for (int c = 0; c < nsplit; ++c) {
-            const int slot = c == 0 ? task.w : 2 * (j0 + c);
-            const float2 ml = a.ws_ml[slot * G + h];
-            const float f = fast_exp2(ml.x - M);
-            L = fmaf(ml.y, f, L);
-            acc = fmaf(a.ws_o[((int64_t)slot * G + h) * D + d], f, acc);
-        }
-        const int64_t row = (int64_t)task.x * a.Hq + (int64_t)task.y * G + h;
-        a.out[row * D + d] = __float2bfloat16_rn(acc / L);
     }
 }
 
@@ -650,38 +837,40 @@ pa_status launch(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_kernel)");
         g_attr_done[dev][gi] = 1;
     }
-    decode_kernel<G><<<grid, Cfg<G>::NTHREADS, Cfg<G>::smem_bytes(a.batch), st>>>(tk, tv, a);
-    pa_status r = check_launch("decode_kernel");
-    if (r != PA_OK) return r;
+    // Programmatic dependent launch: the grid may start while the previous
+    // kernel on the stream finishes; it reads nothing before griddepcontrol.wait.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(D);
-    cfg.dynamicSmemBytes = 0;
+    cfg.blockDim = dim3(Cfg<G>::NTHREADS);
+    cfg.dynamicSmemBytes = Cfg<G>::smem_bytes(a.batch);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_merge_kernel, a, G);
-    if (e != cudaSuccess) return cuda_fail(e, "decode_merge_kernel");
-    return check_launch("decode_merge_kernel");
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<G>, tk, tv, a);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_kernel");
+    return check_launch("decode_kernel");
 }
 
-// Workspace: (m, l) pairs, then fp32 partials, then merge tasks; two partial
-// slots per CTA of the largest grid.
+// Workspace: the two tail counters and the per-range arrival counters first
+// (at offsets that do not depend on the shape, so a workspace can serve calls
+// of any GQA group and stays zero-filled there), then (m, l) pairs and fp32
+// partials, two slots of G heads per range.
 struct WsLayout {
-    size_t ml_off, o_off, task_off, total;
+    size_t ctr_off, cnt_off, ml_off, o_off, total;
 };
 
 WsLayout ws_layout(int G) {
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-    const size_t slots = 2 * (size_t)kMaxGrid * G;
+    const size_t slots = 2 * (size_t)kMaxRanges * G;
     WsLayout L;
-    L.ml_off = 0;
-    L.o_off = up(slots * sizeof(float2));
-    L.task_off = up(L.o_off + slots * D * sizeof(float));
-    L.total = L.task_off + (size_t)kMaxGrid * sizeof(int4);
+    L.ctr_off = 0;
+    L.cnt_off = 256;
+    L.ml_off = up(L.cnt_off + (size_t)kMaxRanges * sizeof(int));
+    L.o_off = up(L.ml_off + slots * sizeof(float2));
+    L.total = L.o_off + slots * D * sizeof(float);
     return L;
 }
 
@@ -722,6 +911,10 @@ pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *
     if ((int64_t)num_blocks * block_size > 0x7fffffffLL ||
         (int64_t)max_blocks_per_seq * block_size > 0x7fffffffLL)
         return fail(PA_ERR_UNSUPPORTED, "pool or table too large for 32-bit slot indices");
+    // The per-head tile prefix sum is 32-bit: batch * ceil(max_blocks * B / 64) must fit.
+    if ((int64_t)batch * (((int64_t)max_blocks_per_seq * block_size + TILE - 1) / TILE) >= 0x7fffffffLL)
+        return fail(PA_ERR_UNSUPPORTED, "batch x block-table capacity too large (%d x %lld tokens)", batch,
+                    (long long)max_blocks_per_seq * block_size);
     if (q_row_stride < (int64_t)num_q_heads * D || q_row_stride % 8)
         return fail(PA_ERR_INVALID_ARG, "q_row_stride must be >= num_q_heads*head_dim and a multiple of 8");
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
@@ -760,7 +953,8 @@ pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     A.ws_ml = reinterpret_cast<float2 *>(ws + W.ml_off);
     A.ws_o = reinterpret_cast<float *>(ws + W.o_off);
-    A.ws_task = reinterpret_cast<int4 *>(ws + W.task_off);
+    A.ws_cnt = reinterpret_cast<int *>(ws + W.cnt_off);
+    A.ws_ctr = reinterpret_cast<int *>(ws + W.ctr_off);
     A.err = device_error_ptr();
     A.checked = checked_mode() ? 1 : 0;
 
@@ -784,9 +978,10 @@ pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *
 // ---------------------------------------------------------------------------
 
 // Split-partial scratch, enough for every shape (the workspace size depends
-// only on the GQA group).  It is loaded with the module, so every GPU that
-// loads this library holds it until the process exits.
-static constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+// only on the GQA group).  It is loaded with the module, zero-filled as the
+// workspace contract asks, so every GPU that loads this library holds it
+// until the process exits.
+static constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char pa_static_scratch[kStaticScratchBytes];
 
 namespace {
@@ -801,7 +996,7 @@ extern "C" pa_status pa_decode_static(void *out, const void *q, int64_t q_row_st
                                       int32_t block_size, int32_t num_blocks, float softmax_scale,
                                       pa_stream_t stream) {
     using namespace pa;
-    static_assert(kStaticScratchBytes >= 2 * (size_t)kMaxGrid * 8 * (D * 4 + 8) + kMaxGrid * 16 + 512,
+    static_assert(kStaticScratchBytes >= 2 * (size_t)kMaxRanges * 8 * (D * 4 + 8) + kMaxRanges * 4 + 1024,
                   "the static scratch holds the workspace of the largest GQA group");
     const size_t need = pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim);
     if (need == 0 || batch <= 0)  // batch == 0 or arguments pa_decode rejects: let it report

@@ -46,13 +46,14 @@ def test_status_strings(L):
 
 
 def test_workspace_size_host_math(L):
-    # Two partial slots of G heads per CTA of the largest grid (256 CTAs), plus merge tasks:
-    # independent of batch and context length.
+    # Two partial slots of G heads per range (a head and a tail range per CTA of
+    # the largest grid, 256 CTAs), plus counters: independent of batch and context length.
+    ranges = 2 * 256
     for hq, hkv in [(16, 8), (32, 8), (8, 8), (64, 8)]:
         g = hq // hkv
         n = L.pa_decode_workspace_size(hq, hkv, 128)
-        assert 2 * 256 * g * (128 * 4 + 8) <= n <= 2 * 256 * g * (128 * 4 + 8) + 256 * 16 + 1024
-    assert L.pa_decode_workspace_size(64, 8, 128) <= 4 << 20       # fits the static scratch
+        assert 2 * ranges * g * (128 * 4 + 8) <= n <= 2 * ranges * g * (128 * 4 + 8) + ranges * 4 + 2048
+    assert L.pa_decode_workspace_size(64, 8, 128) <= 8 << 20       # fits the static scratch
     # Unsupported shapes give 0.
     assert L.pa_decode_workspace_size(16, 8, 64) == 0
     assert L.pa_decode_workspace_size(24, 8, 128) == 0
@@ -103,6 +104,7 @@ def test_decode_argument_checks(L):
     assert _decode(L, k=C.c_void_p(258)) == pa.PA_ERR_INVALID_ARG
     assert _decode(L, ws=C.c_void_p(264)) == pa.PA_ERR_INVALID_ARG      # unaligned workspace
     assert _decode(L, nb=1 << 24) == pa.PA_ERR_UNSUPPORTED       # slots overflow int32
+    assert _decode(L, batch=2048, mb=1 << 20, nb=1024, B=1024) == pa.PA_ERR_UNSUPPORTED  # tile prefix overflows
 
 
 def test_slot_mapping_argument_checks(L):

@@ -114,7 +114,8 @@ def test_decode_fewer_tiles_than_ctas():
 
 
 def test_decode_repeated_calls_reuse_workspace():
-    """Many calls on one (uninitialised) workspace give identical results."""
+    """Many calls on one workspace give identical results: each call leaves
+    its counters zeroed for the next."""
     ctx = [3000, 5000, 257, 1]
     inp = make_decode("repeat", 11, 4, 16, 8, ctx)
     kc, vc = dev_bf16(inp.k_cache), dev_bf16(inp.v_cache)
@@ -166,3 +167,18 @@ def test_decode_workloads_full_size(cfg):
     # The store touched exactly the decoded tokens' slots.
     assert np.array_equal(host_bits(kc), okc) and np.array_equal(host_bits(vc), ovc)
     assert_close(host_f64(out), want, f"workload {cfg}")
+
+
+def test_decode_one_workspace_serves_every_gqa_group():
+    """A workspace sized for the largest group is reused by calls of other
+    groups in turn; its counters stay zeroed between them (they sit at offsets
+    that do not depend on the group)."""
+    ws = pa.decode_workspace(64, 8, 128)
+    for hq, ctx in [(32, [4000, 77, 1300]), (16, [1, 17, 200, 255, 256]), (64, [2500, 9]), (8, [700] * 6),
+                    (16, [5000, 5000])]:
+        inp = make_decode(f"ws {hq}", 20 + hq, len(ctx), hq, 8, ctx)
+        out = pa.decode(dev_bf16(inp.q), dev_bf16(inp.k_cache), dev_bf16(inp.v_cache), dev_i32(inp.block_tables),
+                        dev_i32(inp.context_lens), inp.scale, workspace=ws)
+        assert pa.get_device_error() == (0, 0)
+        want = O.decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale)
+        assert_close(host_f64(out), want, f"shared workspace {hq}/8")
