@@ -297,27 +297,22 @@ def run_ours(args):
     if code:
         raise RuntimeError(f"device error {code} at {where}")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # Headline: whole steps, back to back on the stream (the three kernels are
+    # programmatic dependent launches, so nothing may sit between them).
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
             flush.zero_()
-            e = ev[i]
-            e[0].record(stream)
-            pa.slot_mapping_decode(bt, ctx, inp.block_size, out=slots)
-            e[1].record(stream)
-            pa.store_kvcache(nk, nv, kc, vc, slots)
-            e[2].record(stream)
-            pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out)
-            e[3].record(stream)
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
         torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
-    dec_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    store_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
     t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if ws > 1:
@@ -325,6 +320,21 @@ def run_ours(args):
     total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     value = ws * inp.batch * args.steps / (total_ms / 1000.0)
+
+    # Per-kernel durations for the roofline: events around the store and the
+    # decode launch (same inputs, L2 flushed before each step).
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        pa.slot_mapping_decode(bt, ctx, inp.block_size, out=slots)
+        kev[i][0].record(stream)
+        pa.store_kvcache(nk, nv, kc, vc, slots)
+        kev[i][1].record(stream)
+        pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out)
+        kev[i][2].record(stream)
+    torch.cuda.synchronize()
+    store_ms = [e[0].elapsed_time(e[1]) for e in kev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in kev]
 
     # End to end through the public API: host inputs -> device, step, output -> host.
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -385,7 +395,7 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": alg_bytes, "decode_ms": dec_avg,
                          "store_ms": sum(store_ms) / len(store_ms)},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 3 * args.steps,
             "clocks": clk.summary(),
             "prefill": prefill,
         }

@@ -839,19 +839,8 @@ pa_status launch(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &
     }
     // Programmatic dependent launch: the grid may start while the previous
     // kernel on the stream finishes; it reads nothing before griddepcontrol.wait.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(Cfg<G>::NTHREADS);
-    cfg.dynamicSmemBytes = Cfg<G>::smem_bytes(a.batch);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<G>, tk, tv, a);
-    if (e != cudaSuccess) return cuda_fail(e, "decode_kernel");
-    return check_launch("decode_kernel");
+    return launch_pdl(decode_kernel<G>, dim3((unsigned)grid), dim3(Cfg<G>::NTHREADS), Cfg<G>::smem_bytes(a.batch),
+                      st, "decode_kernel", tk, tv, a);
 }
 
 // Workspace: the two tail counters and the per-range arrival counters first

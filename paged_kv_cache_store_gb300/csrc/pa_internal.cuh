@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <utility>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -149,6 +150,14 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 // ---------------------------------------------------------------------------
 // Named barriers (a subset of the CTA's warps)
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible, then let the grids that
+// depend on this one be scheduled (they wait on this grid the same way).
+__device__ __forceinline__ void pdl_wait_then_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -215,5 +224,27 @@ pa_status encode_tensor_map_3d(CUtensorMap *map, const void *base, int64_t dim0,
                                bool swizzle128);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launches kernel<<<grid, block, smem, stream>>>(args...) as a programmatic
+// dependent launch: the grid may be scheduled while the previous work on the
+// stream drains, so the kernel must execute griddepcontrol.wait before it
+// touches global memory.
+template <typename... KArgs, typename... Args>
+pa_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     const char *name, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    return check_launch(name);
+}
 
 }  // namespace pa

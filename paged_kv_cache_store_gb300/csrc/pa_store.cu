@@ -8,6 +8,10 @@
 // 8 KiB of traffic per stored token (2 KiB read + 2 KiB write for each of K
 // and V).
 //
+// All three kernels are programmatic dependent launches: they start by
+// waiting for the preceding work on the stream (griddepcontrol.wait) and
+// then release the work queued behind them.
+//
 // slot mapping: [PA3 §3/§4] the slot of logical position p of a sequence is
 // block_table[p / B] * B + p % B; the decode form takes p = ctx - 1, the
 // prefill form p = c + i for the uncached suffix of each sequence.
@@ -20,6 +24,7 @@ __global__ void __launch_bounds__(128) store_kvcache_kernel(
     const uint4 *__restrict__ key, int64_t key_stride16, const uint4 *__restrict__ value,
     int64_t value_stride16, uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
     const int32_t *__restrict__ slot_mapping, int32_t row16, int64_t num_slots, DevError *err) {
+    pdl_wait_then_release();
     const int64_t token = blockIdx.x;
     const bool is_v = blockIdx.y != 0;
     const int32_t slot = __ldg(slot_mapping + token);
@@ -43,6 +48,7 @@ __global__ void slot_mapping_decode_kernel(int32_t *__restrict__ slot_mapping,
                                            const int32_t *__restrict__ block_tables,
                                            int32_t max_blocks, const int32_t *__restrict__ ctx_lens,
                                            int32_t batch, int32_t block_size, DevError *err) {
+    pdl_wait_then_release();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= batch) return;
     const int32_t ctx = ctx_lens[b];
@@ -61,6 +67,7 @@ __global__ void slot_mapping_prefill_kernel(int32_t *__restrict__ slot_mapping,
                                             int32_t max_blocks, const int32_t *__restrict__ cu_q,
                                             const int32_t *__restrict__ cu_k, int32_t num_seqs,
                                             int32_t total_q, int32_t block_size, DevError *err) {
+    pdl_wait_then_release();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= total_q) return;
     // The sequence owning query row t: the last s with cu_q[s] <= t.
@@ -111,11 +118,11 @@ pa_status pa_store_kvcache(const void *key, int64_t key_row_stride, const void *
     const int32_t row16 = static_cast<int32_t>(row / 8);
     const dim3 grid(static_cast<unsigned>(num_tokens), 2);
     const int threads = row16 >= 128 ? 128 : ((row16 + 31) / 32) * 32;
-    store_kvcache_kernel<<<grid, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4 *>(key), key_row_stride / 8, static_cast<const uint4 *>(value),
-        value_row_stride / 8, static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
-        slot_mapping, row16, num_slots, device_error_ptr());
-    return check_launch("store_kvcache_kernel");
+    return launch_pdl(store_kvcache_kernel, grid, dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream),
+                      "store_kvcache_kernel", static_cast<const uint4 *>(key), (int64_t)(key_row_stride / 8),
+                      static_cast<const uint4 *>(value), (int64_t)(value_row_stride / 8),
+                      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, row16,
+                      num_slots, device_error_ptr());
 }
 
 pa_status pa_slot_mapping_decode(int32_t *slot_mapping, const int32_t *block_tables,
@@ -127,10 +134,9 @@ pa_status pa_slot_mapping_decode(int32_t *slot_mapping, const int32_t *block_tab
     if (!slot_mapping || !block_tables || !context_lens) return fail(PA_ERR_INVALID_ARG, "null pointer");
     if (block_size <= 0 || max_blocks_per_seq <= 0)
         return fail(PA_ERR_INVALID_ARG, "block_size and max_blocks_per_seq must be positive");
-    slot_mapping_decode_kernel<<<(batch + 127) / 128, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        slot_mapping, block_tables, max_blocks_per_seq, context_lens, batch, block_size,
-        device_error_ptr());
-    return check_launch("slot_mapping_decode_kernel");
+    return launch_pdl(slot_mapping_decode_kernel, dim3((batch + 127) / 128), dim3(128), 0,
+                      reinterpret_cast<cudaStream_t>(stream), "slot_mapping_decode_kernel", slot_mapping,
+                      block_tables, max_blocks_per_seq, context_lens, batch, block_size, device_error_ptr());
 }
 
 pa_status pa_slot_mapping_prefill(int32_t *slot_mapping, const int32_t *block_tables,
@@ -144,10 +150,10 @@ pa_status pa_slot_mapping_prefill(int32_t *slot_mapping, const int32_t *block_ta
         return fail(PA_ERR_INVALID_ARG, "null pointer");
     if (block_size <= 0 || max_blocks_per_seq <= 0)
         return fail(PA_ERR_INVALID_ARG, "block_size and max_blocks_per_seq must be positive");
-    slot_mapping_prefill_kernel<<<(total_q + 255) / 256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        slot_mapping, block_tables, max_blocks_per_seq, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q,
-        block_size, device_error_ptr());
-    return check_launch("slot_mapping_prefill_kernel");
+    return launch_pdl(slot_mapping_prefill_kernel, dim3((total_q + 255) / 256), dim3(256), 0,
+                      reinterpret_cast<cudaStream_t>(stream), "slot_mapping_prefill_kernel", slot_mapping,
+                      block_tables, max_blocks_per_seq, cu_seqlens_q, cu_seqlens_k, num_seqs, total_q,
+                      block_size, device_error_ptr());
 }
 
 }  // extern "C"
