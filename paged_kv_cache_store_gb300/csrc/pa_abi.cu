@@ -110,22 +110,27 @@ pa_status encode_tensor_map_3d(CUtensorMap *map, const void *base, int64_t dim0,
     return PA_OK;
 }
 
-pa_status encode_kv_tensor_map_halves(CUtensorMap *map, const void *base, int64_t num_slots,
-                                      int32_t num_kv_heads, int32_t box_rows) {
+pa_status encode_halves_map(CUtensorMap *map, const void *base, int64_t num_rows, int64_t row_stride_bytes,
+                            int32_t num_heads, int32_t box_rows, int32_t box_halves) {
     pa_status st = get_encoder();
     if (st != PA_OK) return st;
-    // Dims innermost first: 64 elements of a row half, slot, half, kv head.
-    const cuuint64_t dims[4] = {64u, (cuuint64_t)num_slots, 2u, (cuuint64_t)num_kv_heads};
-    const cuuint64_t strides[3] = {(cuuint64_t)num_kv_heads * 256u, 128u, 256u};
-    const cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, 2u, 1u};
+    // Dims innermost first: 64 elements of a row half, row, half, head.
+    const cuuint64_t dims[4] = {64u, (cuuint64_t)num_rows, 2u, (cuuint64_t)num_heads};
+    const cuuint64_t strides[3] = {(cuuint64_t)row_stride_bytes, 128u, 256u};
+    const cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, (cuuint32_t)box_halves, 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
-        return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a KV pool of %lld slots x %d heads",
-                    (int)r, (long long)num_slots, num_kv_heads);
+        return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %lld rows x %d heads", (int)r,
+                    (long long)num_rows, num_heads);
     return PA_OK;
+}
+
+pa_status encode_kv_tensor_map_halves(CUtensorMap *map, const void *base, int64_t num_slots,
+                                      int32_t num_kv_heads, int32_t box_rows) {
+    return encode_halves_map(map, base, num_slots, (int64_t)num_kv_heads * 256, num_kv_heads, box_rows, 2);
 }
 
 }  // namespace pa

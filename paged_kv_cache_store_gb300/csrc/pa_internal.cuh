@@ -217,6 +217,11 @@ bool checked_mode();
 // consecutive rows at one 16-byte column fall in 8 different banks.
 pa_status encode_kv_tensor_map_halves(CUtensorMap *map, const void *base, int64_t num_slots,
                                       int32_t num_kv_heads, int32_t box_rows);
+// The same view for any [rows][heads][128] bf16 tensor with a row stride
+// (bytes, a multiple of 16): box {64, box_rows, box_halves, 1}.  With
+// box_halves == 1 a copy fetches one 64-dim half (coordinate 2 picks it).
+pa_status encode_halves_map(CUtensorMap *map, const void *base, int64_t num_rows, int64_t row_stride_bytes,
+                            int32_t num_heads, int32_t box_rows, int32_t box_halves);
 // General 3-D bf16 tensor map: dims {dim0, dim1, dim2} (dim0 contiguous),
 // byte strides of dims 1 and 2, box {box0, 1, box2}, optional 128-byte swizzle.
 pa_status encode_tensor_map_3d(CUtensorMap *map, const void *base, int64_t dim0, int64_t dim1, int64_t dim2,

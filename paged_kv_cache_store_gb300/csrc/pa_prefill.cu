@@ -6,31 +6,41 @@
 // all Lk keys when causal == 0), keys read through the block table
 // (prefix cache) or from contiguous rows.
 //
-// How (GB300 design): persistent CTAs (one per SM) walk work tiles of
-// (128-row query tile, sequence, q head), highest query tiles first; all
-// roles follow one global KV-tile counter, so the next tile's Q/K/V copies
-// overlap the current tile's softmax and epilogue.
-//  * warps 0 and 10 (one thread each) issue TMA copies: warp 0 the Q tile
-//    and the K tiles of 128 keys, warp 10 the V tiles, into separate rings
-//    (Q: 2, K: 3, V: 2 stages) so neither stream waits behind the other.  Boxes are {64 dims, 1 head,
-//    R rows} with 128-byte swizzle (two boxes per 128-dim row); paged boxes
-//    never straddle a block (R = gcd(block_size, 128)).
-//  * warp 1 (one thread) owns the tensor cores: S = Q.K^T (M=N=128, K=128,
-//    eight tcgen05.mma K=16 steps) into one of two TMEM buffers, then
-//    O += P.V with V as an MN-major operand, O accumulating in TMEM.
-//    tcgen05.commit arrives on mbarriers to free K/V stages, publish S and
-//    release the P buffer.
-//  * warps 2..9: two warps per TMEM lane quarter, one thread per query row
-//    and 64 of the 128 key columns each, read S with tcgen05.ld, apply scale
-//    and mask, share the row max through shared memory (an mbarrier per
-//    warp pair, double-buffered slots), keep running statistics in base 2, and write
-//    their half of P as bf16 pairs into TMEM, where the P.V MMA takes it as
-//    its A operand (only V is read from shared memory).  O in TMEM is rescaled only when a row's max grows by
-//    more than 2^8 (otherwise the stale max keeps P <= 256, exact enough in
-//    bf16 and fp32); the final 1/l is applied in the epilogue.
+// How (GB300 design): persistent CTAs (one per SM) walk work units of
+// (128-row query tile, sequence, q head), highest query tiles first.
+//  * warp 0 issues the TMA copies of Q and K, warp 2 those of V (rings: K 3
+//    stages, V 2 stages of 128 keys; one Q tile).  Tiles land 128-byte
+//    swizzled as [half][row][64] through 4-D tensor maps that view a
+//    [rows][heads][128] tensor as [head][half][row][64]: one copy per tile
+//    when blocks hold 128 rows or more.
+//  * The softmax warps move the unit's Q tile from shared memory into TMEM
+//    (bf16 pairs, one row per lane), so both products take their A operand
+//    from TMEM and only K and V are read from shared memory by the tensor
+//    cores.
+//  * Two single-thread MMA issuers feed the tensor cores, so one's barrier
+//    waits overlap the other's MMAs: warp 1 issues S = Q.K^T (M=N=128, K=128,
+//    8 steps) into one of two S buffers, warp 3 issues O += P.V with P read
+//    from TMEM (bf16 pairs written over its S buffer) and V as an MN-major
+//    operand.  Scores run ahead of P.V by up to two tiles; a Q.K waits until
+//    the P.V that read its buffer two tiles earlier has completed.
+//    tcgen05.commit arrives on mbarriers to free K/V stages and S buffers,
+//    publish S and report O.
+//  * warps 4..7: one thread per query row (its TMEM lane) holds all 128
+//    scores of a tile, so row statistics need no exchange.  Online softmax
+//    in base 2; P goes back to TMEM as bf16 pairs.  O is rescaled only when a
+//    row's max grows by more than 2^8 (P then stays <= 256, exact enough in
+//    bf16 and fp32); the wait for the previous P.V, which a rescale needs,
+//    is otherwise taken after P is published, off the critical path.  The
+//    same warps finish the unit (after moving the next unit's Q into TMEM,
+//    so its first scores overlap): O / l -> bf16 in shared memory, then one
+//    TMA store for a full tile, or coalesced 256-byte row stores for the
+//    last, partial tile of a sequence.
+//  * On the last KV tile the P.V thread zeroes the V rows between the last
+//    needed key and the next multiple of 16 (stale or unloaded data; P is 0
+//    there but 0 * NaN is not) and skips the 16-key steps past it.
 //  * Every mbarrier wait is bounded; a timeout records PA_DEV_TIMEOUT and
 //    the roles skip to the CTA-wide teardown.
-// TMEM: S0 = columns 0..127, S1 = 128..255, O = 256..383, P0/P1 = 384..511.
+// TMEM: Q = columns 0..63, S/P buffers at 128 and 256, O = 384..511.
 #include <math.h>
 
 #include <algorithm>
@@ -41,29 +51,29 @@ namespace pa {
 namespace {
 
 constexpr int D = 128;
-constexpr int BM = 128;                   // query rows per tile
-constexpr int BN = 128;                   // keys per tile
-constexpr int TILE_BYTES = BM * D * 2;    // 32 KiB
+constexpr int BM = 128;                     // query rows per tile
+constexpr int BN = 128;                     // keys per tile
+constexpr int TILE_BYTES = BM * D * 2;      // 32 KiB
 constexpr int HALF_BYTES = TILE_BYTES / 2;  // [128 rows][64 dims], 128-byte rows
-constexpr int NTHREADS = 352;
-constexpr int W_TMA = 0, W_MMA = 1, W_SOFT = 2, W_VTMA = 10;  // softmax warps 2..9
-// Softmax warp w reads TMEM lane quarter w % 4 (hardware rule) and key/dim
-// columns [64*h, 64*h + 64) with h = (w - 2) / 4: two warps share each row.
+constexpr int NTHREADS = 256;
+constexpr int W_QK = 0, W_MMA = 1, W_V = 2, W_PV = 3, W_SOFT = 4;  // softmax warps 4..7
+// Softmax warp w reads TMEM lane quarter w % 4 (hardware rule).
 
-constexpr int QST = 2;  // Q tiles (one per work tile in flight)
-constexpr int KST = 3;  // K ring stages (K is needed first: deepest prefetch)
-constexpr int VST = 2;  // V ring stages (V is needed after the softmax)
+constexpr int KST = 3;  // K ring stages
+constexpr int VST = 2;  // V ring stages
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + QST * TILE_BYTES;
+constexpr int OFF_K = OFF_Q + TILE_BYTES;
 constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
-constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
-enum { B_Q = 0, B_QEMPTY = B_Q + QST, B_KFULL = B_QEMPTY + QST, B_KEMPTY = B_KFULL + KST, B_VFULL = B_KEMPTY + KST,
-       B_SFULL = B_VFULL + VST, B_PFULL = B_SFULL + 2, B_PFREE = B_PFULL + 2, B_OFREE = B_PFREE + 2,
-       B_XCH = B_OFREE + 1 /* [4 quarters][2 slots] */, NBAR = B_XCH + 8 };
+constexpr int OFF_O = OFF_V + VST * TILE_BYTES;  // bf16 output tile, same [half][row][64] swizzled layout
+constexpr int OFF_BAR = OFF_O + TILE_BYTES;
+enum {
+    B_QFULL = 0, B_QEMPTY, B_QREADY, B_KFULL, B_KEMPTY = B_KFULL + KST, B_VFULL = B_KEMPTY + KST,
+    B_VEMPTY = B_VFULL + VST, B_SFULL = B_VEMPTY + VST, B_PFULL = B_SFULL + 2, B_PDONE = B_PFULL + 2,
+    B_OREADY = B_PDONE + 2, B_OEMPTY, B_DRAIN, B_DRAIN2, NBAR
+};
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int OFF_FLAGS = OFF_TMEM + 8;
-constexpr int OFF_XCH = OFF_FLAGS + 16;  // row-statistics exchange [4 quarters][2 slots][2 halves][32] f32
-constexpr int OFF_BID = OFF_XCH + 4 * 2 * 2 * 32 * 4;  // block ids of the current work tile, per producer
+constexpr int OFF_BID = OFF_FLAGS + 16;  // block ids of the current unit, per producer warp
 constexpr int NBID = 32;
 constexpr int SMEM_USED = OFF_BID + 2 * NBID * 4;
 // Slack for aligning the dynamic shared-memory base to the 1 KiB the swizzled
@@ -71,14 +81,13 @@ constexpr int SMEM_USED = OFF_BID + 2 * NBID * 4;
 constexpr int SMEM_SLACK = 256;
 constexpr size_t SMEM_BYTES = SMEM_USED + SMEM_SLACK;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(VST == 2, "V stages are released through the two P buffers' barriers");
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_O = 256;  // O accumulator, 128 fp32 columns
-constexpr uint32_t COL_P = 384;  // two P buffers, 64 columns each (128 keys as bf16 pairs)
-constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
+constexpr uint32_t COL_Q = 0, COL_S = 128, COL_O = 384;
+constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false, false);  // Q (TMEM) and K both K-major
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, false, true);   // P from TMEM, V MN-major
 constexpr uint32_t SBO = 1024;  // 8 rows x 128 B between core-matrix groups
+constexpr int SOFT_BAR = 1;     // named barrier of the softmax warps
 constexpr unsigned FULL = 0xffffffffu;
 
 struct PrefillArgs {
@@ -87,13 +96,15 @@ struct PrefillArgs {
     const int32_t *cu_k;
     const int32_t *bt;
     int32_t max_blocks, num_seqs, Hq, group, mtiles;
-    int32_t block_size, box_rows, paged, causal, num_blocks, checked;
+    int32_t block_size, box_rows, box_halves, paged, causal, num_blocks, checked;
     float scale_log2;
     DevError *err;
 };
 
+// Bounded wait; the abort flag is only read once the barrier is not yet complete.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *flags, DevError *err,
                                               int where) {
+    if (mbar_try_wait(smem_addr(bar), parity)) return true;
     if (flags[0]) return false;
     if (mbar_wait(bar, parity)) return true;
     record_error(err, PA_DEV_TIMEOUT, where);
@@ -111,49 +122,55 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-// Tile coordinates of work tile t: the highest query tiles (the most keys)
-// come first, then sequence, then q head (the heads of one kv group are
+// Byte offset of 16-byte chunk c (0..15) of row r in a [half][128 rows][64]
+// tile with 128-byte swizzle (the layout TMA writes and the MMA reads).
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+    return (uint32_t)((c >> 3) * HALF_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// Coordinates of work unit t: the highest query tiles (the most keys) come
+// first, then sequence, then q head (the heads of one kv head are
 // neighbours, so their K/V tiles are reused from L2).
-struct Tile {
+struct Unit {
     int s, h, m0, q0, Lq, k0, Lk, n_kv, key_end, valid;
 };
 
-__device__ __forceinline__ Tile tile_of(const PrefillArgs &a, int t) {
-    Tile T;
+__device__ __forceinline__ Unit unit_of(const PrefillArgs &a, int t) {
+    Unit U;
     const int per = a.num_seqs * a.Hq;
     const int mt = a.mtiles - 1 - t / per;
     const int rem = t % per;
-    T.s = rem / a.Hq;
-    T.h = rem % a.Hq;
-    T.m0 = mt * BM;
-    T.q0 = __ldg(a.cu_q + T.s);
-    T.Lq = __ldg(a.cu_q + T.s + 1) - T.q0;
-    T.k0 = __ldg(a.cu_k + T.s);
-    T.Lk = __ldg(a.cu_k + T.s + 1) - T.k0;
-    const bool bad = T.Lq < 0 || T.Lk < T.Lq || (a.paged && T.Lk > a.max_blocks * a.block_size);
-    T.valid = !bad && T.m0 < T.Lq;
-    if (bad && mt == 0 && T.h == 0 && threadIdx.x == 0) record_error(a.err, PA_DEV_BAD_SEQLENS, T.s);
-    T.key_end = 0;
-    T.n_kv = 0;
-    if (T.valid) {
-        const int c = T.Lk - T.Lq;
-        const int last_row = min(T.m0 + BM, T.Lq) - 1;
-        T.key_end = a.causal ? min(T.Lk, c + last_row + 1) : T.Lk;
-        T.n_kv = (T.key_end + BN - 1) / BN;
+    U.s = rem / a.Hq;
+    U.h = rem % a.Hq;
+    U.m0 = mt * BM;
+    U.q0 = __ldg(a.cu_q + U.s);
+    U.Lq = __ldg(a.cu_q + U.s + 1) - U.q0;
+    U.k0 = __ldg(a.cu_k + U.s);
+    U.Lk = __ldg(a.cu_k + U.s + 1) - U.k0;
+    const bool bad = U.Lq < 0 || U.Lk < U.Lq || (a.paged && U.Lk > a.max_blocks * a.block_size);
+    U.valid = !bad && U.m0 < U.Lq;
+    if (bad && mt == 0 && U.h == 0 && threadIdx.x == 0) record_error(a.err, PA_DEV_BAD_SEQLENS, U.s);
+    U.key_end = 0;
+    U.n_kv = 0;
+    if (U.valid) {
+        const int c = U.Lk - U.Lq;
+        const int last_row = min(U.m0 + BM, U.Lq) - 1;
+        U.key_end = a.causal ? min(U.Lk, c + last_row + 1) : U.Lk;
+        U.n_kv = (U.key_end + BN - 1) / BN;
     }
-    return T;
+    return U;
 }
 
-// First work tile >= t (stepping by gridDim.x) whose query rows exist.  The
-// warp tests 32 candidates per round of loads and takes the first by ballot,
-// so skipping the many empty high query tiles costs one load latency per 32.
+// First unit >= t (stepping by gridDim.x) whose query rows exist.  The warp
+// tests 32 candidates per round of loads and takes the first by ballot, so
+// skipping the many empty high query tiles costs one load latency per 32.
 // Every lane must call it; every role gets the same answer.
-__device__ __forceinline__ int next_valid_tile(const PrefillArgs &a, int t, int ntiles, int lane) {
+__device__ __forceinline__ int next_valid_unit(const PrefillArgs &a, int t, int nunits, int lane) {
     const int per = a.num_seqs * a.Hq;
-    for (int base = t; base < ntiles; base += 32 * (int)gridDim.x) {
+    for (int base = t; base < nunits; base += 32 * (int)gridDim.x) {
         const int tt = base + lane * (int)gridDim.x;
         bool v = false;
-        if (tt < ntiles) {
+        if (tt < nunits) {
             const int mt = a.mtiles - 1 - tt / per;
             const int s = (tt % per) / a.Hq;
             v = mt * BM < __ldg(a.cu_q + s + 1) - __ldg(a.cu_q + s);
@@ -161,12 +178,13 @@ __device__ __forceinline__ int next_valid_tile(const PrefillArgs &a, int t, int 
         const unsigned m = __ballot_sync(FULL, v);
         if (m) return base + (__ffs(m) - 1) * (int)gridDim.x;
     }
-    return ntiles;
+    return nunits;
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                   const PrefillArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
     if (pad > (uint32_t)SMEM_SLACK) {  // cannot align the tiles inside the allocation
@@ -178,14 +196,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + OFF_FLAGS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ntiles = a.mtiles * a.num_seqs * a.Hq;
+    const int nunits = a.mtiles * a.num_seqs * a.Hq;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NBAR; ++i) {
-            uint32_t cnt = 1;
-            if ((i >= B_PFULL && i < B_PFULL + 2) || i == B_OFREE) cnt = 8;
-            if (i >= B_XCH) cnt = 64;
-            mbar_init(&bar[i], cnt);
+            const bool per_warp = i == B_QEMPTY || i == B_QREADY || i == B_PFULL || i == B_PFULL + 1 || i == B_OEMPTY;
+            mbar_init(&bar[i], per_warp ? 4u : 1u);  // softmax warps arrive one each
         }
         flags[0] = 0;
         fence_mbar_init();
@@ -199,63 +215,49 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // Every role walks the same tiles t = blockIdx.x, +gridDim.x, ... and the
+    // Every role walks the same units t = blockIdx.x, +gridDim.x, ... and the
     // same global KV-tile counter g, so ring stages and barrier phases agree.
-    if (warp == W_TMA || warp == W_VTMA) {
+    if (warp == W_QK || warp == W_V) {
         // ------------------------------------------------------------ TMA producers
-        // Two independent streams: warp W_TMA loads Q and K, warp W_VTMA loads V,
-        // each as far ahead as its own ring allows (V is needed after the
-        // softmax, K before it, so neither waits behind the other).
-        const bool is_k = warp == W_TMA;
+        const bool is_k = warp == W_QK;
         const CUtensorMap *tm = is_k ? &tmk : &tmv;
         const int NS = is_k ? KST : VST;
         const int off = is_k ? OFF_K : OFF_V;
         uint64_t *full = &bar[is_k ? B_KFULL : B_VFULL];
-        // A V stage is free once the P.V that read it is complete: with as many V
-        // stages as P buffers, the P_FREE barrier of that P.V serves, and the
-        // producer waits on its phases in order.  The 3-stage K ring has its
-        // own release barriers (one phase per stage use).
+        uint64_t *empty = &bar[is_k ? B_KEMPTY : B_VEMPTY];
         int *bid = reinterpret_cast<int *>(smem + OFF_BID) + (is_k ? 0 : NBID);
         if (lane == 0) {
             if (is_k) prefetch_tensormap(&tmq);
             prefetch_tensormap(tm);
         }
         const int R = a.box_rows;
-        uint32_t g = 0, tk = 0;  // KV tiles and Q tiles issued by this warp
+        uint32_t g = 0, u = 0, nq = 0;  // KV tiles, units and Q copies issued by this warp
         bool ok = true;
-        for (int t = next_valid_tile(a, blockIdx.x, ntiles, lane); ok && t < ntiles;
-             t = next_valid_tile(a, t + gridDim.x, ntiles, lane)) {
-            const Tile T = tile_of(a, t);
-            const int32_t *bt = a.bt + (int64_t)T.s * a.max_blocks;
-            if (T.valid && a.paged) {
-                // The warp fetches the tile's first NBID block ids at once.
-                const int nblk = min((T.key_end - 1) / a.block_size + 1, NBID);
+        for (int t = next_valid_unit(a, blockIdx.x, nunits, lane); ok && t < nunits;
+             t = next_valid_unit(a, t + gridDim.x, nunits, lane)) {
+            const Unit U = unit_of(a, t);
+            const int32_t *bt = a.bt + (int64_t)U.s * a.max_blocks;
+            if (U.valid && a.paged) {
+                // The warp fetches the unit's first NBID block ids at once.
+                const int nblk = min((U.key_end - 1) / a.block_size + 1, NBID);
                 for (int b = lane; b < nblk; b += 32) bid[b] = __ldg(bt + b);
             }
             __syncwarp();
-            if (lane == 0 && T.valid) {
-                const int kvh = T.h / a.group;
+            if (lane == 0 && U.valid) {
+                const int kvh = U.h / a.group;
                 if (is_k) {
-                    const uint32_t qs = tk % QST;
-                    ok = wait_or_abort(&bar[B_QEMPTY + qs], ((tk / QST) & 1u) ^ 1u, flags, a.err, 400);
+                    ok = wait_or_abort(&bar[B_QEMPTY], (u & 1u) ^ 1u, flags, a.err, 400);
                     if (ok) {
-                        mbar_arrive_expect_tx(&bar[B_Q + qs], TILE_BYTES);
-                        uint8_t *qd = smem + OFF_Q + qs * TILE_BYTES;
-                        tma_load_3d_plain(qd, &tmq, 0, T.h, T.q0 + T.m0, &bar[B_Q + qs]);
-                        tma_load_3d_plain(qd + HALF_BYTES, &tmq, 64, T.h, T.q0 + T.m0, &bar[B_Q + qs]);
-                        ++tk;
+                        mbar_arrive_expect_tx(&bar[B_QFULL], TILE_BYTES);
+                        tma_load_4d_plain(smem + OFF_Q, &tmq, 0, U.q0 + U.m0, 0, U.h, &bar[B_QFULL]);
+                        ++nq;
                     }
                 }
-                for (int j = 0; ok && j < T.n_kv; ++j, ++g) {
+                for (int j = 0; ok && j < U.n_kv; ++j, ++g) {
                     const int st = g % NS;
                     const int kb = j * BN;
-                    const int nsub = (min(BN, T.key_end - kb) + R - 1) / R;
-                    if (is_k) {
-                        if (!(ok = wait_or_abort(&bar[B_KEMPTY + st], ((g / KST) & 1u) ^ 1u, flags, a.err, 401))) break;
-                    } else if (g >= (uint32_t)VST) {  // the P.V of tile g - VST read this stage
-                        const uint32_t u = g - VST;
-                        if (!(ok = wait_or_abort(&bar[B_PFREE + (u & 1)], (u >> 1) & 1u, flags, a.err, 402))) break;
-                    }
+                    const int nsub = (min(BN, U.key_end - kb) + R - 1) / R;
+                    if (!(ok = wait_or_abort(&empty[st], ((g / NS) & 1u) ^ 1u, flags, a.err, 401))) break;
                     mbar_arrive_expect_tx(&full[st], (uint32_t)nsub * R * D * 2);
                     uint8_t *dst = smem + off + st * TILE_BYTES;
                     for (int sub = 0; sub < nsub; ++sub) {
@@ -265,255 +267,284 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             const int lb = key / a.block_size;
                             const int blk = lb < NBID ? bid[lb] : __ldg(bt + lb);
                             if (a.checked && is_k && (blk < 0 || blk >= a.num_blocks))
-                                record_error(a.err, PA_DEV_BAD_BLOCK, (long long)T.s * a.max_blocks + lb);
+                                record_error(a.err, PA_DEV_BAD_BLOCK, (long long)U.s * a.max_blocks + lb);
                             // An invalid block id reads as zeros: TMA fills out-of-range boxes.
                             row = (blk < 0 || blk >= a.num_blocks) ? -2 * R : blk * a.block_size + key % a.block_size;
                         } else {
-                            row = T.k0 + key;
+                            row = U.k0 + key;
                         }
-                        tma_load_3d_plain(dst + sub * R * 128, tm, 0, kvh, row, &full[st]);
-                        tma_load_3d_plain(dst + HALF_BYTES + sub * R * 128, tm, 64, kvh, row, &full[st]);
+                        if (a.box_halves == 2) {
+                            tma_load_4d_plain(dst, tm, 0, row, 0, kvh, &full[st]);
+                        } else {
+                            tma_load_4d_plain(dst + sub * R * 128, tm, 0, row, 0, kvh, &full[st]);
+                            tma_load_4d_plain(dst + HALF_BYTES + sub * R * 128, tm, 0, row, 1, kvh, &full[st]);
+                        }
                     }
                 }
+                ++u;
             }
             ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
         }
         if (lane == 0 && !ok) {
             // Let issued copies land before the CTA's shared memory is released.
-            for (uint32_t x = (tk >= QST ? tk - QST : 0); x < tk; ++x)
-                (void)mbar_wait(&bar[B_Q + x % QST], (x / QST) & 1u);
+            if (is_k && nq > 0) (void)mbar_wait(&bar[B_QFULL], (nq - 1) & 1u);
             for (uint32_t x = (g >= (uint32_t)NS ? g - NS : 0); x < g; ++x) (void)mbar_wait(&full[x % NS], (x / NS) & 1u);
         }
-    } else if (warp == W_MMA) {
-        // ------------------------------------------------------------ MMA issuer
-        // The warp walks the tiles together; lane 0 waits and issues.
-        {
-            uint32_t g = 0, tk = 0;
-            int64_t last_pv = -1;  // global index of the last P.V issued
-            bool ok = true;
-            // O += P_gg V_gg; `first` overwrites O (first KV tile of a work tile).
-            auto issue_pv = [&](uint32_t gg, bool first) -> bool {
-                const int pb = gg & 1, vs = gg % VST;
-                if (first && tk > 1 &&
-                    !wait_or_abort(&bar[B_OFREE], (tk - 2) & 1u, flags, a.err, 410))  // previous epilogue read O
-                    return false;
-                // (The softmax publishes P only after V of the same tile has landed.)
-                if (!wait_or_abort(&bar[B_PFULL + pb], (gg >> 1) & 1u, flags, a.err, 411)) return false;
-                tc_fence_after();
-                // One descriptor per operand; each K=16 step only moves the start
-                // address (low 14 bits, in 16-byte units) by a constant.
-                const uint64_t vdesc = smem_desc_sw128(smem_addr(smem + OFF_V + vs * TILE_BYTES), HALF_BYTES, SBO);
-                const uint32_t pcol = tmem + COL_P + pb * 64;
+    } else if (warp == W_MMA || warp == W_PV) {
+        // ------------------------------------------------------------ MMA issuers (lane 0)
+        const bool is_qk = warp == W_MMA;
+        uint32_t g = 0, u = 0;  // KV tiles and units
+        bool ok = true, issued = false;
+        // S[buffer gk & 1] = Q K(gk)^T, Q from TMEM.
+        auto qk = [&](uint32_t gk) -> bool {
+            const int ks = gk % KST, sb = gk & 1;
+            if (!wait_or_abort(&bar[B_KFULL + ks], (gk / KST) & 1u, flags, a.err, 418)) return false;
+            // The P.V that read this buffer two tiles ago must be complete.
+            if (!wait_or_abort(&bar[B_PDONE + sb], ((gk >> 1) & 1u) ^ 1u, flags, a.err, 419)) return false;
+            tc_fence_after();
+            const uint64_t kdesc = smem_desc_sw128(smem_addr(smem + OFF_K + ks * TILE_BYTES), 16, SBO);
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k)  // 16 keys per step = 8 TMEM columns of P
-                    mma_bf16_ts(tmem + COL_O, pcol + k * 8, vdesc + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV,
-                                (!first || k > 0) ? 1u : 0u);
-                mma_commit(&bar[B_PFREE + pb]);
-                last_pv = gg;
-                return true;
-            };
-            // All MMAs of one work tile (lane 0 only); false on a timeout.
-            auto mma_tile = [&](const Tile &T) -> bool {
-                const uint32_t qs = tk % QST;
-                if (!wait_or_abort(&bar[B_Q + qs], (tk / QST) & 1u, flags, a.err, 413)) return false;
-                const uint64_t qdesc = smem_desc_sw128(smem_addr(smem + OFF_Q + qs * TILE_BYTES), 16, SBO);
-                ++tk;
-                for (int j = 0; j < T.n_kv; ++j, ++g) {
-                    const int st = g & 1, ks = g % KST;
-                    // (S buffer st is free: P of tile g-2 was published, so its S was read.)
-                    if (!wait_or_abort(&bar[B_KFULL + ks], (g / KST) & 1u, flags, a.err, 414)) return false;
-                    tc_fence_after();
-                    const uint64_t kdesc = smem_desc_sw128(smem_addr(smem + OFF_K + ks * TILE_BYTES), 16, SBO);
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint64_t off = (uint64_t)(((k >> 2) * HALF_BYTES + (k & 3) * 32) >> 4);
-                        mma_bf16_ss(tmem + st * BN, qdesc + off, kdesc + off, IDESC_S, k > 0 ? 1u : 0u);
-                    }
-                    mma_commit(&bar[B_KEMPTY + ks]);
-                    mma_commit(&bar[B_SFULL + st]);
-                    if (j == T.n_kv - 1) mma_commit(&bar[B_QEMPTY + qs]);  // this Q tile may be reloaded
-                    if (j >= 1 && !issue_pv(g - 1, j == 1)) return false;
-                }
-                return issue_pv(g - 1, T.n_kv == 1);
-            };
-            for (int t = next_valid_tile(a, blockIdx.x, ntiles, lane); ok && t < ntiles;
-                 t = next_valid_tile(a, t + gridDim.x, ntiles, lane)) {
-                if (lane == 0) {
-                    const Tile T = tile_of(a, t);
-                    if (T.valid) ok = mma_tile(T);
-                }
-                ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+            for (int k = 0; k < D / 16; ++k)  // 16 dims per step = 8 TMEM columns of Q
+                mma_bf16_ts(tmem + COL_S + sb * BN, tmem + COL_Q + k * 8,
+                            kdesc + (uint64_t)(((k >> 2) * HALF_BYTES + (k & 3) * 32) >> 4), IDESC_S,
+                            k > 0 ? 1u : 0u);
+            mma_commit(&bar[B_SFULL + sb]);
+            mma_commit(&bar[B_KEMPTY + ks]);
+            issued = true;
+            return true;
+        };
+        // O += P V for KV tile gv = g + jj of the current unit.
+        auto pv = [&](const Unit &U, int jj) -> bool {
+            const uint32_t gv = g + jj;
+            const int vs = gv % VST, sb = gv & 1;
+            if (jj == 0 && !wait_or_abort(&bar[B_OEMPTY], (u & 1u) ^ 1u, flags, a.err, 410)) return false;
+            if (!wait_or_abort(&bar[B_PFULL + sb], (gv >> 1) & 1u, flags, a.err, 412)) return false;
+            if (!wait_or_abort(&bar[B_VFULL + vs], (gv / VST) & 1u, flags, a.err, 414)) return false;
+            const int kend = min(BN, U.key_end - jj * BN);  // keys of this tile that are needed
+            const int kpad = (kend + 15) & ~15;
+            if (kend < kpad) {
+                // Rows kend..kpad-1 are read by the last 16-key step: zero them.
+                const uint32_t vb = smem_addr(smem + OFF_V + vs * TILE_BYTES);
+                for (int r = kend; r < kpad; ++r)
+                    for (int c = 0; c < 16; ++c) st_shared_v4(vb + sw128_off(r, c), 0, 0, 0, 0);
+                fence_proxy_async_smem();
             }
-            if (lane == 0 && !ok && last_pv >= 0) {
-                // Let the issued MMAs finish before TMEM is released.
-                (void)mbar_wait(&bar[B_PFREE + (last_pv & 1)], (uint32_t)(last_pv >> 1) & 1u);
+            tc_fence_after();
+            const uint64_t vdesc = smem_desc_sw128(smem_addr(smem + OFF_V + vs * TILE_BYTES), HALF_BYTES, SBO);
+            for (int k = 0; k < kpad / 16; ++k)  // 16 keys per step = 8 TMEM columns of P
+                mma_bf16_ts(tmem + COL_O, tmem + COL_S + sb * BN + k * 8, vdesc + (uint64_t)((k * 16 * 128) >> 4),
+                            IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
+            mma_commit(&bar[B_OREADY]);
+            mma_commit(&bar[B_VEMPTY + vs]);
+            mma_commit(&bar[B_PDONE + sb]);
+            issued = true;
+            return true;
+        };
+        // All lanes walk the units (next_valid_unit is warp-collective); lane 0
+        // waits and issues.
+        for (int t = next_valid_unit(a, blockIdx.x, nunits, lane); ok && t < nunits;
+             t = next_valid_unit(a, t + gridDim.x, nunits, lane)) {
+            const Unit U = unit_of(a, t);
+            if (!U.valid) continue;
+            if (lane == 0) {
+                if (is_qk) {
+                    ok = wait_or_abort(&bar[B_QREADY], u & 1u, flags, a.err, 416);
+                    if (ok) tc_fence_after();
+                    for (int j = 0; ok && j < U.n_kv; ++j) ok = qk(g + j);
+                } else {
+                    for (int j = 0; ok && j < U.n_kv; ++j) ok = pv(U, j);
+                }
             }
+            g += U.n_kv;
+            ++u;
+            ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+        }
+        if (lane == 0 && !ok && issued) {
+            // Let the issued MMAs finish before TMEM is released.
+            uint64_t *dr = &bar[is_qk ? B_DRAIN : B_DRAIN2];
+            mma_commit(dr);
+            (void)mbar_wait(dr, 0);
         }
     } else if (warp >= W_SOFT) {
-        // ------------------------------------------------------------ softmax
-        const int quarter = warp & 3, half = (warp - W_SOFT) >> 2;
+        // ------------------------------------------------------------ Q copy, softmax, epilogue
+        const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // tile row == TMEM lane
+        const int tid = threadIdx.x - W_SOFT * 32;  // 0..127
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t col0 = half * 64;      // this warp's 64 key columns of S and dim columns of O
-        float *xch = reinterpret_cast<float *>(smem + OFF_XCH) + quarter * 128;  // [2 slots][2 halves][32]
         const float sl = a.scale_log2;
-        uint32_t g = 0, xc = 0;  // KV tiles consumed; exchanges done with the partner warp
+        uint32_t gs = 0, u = 0, po = 0;  // S tiles consumed, units finished, P.V results waited for
         bool ok = true;
-        // Exchange one value per row with the partner warp (same rows, other
-        // half): slots alternate, so one bounded mbarrier wait per exchange.
-        auto exchange = [&](float v, float &partner) -> bool {
-            const uint32_t slot = xc & 1u;
-            float *x2 = xch + slot * 64;
-            x2[half * 32 + lane] = v;
-            mbar_arrive(&bar[B_XCH + quarter * 2 + slot]);
-            const bool done = __all_sync(FULL, wait_or_abort(&bar[B_XCH + quarter * 2 + slot], (xc >> 1) & 1u, flags,
-                                                              a.err, 425));
-            partner = x2[(half ^ 1) * 32 + lane];
-            ++xc;
-            return done;
+        // Waits in this role are warp-uniform: tcgen05.ld/st are warp-collective.
+        auto wwait = [&](uint64_t *b, uint32_t parity, int where) -> bool {
+            return __all_sync(FULL, wait_or_abort(b, parity, flags, a.err, where));
         };
-        for (int t = next_valid_tile(a, blockIdx.x, ntiles, lane); ok && t < ntiles;
-             t = next_valid_tile(a, t + gridDim.x, ntiles, lane)) {
-            const Tile T = tile_of(a, t);
-            if (!T.valid) continue;
-            const int i = T.m0 + row;          // query index in the sequence (>= Lq: padding row)
-            const int pos = (T.Lk - T.Lq) + i;
-            const int key_last = (a.causal ? min(pos, T.Lk - 1) : T.Lk - 1);  // last key this row sees
-            float m_run = -INFINITY;           // running max of raw scores (shared with the partner warp)
-            float l_run = 0.f;                 // this half's running sum
-            for (int j = 0; j < T.n_kv; ++j, ++g) {
-                const int sb = g & 1;
-                const uint32_t ph = (g >> 1) & 1u;
-                // Waits in this role are warp-uniform: tcgen05.ld/st are warp-collective.
-                if (!(ok = __all_sync(FULL, wait_or_abort(&bar[B_SFULL + sb], ph, flags, a.err, 420)))) break;
+        auto wait_o = [&]() -> bool {
+            const bool r = wwait(&bar[B_OREADY], po & 1u, 421);
+            ++po;
+            return r;
+        };
+        const uint32_t qs = smem_addr(smem + OFF_Q), os = smem_addr(smem + OFF_O);
+        // The next unit with work, from t on (next_valid_unit is warp-collective).
+        auto next_unit = [&](int t) -> int {
+            for (t = next_valid_unit(a, t, nunits, lane); t < nunits; t = next_valid_unit(a, t + gridDim.x, nunits, lane))
+                if (unit_of(a, t).valid) break;
+            return t;
+        };
+        // Unit uu's Q tile: shared memory -> TMEM (bf16 pairs, one row per lane).
+        // Its previous contents are free: this warp waited for the S of every
+        // earlier Q.K.
+        auto copy_q = [&](uint32_t uu) -> bool {
+            if (!wwait(&bar[B_QFULL], uu & 1u, 419)) return false;
+            uint32_t qw[64];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const uint4 v = ld_shared_v4(qs + sw128_off(row, c));
+                qw[4 * c] = v.x;
+                qw[4 * c + 1] = v.y;
+                qw[4 * c + 2] = v.z;
+                qw[4 * c + 3] = v.w;
+            }
+            tmem_st32(t_lane + COL_Q, *reinterpret_cast<uint32_t(*)[32]>(&qw[0]));
+            tmem_st32(t_lane + COL_Q + 32, *reinterpret_cast<uint32_t(*)[32]>(&qw[32]));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bar[B_QEMPTY]);  // the Q buffer may be reloaded
+                mbar_arrive(&bar[B_QREADY]);  // Q is in TMEM
+            }
+            return true;
+        };
+        int t = next_unit(blockIdx.x);
+        if (t < nunits) ok = copy_q(0);
+        while (ok && t < nunits) {
+            const Unit U = unit_of(a, t);
+            const int i = U.m0 + row;  // query index in the sequence (>= Lq: padding row)
+            const int pos = (U.Lk - U.Lq) + i;
+            const int key_last = (a.causal ? min(pos, U.Lk - 1) : U.Lk - 1);  // last key this row sees
+            float m_run = -INFINITY;  // running reference max of raw scores
+            float l_run = 0.f;        // running sum of P relative to it
+            for (int j = 0; j < U.n_kv; ++j, ++gs) {
+                const int sb = gs & 1;
+                const uint32_t cs = t_lane + COL_S + sb * BN;
+                if (!(ok = wwait(&bar[B_SFULL + sb], (gs >> 1) & 1u, 420))) break;
                 tc_fence_after();
-                // Each warp reads its 64 columns of the S row; the row max is
-                // shared with the partner warp (the other 64 columns).
-                uint32_t r[2][32];
-                tmem_ld32(t_lane + sb * BN + col0, r[0]);
-                tmem_ld32(t_lane + sb * BN + col0 + 32, r[1]);
+                uint32_t r[128];
+                tmem_ld32(cs, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                tmem_ld32(cs + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                tmem_ld32(cs + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+                tmem_ld32(cs + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
                 tmem_ld_wait();
-
-                const int kb = j * BN + col0;
-                const int lim = key_last - kb;  // this warp's keys kb+k with k <= lim are visible
-                float x[64];
+                const int lim = key_last - j * BN;  // keys j*BN + k with k <= lim are visible
+                if (__any_sync(FULL, lim < BN - 1)) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    x[e] = __uint_as_float(r[0][e]);
-                    x[32 + e] = __uint_as_float(r[1][e]);
+                    for (int k = 0; k < BN; ++k)
+                        if (k > lim) r[k] = __float_as_uint(-INFINITY);
                 }
-                if (__any_sync(FULL, lim < 63)) {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int k = 0; k < 64; ++k)
-                        if (k > lim) x[k] = -INFINITY;
-                }
-                float mx[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mx[e] = x[e];
-#pragma unroll
-                for (int k = 8; k < 64; k += 8)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], x[k + e]);
-                float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                float tpart;
-                if (!(ok = exchange(tmax, tpart))) break;
-                tmax = fmaxf(tmax, tpart);
+                for (int k = 0; k < BN; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(r[k]));
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 // Lazy rescaling: keep the old max unless this tile's max exceeds it
                 // by more than 8 in log2 units (P then stays <= 2^8).
-                const bool grow = (tmax - m_run) * sl > 8.f;
-                const float m_new = grow ? tmax : m_run;
+                const bool grow = (mx - m_run) * sl > 8.f;
+                const float m_new = grow ? mx : m_run;
                 const float alpha = grow ? fast_exp2((m_run - m_new) * sl) : 1.f;
-                if (__any_sync(FULL, grow) && j > 0) {
-                    // O holds the previous tiles' P.V: wait for the last one, then
-                    // rescale this warp's 64 columns of O.
-                    const uint32_t pg = g - 1;
-                    ok = __all_sync(FULL, wait_or_abort(&bar[B_PFREE + (pg & 1)], (pg >> 1) & 1u, flags, a.err, 421));
-                    if (!ok) break;
+                bool waited = j == 0;  // tile 0: no earlier P.V of this unit to wait for
+                if (j > 0 && __any_sync(FULL, grow)) {
+                    // O must hold P.V up to tile j-1 before it is rescaled.
+                    if (!(ok = wait_o())) break;
+                    waited = true;
                     tc_fence_after();
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
                         uint32_t o[32];
-                        tmem_ld32(t_lane + COL_O + col0 + cc * 32, o);
+                        tmem_ld32(t_lane + COL_O + c * 32, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(t_lane + COL_O + col0 + cc * 32, o);
+                        tmem_st32(t_lane + COL_O + c * 32, o);
                     }
-                    tmem_st_wait();
                 }
                 l_run *= alpha;
                 m_run = m_new;
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run * sl;
-                if (g >= 2 && !(ok = __all_sync(FULL, wait_or_abort(&bar[B_PFREE + sb], ph ^ 1u, flags, a.err, 422))))
-                    break;
-                // This warp's 64 keys become 32 TMEM columns of bf16 pairs (the A
-                // operand of the P.V MMA), in this buffer's half `half`.
+                // P = 2^(s*scale - m) as bf16 pairs over the first 64 columns of the buffer.
                 float rs[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[32];
+                uint32_t pk[64];
 #pragma unroll
-                for (int k2 = 0; k2 < 32; ++k2) {
-                    const float p0 = fast_exp2(fmaf(x[2 * k2], sl, neg_m));
-                    const float p1 = fast_exp2(fmaf(x[2 * k2 + 1], sl, neg_m));
+                for (int k2 = 0; k2 < 64; ++k2) {
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * k2]), sl, neg_m));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * k2 + 1]), sl, neg_m));
                     rs[(2 * k2) & 3] += p0;
                     rs[(2 * k2 + 1) & 3] += p1;
                     pk[k2] = pack_bf16(p0, p1);
                 }
-                tmem_st32(t_lane + COL_P + sb * 64 + half * 32, pk);
+                tmem_st32(cs, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+                tmem_st32(cs + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
                 tmem_st_wait();
                 l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-                const int kend = T.key_end - j * BN;
-                const int vs = g % VST;
-                // V of this tile must have landed before P is published (the MMA
-                // thread then issues P.V without its own wait).
-                if (!(ok = __all_sync(FULL, wait_or_abort(&bar[B_VFULL + vs], (g / VST) & 1u, flags, a.err, 423))))
-                    break;
-                if (j == T.n_kv - 1 && kend < BN) {
-                    // Rows past the last needed key hold stale or unloaded data:
-                    // zero them (this warp: one 64-dim half) so 0 * garbage cannot reach O.
-                    if (row >= kend) {
-                        const uint32_t vrow = smem_addr(smem + OFF_V + vs * TILE_BYTES) + half * HALF_BYTES + row * 128;
-#pragma unroll
-                        for (int q16 = 0; q16 < 8; ++q16) st_shared_v4(vrow + q16 * 16, 0, 0, 0, 0);
-                    }
-                }
-                fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[B_PFULL + sb]);
+                // The previous tile's P.V, if not waited for above (keeps one wait per P.V, in order).
+                if (!waited && !(ok = wait_o())) break;
             }
             if (!ok) break;
-            // ---- epilogue: O / l -> bf16; this warp writes its 64 dims of each row
-            const uint32_t pg = g - 1;
-            if (!(ok = __all_sync(FULL, wait_or_abort(&bar[B_PFREE + (pg & 1)], (pg >> 1) & 1u, flags, a.err, 424))))
-                break;
+            // The next unit's Q goes into TMEM now, so its first Q.K overlap this epilogue.
+            const int tn = next_unit(t + gridDim.x);
+            if (tn < nunits && !(ok = copy_q(u + 1))) break;
+            // ---- epilogue: O / l -> bf16 tile in shared memory -> global memory
+            if (!(ok = wait_o())) break;
             tc_fence_after();
-            uint32_t o[2][32];
-            tmem_ld32(t_lane + COL_O + col0, o[0]);
-            tmem_ld32(t_lane + COL_O + col0 + 32, o[1]);
+            uint32_t o[128];
+            tmem_ld32(t_lane + COL_O, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+            tmem_ld32(t_lane + COL_O + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+            tmem_ld32(t_lane + COL_O + 64, *reinterpret_cast<uint32_t(*)[32]>(&o[64]));
+            tmem_ld32(t_lane + COL_O + 96, *reinterpret_cast<uint32_t(*)[32]>(&o[96]));
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[B_OFREE]);  // O may be overwritten by the next tile
-            float lpart;
-            if (!(ok = exchange(l_run, lpart))) break;
-            const float l_tot = l_run + lpart;
-            if (i < T.Lq) {
-                const float inv = 1.f / l_tot;
-                uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((int64_t)(T.q0 + i) * a.Hq + T.h) * D + col0);
+            if (lane == 0) mbar_arrive(&bar[B_OEMPTY]);  // O may be overwritten by the next unit
+            // The previous unit's tile store must have read the staging tile.
+            if (tid == 0) bulk_wait_read0();
+            named_bar_sync(SOFT_BAR, 128);
+            const float inv = 1.f / l_run;
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t *v = &o[cc][8 * e];
-                        dst[cc * 4 + e] = make_uint4(
-                            pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
-                            pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
-                            pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
-                            pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
-                    }
+            for (int c = 0; c < 16; ++c) {
+                const uint32_t *v = &o[8 * c];
+                st_shared_v4(os + sw128_off(row, c),
+                             pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                             pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                             pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                             pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
             }
+            const int nrows = min(BM, U.Lq - U.m0);
+            if (nrows == BM) {
+                fence_proxy_async_smem();  // the tile store reads the staging tile through the async proxy
+                named_bar_sync(SOFT_BAR, 128);
+                if (tid == 0) {
+                    tma_store_4d(&tmo, smem + OFF_O, 0, U.q0 + U.m0, 0, U.h);
+                    bulk_commit_group();
+                }
+            } else {
+                // The last tile of a sequence: rows past Lq belong to the next
+                // sequence, so only the valid rows are written, 16 threads per row.
+                named_bar_sync(SOFT_BAR, 128);
+#pragma unroll 4
+                for (int it = 0; it < BM * 16 / 128; ++it) {
+                    const int q = it * 128 + tid, rr = q >> 4, c = q & 15;
+                    if (rr < nrows) {
+                        const uint4 v = ld_shared_v4(os + sw128_off(rr, c));
+                        *reinterpret_cast<uint4 *>(a.out + ((int64_t)(U.q0 + U.m0 + rr) * a.Hq + U.h) * D + c * 8) = v;
+                    }
+                }
+                named_bar_sync(SOFT_BAR, 128);  // the staging tile may be rewritten
+            }
+            ++u;
+            t = tn;
         }
+        if (tid == 0) bulk_wait0();  // tile stores complete before the CTA exits
     }
     tc_fence_before();
     __syncthreads();
@@ -551,9 +582,9 @@ extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_s
     if (!(softmax_scale > 0.f) || !isfinite(softmax_scale))
         return fail(PA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
     const bool paged = block_tables != nullptr;
-    int R = 128;
+    int R = BN;
     CUtensorMap tq, tk, tv;
-    pa_status st = encode_tensor_map_3d(&tq, q, D, num_q_heads, total_q, D * 2, q_row_stride * 2, 64, BM, true);
+    pa_status st = encode_halves_map(&tq, q, total_q, q_row_stride * 2, num_q_heads, BM, 2);
     if (st != PA_OK) return st;
     if (paged) {
         if (block_size <= 0 || block_size % 16)
@@ -564,17 +595,21 @@ extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_s
             (int64_t)max_blocks_per_seq * block_size > 0x7fffffffLL)
             return fail(PA_ERR_UNSUPPORTED, "pool or table too large for 32-bit slot indices");
         while (block_size % R) R >>= 1;  // gcd(block_size, 128) in {16, 32, 64, 128}
-        const int64_t slots = (int64_t)num_blocks * block_size;
-        const int64_t rs = (int64_t)num_kv_heads * D * 2;
-        st = encode_tensor_map_3d(&tk, k, D, num_kv_heads, slots, D * 2, rs, 64, R, true);
-        if (st == PA_OK) st = encode_tensor_map_3d(&tv, v, D, num_kv_heads, slots, D * 2, rs, 64, R, true);
     } else {
         if (total_k <= 0) return fail(PA_ERR_INVALID_ARG, "total_k must be positive for contiguous k/v");
         if (kv_row_stride < (int64_t)num_kv_heads * D || kv_row_stride % 8)
             return fail(PA_ERR_INVALID_ARG, "kv_row_stride must be >= num_kv_heads*head_dim and a multiple of 8");
-        st = encode_tensor_map_3d(&tk, k, D, num_kv_heads, total_k, D * 2, kv_row_stride * 2, 64, R, true);
-        if (st == PA_OK) st = encode_tensor_map_3d(&tv, v, D, num_kv_heads, total_k, D * 2, kv_row_stride * 2, 64, R, true);
     }
+    // A box of BN rows holds a whole K/V tile in [half][row][64] order;
+    // shorter boxes (small blocks) are fetched one 64-dim half at a time.
+    const int halves = R == BN ? 2 : 1;
+    const int64_t kv_rows = paged ? (int64_t)num_blocks * block_size : (int64_t)total_k;
+    const int64_t kv_stride = paged ? (int64_t)num_kv_heads * D * 2 : kv_row_stride * 2;
+    st = encode_halves_map(&tk, k, kv_rows, kv_stride, num_kv_heads, R, halves);
+    if (st == PA_OK) st = encode_halves_map(&tv, v, kv_rows, kv_stride, num_kv_heads, R, halves);
+    // Output tiles of 128 full rows go out by TMA store.
+    CUtensorMap to;
+    if (st == PA_OK) st = encode_halves_map(&to, out, total_q, (int64_t)num_q_heads * D * 2, num_q_heads, BM, 2);
     if (st != PA_OK) return st;
 
     PrefillArgs A;
@@ -589,6 +624,7 @@ extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_s
     A.mtiles = (max_seqlen_q + BM - 1) / BM;
     A.block_size = paged ? block_size : 1;
     A.box_rows = R;
+    A.box_halves = halves;
     A.paged = paged ? 1 : 0;
     A.causal = causal ? 1 : 0;
     A.num_blocks = num_blocks;
@@ -609,6 +645,6 @@ extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_s
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_kernel)");
         g_attr_done[dev] = 1;
     }
-    prefill_kernel<<<(unsigned)grid, NTHREADS, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(tq, tk, tv, A);
+    prefill_kernel<<<(unsigned)grid, NTHREADS, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, A);
     return check_launch("prefill_kernel");
 }
