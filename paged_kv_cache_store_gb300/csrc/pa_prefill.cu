@@ -112,6 +112,32 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     return false;
 }
 
+// Softmax arithmetic with fewer instructions per score: a three-input max,
+// and fp32x2 (two-lane) fma/add, all native on sm_100-class SMs.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -443,7 +469,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int k = 0; k < BN; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(r[k]));
+                for (int k2 = 0; k2 < BN / 2; ++k2)
+                    m4[k2 & 3] = max3f(m4[k2 & 3], __uint_as_float(r[2 * k2]), __uint_as_float(r[2 * k2 + 1]));
                 const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 // Lazy rescaling: keep the old max unless this tile's max exceeds it
                 // by more than 8 in log2 units (P then stays <= 2^8).
@@ -470,20 +497,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 m_run = m_new;
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run * sl;
                 // P = 2^(s*scale - m) as bf16 pairs over the first 64 columns of the buffer.
-                float rs[4] = {0.f, 0.f, 0.f, 0.f};
+                float2 rs[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+                const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(neg_m, neg_m);
                 uint32_t pk[64];
 #pragma unroll
                 for (int k2 = 0; k2 < 64; ++k2) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * k2]), sl, neg_m));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * k2 + 1]), sl, neg_m));
-                    rs[(2 * k2) & 3] += p0;
-                    rs[(2 * k2 + 1) & 3] += p1;
-                    pk[k2] = pack_bf16(p0, p1);
+                    const float2 xx =
+                        fma2(make_float2(__uint_as_float(r[2 * k2]), __uint_as_float(r[2 * k2 + 1])), sl2, nm2);
+                    const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+                    rs[k2 & 3] = add2(rs[k2 & 3], pp);
+                    pk[k2] = pack_bf16(pp.x, pp.y);
                 }
                 tmem_st32(cs, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
                 tmem_st32(cs + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
                 tmem_st_wait();
-                l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+                l_run += ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y)) + ((rs[2].x + rs[2].y) + (rs[3].x + rs[3].y));
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[B_PFULL + sb]);
