@@ -8,21 +8,18 @@
 //
 // How (GB300 design): persistent CTAs (one per SM) walk work units of
 // (128-row query tile, sequence, q head), highest query tiles first.
-//  * warp 0 issues the TMA copies of Q and K, warp 2 those of V (rings: K 3
-//    stages, V 2 stages of 128 keys; one Q tile).  Tiles land 128-byte
+//  * warp 0 issues the TMA copies of Q and K, warp 2 those of V (rings: Q 2,
+//    K 3 and V 2 stages; K/V tiles of 128 keys).  Tiles land 128-byte
 //    swizzled as [half][row][64] through 4-D tensor maps that view a
 //    [rows][heads][128] tensor as [head][half][row][64]: one copy per tile
 //    when blocks hold 128 rows or more.
-//  * The softmax warps move the unit's Q tile from shared memory into TMEM
-//    (bf16 pairs, one row per lane), so both products take their A operand
-//    from TMEM and only K and V are read from shared memory by the tensor
-//    cores.
 //  * Two single-thread MMA issuers feed the tensor cores, so one's barrier
 //    waits overlap the other's MMAs: warp 1 issues S = Q.K^T (M=N=128, K=128,
-//    8 steps) into one of two S buffers, warp 3 issues O += P.V with P read
-//    from TMEM (bf16 pairs written over its S buffer) and V as an MN-major
-//    operand.  Scores run ahead of P.V by up to two tiles; a Q.K waits until
-//    the P.V that read its buffer two tiles earlier has completed.
+//    8 steps; both operands from shared memory) into one of three S buffers,
+//    warp 3 issues O += P.V with P read from TMEM (bf16 pairs written over
+//    its S buffer) and V as an MN-major operand.  Scores run up to three
+//    tiles ahead of P.V; a Q.K waits until the P.V that read its buffer three
+//    tiles earlier has completed.
 //    tcgen05.commit arrives on mbarriers to free K/V stages and S buffers,
 //    publish S and report O.
 //  * warps 4..7: one thread per query row (its TMEM lane) holds all 128
@@ -31,16 +28,17 @@
 //    row's max grows by more than 2^8 (P then stays <= 256, exact enough in
 //    bf16 and fp32); the wait for the previous P.V, which a rescale needs,
 //    is otherwise taken after P is published, off the critical path.  The
-//    same warps finish the unit (after moving the next unit's Q into TMEM,
-//    so its first scores overlap): O / l -> bf16 in shared memory, then one
-//    TMA store for a full tile, or coalesced 256-byte row stores for the
-//    last, partial tile of a sequence.
+//    same warps finish the unit: O / l -> bf16 into the unit's Q buffer (no
+//    longer read once its last S is in), then one TMA store for a full tile,
+//    or coalesced 256-byte row stores for the last, partial tile of a
+//    sequence; the buffer is released for a later Q when that store has read
+//    it.
 //  * On the last KV tile the P.V thread zeroes the V rows between the last
 //    needed key and the next multiple of 16 (stale or unloaded data; P is 0
 //    there but 0 * NaN is not) and skips the 16-key steps past it.
 //  * Every mbarrier wait is bounded; a timeout records PA_DEV_TIMEOUT and
 //    the roles skip to the CTA-wide teardown.
-// TMEM: Q = columns 0..63, S/P buffers at 128 and 256, O = 384..511.
+// TMEM: S/P buffers at columns 0, 128 and 256, O = 384..511.
 #include <math.h>
 
 #include <algorithm>
@@ -59,17 +57,18 @@ constexpr int NTHREADS = 256;
 constexpr int W_QK = 0, W_MMA = 1, W_V = 2, W_PV = 3, W_SOFT = 4;  // softmax warps 4..7
 // Softmax warp w reads TMEM lane quarter w % 4 (hardware rule).
 
+constexpr int QST = 2;  // Q buffers (a finished unit's buffer stages its output tile)
 constexpr int KST = 3;  // K ring stages
 constexpr int VST = 2;  // V ring stages
+constexpr int NSB = 3;  // S/P buffers in TMEM
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE_BYTES;
+constexpr int OFF_K = OFF_Q + QST * TILE_BYTES;
 constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
-constexpr int OFF_O = OFF_V + VST * TILE_BYTES;  // bf16 output tile, same [half][row][64] swizzled layout
-constexpr int OFF_BAR = OFF_O + TILE_BYTES;
+constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
 enum {
-    B_QFULL = 0, B_QEMPTY, B_QREADY, B_KFULL, B_KEMPTY = B_KFULL + KST, B_VFULL = B_KEMPTY + KST,
-    B_VEMPTY = B_VFULL + VST, B_SFULL = B_VEMPTY + VST, B_PFULL = B_SFULL + 2, B_PDONE = B_PFULL + 2,
-    B_OREADY = B_PDONE + 2, B_OEMPTY, B_DRAIN, B_DRAIN2, NBAR
+    B_QFULL = 0, B_QEMPTY = B_QFULL + QST, B_KFULL = B_QEMPTY + QST, B_KEMPTY = B_KFULL + KST,
+    B_VFULL = B_KEMPTY + KST, B_VEMPTY = B_VFULL + VST, B_SFULL = B_VEMPTY + VST, B_PFULL = B_SFULL + NSB,
+    B_PDONE = B_PFULL + NSB, B_OREADY = B_PDONE + NSB, B_OEMPTY, B_DRAIN, B_DRAIN2, NBAR
 };
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int OFF_FLAGS = OFF_TMEM + 8;
@@ -83,8 +82,8 @@ constexpr size_t SMEM_BYTES = SMEM_USED + SMEM_SLACK;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_Q = 0, COL_S = 128, COL_O = 384;
-constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false, false);  // Q (TMEM) and K both K-major
+constexpr uint32_t COL_S = 0, COL_O = 384;
+constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false, false);  // Q and K both K-major
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, false, true);   // P from TMEM, V MN-major
 constexpr uint32_t SBO = 1024;  // 8 rows x 128 B between core-matrix groups
 constexpr int SOFT_BAR = 1;     // named barrier of the softmax warps
@@ -226,7 +225,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NBAR; ++i) {
-            const bool per_warp = i == B_QEMPTY || i == B_QREADY || i == B_PFULL || i == B_PFULL + 1 || i == B_OEMPTY;
+            const bool per_warp = (i >= B_PFULL && i < B_PFULL + NSB) || i == B_OEMPTY;
             mbar_init(&bar[i], per_warp ? 4u : 1u);  // softmax warps arrive one each
         }
         flags[0] = 0;
@@ -272,10 +271,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (lane == 0 && U.valid) {
                 const int kvh = U.h / a.group;
                 if (is_k) {
-                    ok = wait_or_abort(&bar[B_QEMPTY], (u & 1u) ^ 1u, flags, a.err, 400);
+                    const int qb = u % QST;
+                    ok = wait_or_abort(&bar[B_QEMPTY + qb], ((u / QST) & 1u) ^ 1u, flags, a.err, 400);
                     if (ok) {
-                        mbar_arrive_expect_tx(&bar[B_QFULL], TILE_BYTES);
-                        tma_load_4d_plain(smem + OFF_Q, &tmq, 0, U.q0 + U.m0, 0, U.h, &bar[B_QFULL]);
+                        mbar_arrive_expect_tx(&bar[B_QFULL + qb], TILE_BYTES);
+                        tma_load_4d_plain(smem + OFF_Q + qb * TILE_BYTES, &tmq, 0, U.q0 + U.m0, 0, U.h,
+                                          &bar[B_QFULL + qb]);
                         ++nq;
                     }
                 }
@@ -313,7 +314,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (lane == 0 && !ok) {
             // Let issued copies land before the CTA's shared memory is released.
-            if (is_k && nq > 0) (void)mbar_wait(&bar[B_QFULL], (nq - 1) & 1u);
+            for (uint32_t x = (nq >= (uint32_t)QST ? nq - QST : 0); is_k && x < nq; ++x)
+                (void)mbar_wait(&bar[B_QFULL + x % QST], (x / QST) & 1u);
             for (uint32_t x = (g >= (uint32_t)NS ? g - NS : 0); x < g; ++x) (void)mbar_wait(&full[x % NS], (x / NS) & 1u);
         }
     } else if (warp == W_MMA || warp == W_PV) {
@@ -322,18 +324,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint32_t g = 0, u = 0;  // KV tiles and units
         bool ok = true, issued = false;
         // S[buffer gk & 1] = Q K(gk)^T, Q from TMEM.
+        uint64_t qdesc = 0;
         auto qk = [&](uint32_t gk) -> bool {
-            const int ks = gk % KST, sb = gk & 1;
+            const int ks = gk % KST, sb = gk % NSB;
             if (!wait_or_abort(&bar[B_KFULL + ks], (gk / KST) & 1u, flags, a.err, 418)) return false;
-            // The P.V that read this buffer two tiles ago must be complete.
-            if (!wait_or_abort(&bar[B_PDONE + sb], ((gk >> 1) & 1u) ^ 1u, flags, a.err, 419)) return false;
+            // The P.V that read this buffer NSB tiles ago must be complete.
+            if (!wait_or_abort(&bar[B_PDONE + sb], ((gk / NSB) & 1u) ^ 1u, flags, a.err, 419)) return false;
             tc_fence_after();
             const uint64_t kdesc = smem_desc_sw128(smem_addr(smem + OFF_K + ks * TILE_BYTES), 16, SBO);
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k)  // 16 dims per step = 8 TMEM columns of Q
-                mma_bf16_ts(tmem + COL_S + sb * BN, tmem + COL_Q + k * 8,
-                            kdesc + (uint64_t)(((k >> 2) * HALF_BYTES + (k & 3) * 32) >> 4), IDESC_S,
-                            k > 0 ? 1u : 0u);
+            for (int k = 0; k < D / 16; ++k) {
+                const uint64_t o = (uint64_t)(((k >> 2) * HALF_BYTES + (k & 3) * 32) >> 4);
+                mma_bf16_ss(tmem + COL_S + sb * BN, qdesc + o, kdesc + o, IDESC_S, k > 0 ? 1u : 0u);
+            }
             mma_commit(&bar[B_SFULL + sb]);
             mma_commit(&bar[B_KEMPTY + ks]);
             issued = true;
@@ -342,9 +345,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // O += P V for KV tile gv = g + jj of the current unit.
         auto pv = [&](const Unit &U, int jj) -> bool {
             const uint32_t gv = g + jj;
-            const int vs = gv % VST, sb = gv & 1;
+            const int vs = gv % VST, sb = gv % NSB;
             if (jj == 0 && !wait_or_abort(&bar[B_OEMPTY], (u & 1u) ^ 1u, flags, a.err, 410)) return false;
-            if (!wait_or_abort(&bar[B_PFULL + sb], (gv >> 1) & 1u, flags, a.err, 412)) return false;
+            if (!wait_or_abort(&bar[B_PFULL + sb], (gv / NSB) & 1u, flags, a.err, 412)) return false;
             if (!wait_or_abort(&bar[B_VFULL + vs], (gv / VST) & 1u, flags, a.err, 414)) return false;
             const int kend = min(BN, U.key_end - jj * BN);  // keys of this tile that are needed
             const int kpad = (kend + 15) & ~15;
@@ -374,8 +377,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!U.valid) continue;
             if (lane == 0) {
                 if (is_qk) {
-                    ok = wait_or_abort(&bar[B_QREADY], u & 1u, flags, a.err, 416);
-                    if (ok) tc_fence_after();
+                    ok = wait_or_abort(&bar[B_QFULL + u % QST], (u / QST) & 1u, flags, a.err, 416);
+                    qdesc = smem_desc_sw128(smem_addr(smem + OFF_Q + (u % QST) * TILE_BYTES), 16, SBO);
                     for (int j = 0; ok && j < U.n_kv; ++j) ok = qk(g + j);
                 } else {
                     for (int j = 0; ok && j < U.n_kv; ++j) ok = pv(U, j);
@@ -392,7 +395,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             (void)mbar_wait(dr, 0);
         }
     } else if (warp >= W_SOFT) {
-        // ------------------------------------------------------------ Q copy, softmax, epilogue
+        // ------------------------------------------------------------ softmax, epilogue
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // tile row == TMEM lane
         const int tid = threadIdx.x - W_SOFT * 32;  // 0..127
@@ -409,40 +412,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ++po;
             return r;
         };
-        const uint32_t qs = smem_addr(smem + OFF_Q), os = smem_addr(smem + OFF_O);
         // The next unit with work, from t on (next_valid_unit is warp-collective).
         auto next_unit = [&](int t) -> int {
             for (t = next_valid_unit(a, t, nunits, lane); t < nunits; t = next_valid_unit(a, t + gridDim.x, nunits, lane))
                 if (unit_of(a, t).valid) break;
             return t;
         };
-        // Unit uu's Q tile: shared memory -> TMEM (bf16 pairs, one row per lane).
-        // Its previous contents are free: this warp waited for the S of every
-        // earlier Q.K.
-        auto copy_q = [&](uint32_t uu) -> bool {
-            if (!wwait(&bar[B_QFULL], uu & 1u, 419)) return false;
-            uint32_t qw[64];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint4 v = ld_shared_v4(qs + sw128_off(row, c));
-                qw[4 * c] = v.x;
-                qw[4 * c + 1] = v.y;
-                qw[4 * c + 2] = v.z;
-                qw[4 * c + 3] = v.w;
-            }
-            tmem_st32(t_lane + COL_Q, *reinterpret_cast<uint32_t(*)[32]>(&qw[0]));
-            tmem_st32(t_lane + COL_Q + 32, *reinterpret_cast<uint32_t(*)[32]>(&qw[32]));
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bar[B_QEMPTY]);  // the Q buffer may be reloaded
-                mbar_arrive(&bar[B_QREADY]);  // Q is in TMEM
-            }
-            return true;
-        };
         int t = next_unit(blockIdx.x);
-        if (t < nunits) ok = copy_q(0);
         while (ok && t < nunits) {
             const Unit U = unit_of(a, t);
             const int i = U.m0 + row;  // query index in the sequence (>= Lq: padding row)
@@ -451,9 +427,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float m_run = -INFINITY;  // running reference max of raw scores
             float l_run = 0.f;        // running sum of P relative to it
             for (int j = 0; j < U.n_kv; ++j, ++gs) {
-                const int sb = gs & 1;
+                const int sb = gs % NSB;
                 const uint32_t cs = t_lane + COL_S + sb * BN;
-                if (!(ok = wwait(&bar[B_SFULL + sb], (gs >> 1) & 1u, 420))) break;
+                if (!(ok = wwait(&bar[B_SFULL + sb], (gs / NSB) & 1u, 420))) break;
                 tc_fence_after();
                 uint32_t r[128];
                 tmem_ld32(cs, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
@@ -519,9 +495,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!waited && !(ok = wait_o())) break;
             }
             if (!ok) break;
-            // The next unit's Q goes into TMEM now, so its first Q.K overlap this epilogue.
             const int tn = next_unit(t + gridDim.x);
-            if (tn < nunits && !(ok = copy_q(u + 1))) break;
             // ---- epilogue: O / l -> bf16 tile in shared memory -> global memory
             if (!(ok = wait_o())) break;
             tc_fence_after();
@@ -534,9 +508,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[B_OEMPTY]);  // O may be overwritten by the next unit
-            // The previous unit's tile store must have read the staging tile.
-            if (tid == 0) bulk_wait_read0();
-            named_bar_sync(SOFT_BAR, 128);
+            // This unit's Q buffer stages the output tile: every Q.K that read it
+            // is complete (this warp waited for the unit's last S).
+            const uint32_t os = smem_addr(smem + OFF_Q + (u % QST) * TILE_BYTES);
             const float inv = 1.f / l_run;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
@@ -552,8 +526,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 fence_proxy_async_smem();  // the tile store reads the staging tile through the async proxy
                 named_bar_sync(SOFT_BAR, 128);
                 if (tid == 0) {
-                    tma_store_4d(&tmo, smem + OFF_O, 0, U.q0 + U.m0, 0, U.h);
+                    tma_store_4d(&tmo, smem + OFF_Q + (u % QST) * TILE_BYTES, 0, U.q0 + U.m0, 0, U.h);
                     bulk_commit_group();
+                    bulk_wait_read0();  // the store has read the tile: the buffer may take a later Q
+                    mbar_arrive(&bar[B_QEMPTY + u % QST]);
                 }
             } else {
                 // The last tile of a sequence: rows past Lq belong to the next
@@ -567,7 +543,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         *reinterpret_cast<uint4 *>(a.out + ((int64_t)(U.q0 + U.m0 + rr) * a.Hq + U.h) * D + c * 8) = v;
                     }
                 }
-                named_bar_sync(SOFT_BAR, 128);  // the staging tile may be rewritten
+                named_bar_sync(SOFT_BAR, 128);  // the staging tile was read: it may take a later Q
+                if (tid == 0) mbar_arrive(&bar[B_QEMPTY + u % QST]);
             }
             ++u;
             t = tn;
