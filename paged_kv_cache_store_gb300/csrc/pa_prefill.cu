@@ -26,8 +26,7 @@
 //    scores of a tile, so row statistics need no exchange.  Online softmax
 //    in base 2; P goes back to TMEM as bf16 pairs.  O is rescaled only when a
 //    row's max grows by more than 2^8 (P then stays <= 256, exact enough in
-//    bf16 and fp32); the wait for the previous P.V, which a rescale needs,
-//    is otherwise taken after P is published, off the critical path.  The
+//    bf16 and fp32); only a rescale waits for the previous P.V.  The
 //    same warps finish the unit: O / l -> bf16 into the unit's Q buffer (no
 //    longer read once its last S is in), then one TMA store for a full tile,
 //    or coalesced 256-byte row stores for the last, partial tile of a
@@ -68,7 +67,7 @@ constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
 enum {
     B_QFULL = 0, B_QEMPTY = B_QFULL + QST, B_KFULL = B_QEMPTY + QST, B_KEMPTY = B_KFULL + KST,
     B_VFULL = B_KEMPTY + KST, B_VEMPTY = B_VFULL + VST, B_SFULL = B_VEMPTY + VST, B_PFULL = B_SFULL + NSB,
-    B_PDONE = B_PFULL + NSB, B_OREADY = B_PDONE + NSB, B_OEMPTY, B_DRAIN, B_DRAIN2, NBAR
+    B_PDONE = B_PFULL + NSB, B_OREADY = B_PDONE + NSB, B_OEMPTY = B_OREADY + 2, B_DRAIN, B_DRAIN2, NBAR
 };
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int OFF_FLAGS = OFF_TMEM + 8;
@@ -363,7 +362,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int k = 0; k < kpad / 16; ++k)  // 16 keys per step = 8 TMEM columns of P
                 mma_bf16_ts(tmem + COL_O, tmem + COL_S + sb * BN + k * 8, vdesc + (uint64_t)((k * 16 * 128) >> 4),
                             IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
-            mma_commit(&bar[B_OREADY]);
+            mma_commit(&bar[B_OREADY + (gv & 1)]);
             mma_commit(&bar[B_VEMPTY + vs]);
             mma_commit(&bar[B_PDONE + sb]);
             issued = true;
@@ -401,17 +400,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int tid = threadIdx.x - W_SOFT * 32;  // 0..127
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         const float sl = a.scale_log2;
-        uint32_t gs = 0, u = 0, po = 0;  // S tiles consumed, units finished, P.V results waited for
+        uint32_t gs = 0, u = 0;  // S tiles consumed, units finished
         bool ok = true;
         // Waits in this role are warp-uniform: tcgen05.ld/st are warp-collective.
         auto wwait = [&](uint64_t *b, uint32_t parity, int where) -> bool {
             return __all_sync(FULL, wait_or_abort(b, parity, flags, a.err, where));
         };
-        auto wait_o = [&]() -> bool {
-            const bool r = wwait(&bar[B_OREADY], po & 1u, 421);
-            ++po;
-            return r;
-        };
+        // P.V number x (global tile count) has completed.  OREADY alternates by
+        // tile parity; the waits skip phases, which is safe because P.V x+2
+        // cannot complete before this warpgroup publishes its P, so the barrier
+        // is never two phases past the one awaited.
+        auto wait_o = [&](uint32_t x) -> bool { return wwait(&bar[B_OREADY + (x & 1)], (x >> 1) & 1u, 421); };
         // The next unit with work, from t on (next_valid_unit is warp-collective).
         auto next_unit = [&](int t) -> int {
             for (t = next_valid_unit(a, t, nunits, lane); t < nunits; t = next_valid_unit(a, t + gridDim.x, nunits, lane))
@@ -453,11 +452,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const bool grow = (mx - m_run) * sl > 8.f;
                 const float m_new = grow ? mx : m_run;
                 const float alpha = grow ? fast_exp2((m_run - m_new) * sl) : 1.f;
-                bool waited = j == 0;  // tile 0: no earlier P.V of this unit to wait for
                 if (j > 0 && __any_sync(FULL, grow)) {
                     // O must hold P.V up to tile j-1 before it is rescaled.
-                    if (!(ok = wait_o())) break;
-                    waited = true;
+                    if (!(ok = wait_o(gs - 1))) break;
                     tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
@@ -491,13 +488,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[B_PFULL + sb]);
-                // The previous tile's P.V, if not waited for above (keeps one wait per P.V, in order).
-                if (!waited && !(ok = wait_o())) break;
             }
             if (!ok) break;
             const int tn = next_unit(t + gridDim.x);
             // ---- epilogue: O / l -> bf16 tile in shared memory -> global memory
-            if (!(ok = wait_o())) break;
+            if (!(ok = wait_o(gs - 1))) break;
             tc_fence_after();
             uint32_t o[128];
             tmem_ld32(t_lane + COL_O, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
