@@ -20,8 +20,8 @@
 //    its S buffer) and V as an MN-major operand.  Scores run up to three
 //    tiles ahead of P.V; a Q.K waits until the P.V that read its buffer three
 //    tiles earlier has completed.
-//    tcgen05.commit arrives on mbarriers to free K/V stages and S buffers,
-//    publish S and report O.
+//    tcgen05.commit arrives on mbarriers to free K/V stages and S buffers
+//    (which also reports O) and to publish S.
 //  * warps 4..7: one thread per query row (its TMEM lane) holds all 128
 //    scores of a tile, so row statistics need no exchange.  Online softmax
 //    in base 2; P goes back to TMEM as bf16 pairs.  O is rescaled only when a
@@ -67,13 +67,15 @@ constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
 enum {
     B_QFULL = 0, B_QEMPTY = B_QFULL + QST, B_KFULL = B_QEMPTY + QST, B_KEMPTY = B_KFULL + KST,
     B_VFULL = B_KEMPTY + KST, B_VEMPTY = B_VFULL + VST, B_SFULL = B_VEMPTY + VST, B_PFULL = B_SFULL + NSB,
-    B_PDONE = B_PFULL + NSB, B_OREADY = B_PDONE + NSB, B_OEMPTY = B_OREADY + 2, B_DRAIN, B_DRAIN2, NBAR
+    B_PDONE = B_PFULL + NSB, B_OEMPTY = B_PDONE + NSB, B_DRAIN, B_DRAIN2,
+    B_NU /* [2] next-unit slots, Q.K thread -> softmax */, NBAR = B_NU + 2
 };
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int OFF_FLAGS = OFF_TMEM + 8;
 constexpr int OFF_BID = OFF_FLAGS + 16;  // block ids of the current unit, per producer warp
 constexpr int NBID = 32;
-constexpr int SMEM_USED = OFF_BID + 2 * NBID * 4;
+constexpr int OFF_NU = OFF_BID + 2 * NBID * 4;  // two Unit slots (the softmax's next unit)
+constexpr int SMEM_USED = OFF_NU + 2 * 48;
 // Slack for aligning the dynamic shared-memory base to the 1 KiB the swizzled
 // tiles need (the base is normally aligned already; the kernel checks).
 constexpr int SMEM_SLACK = 256;
@@ -158,6 +160,8 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
 struct Unit {
     int s, h, m0, q0, Lq, k0, Lk, n_kv, key_end, valid;
 };
+static_assert(sizeof(Unit) <= 48, "next-unit slot");
+static_assert(QST == 2, "the next-unit ring reuses a slot with the Q buffer of the same parity");
 
 __device__ __forceinline__ Unit unit_of(const PrefillArgs &a, int t) {
     Unit U;
@@ -238,6 +242,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Unit i goes to slot i & 1; a slot is rewritten only after the softmax read
+    // it (the Q.K thread cannot start unit i+2 before the softmax has released
+    // the Q buffer of unit i), so a reader is never two phases behind.
+    Unit *nu = reinterpret_cast<Unit *>(smem + OFF_NU);
 
     // Every role walks the same units t = blockIdx.x, +gridDim.x, ... and the
     // same global KV-tile counter g, so ring stages and barrier phases agree.
@@ -362,10 +370,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int k = 0; k < kpad / 16; ++k)  // 16 keys per step = 8 TMEM columns of P
                 mma_bf16_ts(tmem + COL_O, tmem + COL_S + sb * BN + k * 8, vdesc + (uint64_t)((k * 16 * 128) >> 4),
                             IDESC_PV, (jj > 0 || k > 0) ? 1u : 0u);
-            mma_commit(&bar[B_OREADY + (gv & 1)]);
             mma_commit(&bar[B_VEMPTY + vs]);
             mma_commit(&bar[B_PDONE + sb]);
             issued = true;
+            return true;
+        };
+        // Unit i goes to slot i & 1 of the softmax's next-unit ring once the Q
+        // buffer of unit i - 2 is released.  The softmax releases that buffer
+        // only after all its threads passed unit i - 2's epilogue barrier and
+        // after it published the first P of unit i - 1, so every thread has
+        // read slot i & 1 (unit i - 2) before it is rewritten, and a waiter is
+        // never two phases behind.
+        auto post_unit = [&](uint32_t i, const Unit &V) -> bool {
+            if (!wait_or_abort(&bar[B_QEMPTY + i % QST], ((i / QST) & 1u) ^ 1u, flags, a.err, 417)) return false;
+            nu[i & 1] = V;
+            mbar_arrive(&bar[B_NU + (i & 1)]);
             return true;
         };
         // All lanes walk the units (next_valid_unit is warp-collective); lane 0
@@ -376,7 +395,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!U.valid) continue;
             if (lane == 0) {
                 if (is_qk) {
-                    ok = wait_or_abort(&bar[B_QFULL + u % QST], (u / QST) & 1u, flags, a.err, 416);
+                    // The softmax warps learn their next unit here, off their critical path.
+                    ok = post_unit(u, U);
+                    ok = ok && wait_or_abort(&bar[B_QFULL + u % QST], (u / QST) & 1u, flags, a.err, 416);
                     qdesc = smem_desc_sw128(smem_addr(smem + OFF_Q + (u % QST) * TILE_BYTES), 16, SBO);
                     for (int j = 0; ok && j < U.n_kv; ++j) ok = qk(g + j);
                 } else {
@@ -386,6 +407,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             g += U.n_kv;
             ++u;
             ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+        }
+        if (lane == 0 && ok && is_qk) {  // the end of the CTA's units
+            Unit end = {};
+            end.valid = 0;
+            (void)post_unit(u, end);
         }
         if (lane == 0 && !ok && issued) {
             // Let the issued MMAs finish before TMEM is released.
@@ -406,20 +432,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         auto wwait = [&](uint64_t *b, uint32_t parity, int where) -> bool {
             return __all_sync(FULL, wait_or_abort(b, parity, flags, a.err, where));
         };
-        // P.V number x (global tile count) has completed.  OREADY alternates by
-        // tile parity; the waits skip phases, which is safe because P.V x+2
-        // cannot complete before this warpgroup publishes its P, so the barrier
-        // is never two phases past the one awaited.
-        auto wait_o = [&](uint32_t x) -> bool { return wwait(&bar[B_OREADY + (x & 1)], (x >> 1) & 1u, 421); };
-        // The next unit with work, from t on (next_valid_unit is warp-collective).
-        auto next_unit = [&](int t) -> int {
-            for (t = next_valid_unit(a, t, nunits, lane); t < nunits; t = next_valid_unit(a, t + gridDim.x, nunits, lane))
-                if (unit_of(a, t).valid) break;
-            return t;
+        // P.V number x (global tile count) and all before it have completed:
+        // wait for its commit on PDONE[x % NSB].  Called only after S(x) was
+        // waited for: the Q.K that wrote S(x) had waited for this barrier's
+        // previous phase (P.V x - NSB), so the phase awaited is the next to
+        // complete, never one further (a parity wait would pass at once); and
+        // P.V x + NSB needs a P this warpgroup has not published yet.
+        auto wait_o = [&](uint32_t x) -> bool { return wwait(&bar[B_PDONE + x % NSB], (x / NSB) & 1u, 421); };
+        auto take_unit = [&](uint32_t i, Unit &U) -> bool {
+            if (!wwait(&bar[B_NU + (i & 1)], (i >> 1) & 1u, 430)) return false;
+            U = nu[i & 1];
+            return U.valid != 0;
         };
-        int t = next_unit(blockIdx.x);
-        while (ok && t < nunits) {
-            const Unit U = unit_of(a, t);
+        Unit U;
+        bool have = take_unit(0, U);
+        int pend_q = -1;  // Q buffer whose output store still has to be read out (thread 0)
+        while (ok && have) {
             const int i = U.m0 + row;  // query index in the sequence (>= Lq: padding row)
             const int pos = (U.Lk - U.Lq) + i;
             const int key_last = (a.causal ? min(pos, U.Lk - 1) : U.Lk - 1);  // last key this row sees
@@ -488,9 +516,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[B_PFULL + sb]);
+                if (tid == 0 && pend_q >= 0) {
+                    // The previous unit's tile store has read its staging buffer by
+                    // now: release the buffer for a later Q.
+                    bulk_wait_read0();
+                    mbar_arrive(&bar[B_QEMPTY + pend_q]);
+                    pend_q = -1;
+                }
             }
             if (!ok) break;
-            const int tn = next_unit(t + gridDim.x);
             // ---- epilogue: O / l -> bf16 tile in shared memory -> global memory
             if (!(ok = wait_o(gs - 1))) break;
             tc_fence_after();
@@ -523,8 +557,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (tid == 0) {
                     tma_store_4d(&tmo, smem + OFF_Q + (u % QST) * TILE_BYTES, 0, U.q0 + U.m0, 0, U.h);
                     bulk_commit_group();
-                    bulk_wait_read0();  // the store has read the tile: the buffer may take a later Q
-                    mbar_arrive(&bar[B_QEMPTY + u % QST]);
+                    pend_q = u % QST;  // released after the next tile (or below, at the end)
                 }
             } else {
                 // The last tile of a sequence: rows past Lq belong to the next
@@ -538,11 +571,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         *reinterpret_cast<uint4 *>(a.out + ((int64_t)(U.q0 + U.m0 + rr) * a.Hq + U.h) * D + c * 8) = v;
                     }
                 }
-                named_bar_sync(SOFT_BAR, 128);  // the staging tile was read: it may take a later Q
-                if (tid == 0) mbar_arrive(&bar[B_QEMPTY + u % QST]);
+                named_bar_sync(SOFT_BAR, 128);  // the staging tile was read
+                if (tid == 0) pend_q = u % QST;   // released with the next unit's first P, like a tile store
             }
             ++u;
-            t = tn;
+            have = ok && take_unit(u, U);
+        }
+        if (tid == 0 && pend_q >= 0) {
+            bulk_wait_read0();
+            mbar_arrive(&bar[B_QEMPTY + pend_q]);
         }
         if (tid == 0) bulk_wait0();  // tile stores complete before the CTA exits
     }
