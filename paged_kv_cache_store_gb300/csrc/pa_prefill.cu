@@ -618,11 +618,10 @@ extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_s
         return fail(PA_ERR_INVALID_ARG, "out/q/k/v pointers must be 16-byte aligned");
     if (!(softmax_scale > 0.f) || !isfinite(softmax_scale))
         return fail(PA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
+    if (((int64_t)max_seqlen_q + BM - 1) / BM * num_seqs * num_q_heads > 0x7fffffffLL)
+        return fail(PA_ERR_UNSUPPORTED, "too many tiles");
     const bool paged = block_tables != nullptr;
     int R = BN;
-    CUtensorMap tq, tk, tv;
-    pa_status st = encode_halves_map(&tq, q, total_q, q_row_stride * 2, num_q_heads, BM, 2);
-    if (st != PA_OK) return st;
     if (paged) {
         if (block_size <= 0 || block_size % 16)
             return fail(PA_ERR_UNSUPPORTED, "block_size %d (must be a positive multiple of 16)", block_size);
@@ -640,6 +639,9 @@ extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_s
     // A box of BN rows holds a whole K/V tile in [half][row][64] order;
     // shorter boxes (small blocks) are fetched one 64-dim half at a time.
     const int halves = R == BN ? 2 : 1;
+    CUtensorMap tq, tk, tv;
+    pa_status st = encode_halves_map(&tq, q, total_q, q_row_stride * 2, num_q_heads, BM, 2);
+    if (st != PA_OK) return st;
     const int64_t kv_rows = paged ? (int64_t)num_blocks * block_size : (int64_t)total_k;
     const int64_t kv_stride = paged ? (int64_t)num_kv_heads * D * 2 : kv_row_stride * 2;
     st = encode_halves_map(&tk, k, kv_rows, kv_stride, num_kv_heads, R, halves);
@@ -670,7 +672,6 @@ extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_s
     A.err = device_error_ptr();
 
     const int64_t ntiles = (int64_t)A.mtiles * num_seqs * num_q_heads;
-    if (ntiles > 0x7fffffffLL) return fail(PA_ERR_UNSUPPORTED, "too many tiles");
     const int sms = sm_count();
     if (sms <= 0) return fail(PA_ERR_CUDA, "no CUDA device");
     const int64_t grid = std::min<int64_t>(ntiles, sms);  // persistent: one CTA per SM

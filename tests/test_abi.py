@@ -114,3 +114,30 @@ def test_slot_mapping_argument_checks(L):
     assert L.pa_slot_mapping_decode(p, p, 4, p, 3, 0, None) == pa.PA_ERR_INVALID_ARG
     assert L.pa_slot_mapping_prefill(p, p, 4, p, p, 2, 0, 256, None) == pa.PA_OK
     assert L.pa_slot_mapping_prefill(p, p, 4, p, p, -1, 3, 256, None) == pa.PA_ERR_INVALID_ARG
+
+
+def _prefill(L, **kw):
+    p = C.c_void_p(256)
+    a = dict(out=p, q=p, qs=32 * 128, tq=100, k=p, v=p, kvs=0, tk=0, bt=p, mb=8, cq=p, ck=p, ns=2, mq=64, mk=900,
+             hq=32, hkv=8, d=128, B=256, nb=64, scale=0.088, causal=1, stream=None)
+    a.update(kw)
+    return L.pa_prefill_varlen(a["out"], a["q"], a["qs"], a["tq"], a["k"], a["v"], a["kvs"], a["tk"], a["bt"],
+                               a["mb"], a["cq"], a["ck"], a["ns"], a["mq"], a["mk"], a["hq"], a["hkv"], a["d"],
+                               a["B"], a["nb"], a["scale"], a["causal"], a["stream"])
+
+
+def test_prefill_argument_checks(L):
+    assert _prefill(L, ns=0) == pa.PA_OK                      # nothing to do
+    assert _prefill(L, tq=0) == pa.PA_OK
+    assert _prefill(L, ns=-1) == pa.PA_ERR_INVALID_ARG
+    assert _prefill(L, q=None) == pa.PA_ERR_INVALID_ARG
+    assert _prefill(L, hq=12) == pa.PA_ERR_INVALID_ARG        # not a multiple of Hkv
+    assert _prefill(L, d=64) == pa.PA_ERR_UNSUPPORTED
+    assert _prefill(L, qs=32 * 128 - 8) == pa.PA_ERR_INVALID_ARG
+    assert _prefill(L, out=C.c_void_p(264)) == pa.PA_ERR_INVALID_ARG   # unaligned output
+    assert _prefill(L, scale=-1.0) == pa.PA_ERR_INVALID_ARG
+    assert _prefill(L, B=24) == pa.PA_ERR_UNSUPPORTED                # block size not a multiple of 16
+    assert _prefill(L, nb=0) == pa.PA_ERR_INVALID_ARG
+    assert _prefill(L, bt=None, tk=0) == pa.PA_ERR_INVALID_ARG        # contiguous k/v without total_k
+    assert _prefill(L, bt=None, tk=100, kvs=8 * 128 - 8) == pa.PA_ERR_INVALID_ARG
+    assert _prefill(L, ns=1 << 20, mq=1 << 20) == pa.PA_ERR_UNSUPPORTED  # tiles overflow int32
