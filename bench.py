@@ -255,6 +255,41 @@ def measure_prefill(args, dev, stream, flush, bf16_peak):
             "store_gbs": store_bytes / (store_ms / 1000.0) / 1e9}
 
 
+def measure_sampler(args, dev, stream, flush, hbm_peak):
+    """The Gumbel-max sampler after the decode step: 64 rows over the Qwen3
+    vocabulary (bf16 logits, fp32 Exp(1) draws).  HBM-bound: every logit and
+    draw is read once."""
+    import torch
+    import paged_kv_cache_store_gb300 as pa
+    from paged_kv_cache_store_gb300.workloads import sampler_config
+
+    sp = sampler_config(64)
+    lg = torch.from_numpy(np.ascontiguousarray(sp.logits).view(np.int16)).view(torch.bfloat16).to(dev)
+    temps = torch.from_numpy(sp.temperatures).to(dev)
+    noise = torch.from_numpy(sp.exp_noise).to(dev)
+    out = torch.empty(sp.batch, dtype=torch.int32, device=dev)
+    for _ in range(max(3, args.warmup)):
+        pa.sample_gumbel(lg, temps, noise, out=out)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        pa.sample_gumbel(lg, temps, noise, out=out)
+        b.record(stream)
+    torch.cuda.synchronize()
+    code, where = pa.get_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} at {where}")
+    ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    alg = sp.batch * sp.vocab * (2 + 4) + sp.batch * (4 + 4)
+    gbs = alg / (ms / 1000.0) / 1e9
+    return {"workload": sp.name + ", fp32 Exp(1) draws", "ms": ms, "algorithmic_bytes": alg,
+            "roofline": {"bound": "hbm", "kernel": "sample_gumbel_kernel", "achieved": gbs, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": gbs / hbm_peak, "traffic": None},
+            "l2": "flushed (256 MiB write) before every timed call; inputs 58 MB"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -373,6 +408,7 @@ def run_ours(args):
         del kc, vc
         torch.cuda.empty_cache()
         prefill = measure_prefill(args, dev, stream, flush, peaks()[1])
+    sampler = measure_sampler(args, dev, stream, flush, peaks()[0])
 
     if rank == 0:
         hbm, _, peak_kind = peaks()
@@ -398,6 +434,7 @@ def run_ours(args):
             "gpu_launches": 3 * args.steps,
             "clocks": clk.summary(),
             "prefill": prefill,
+            "sampler": sampler,
         }
         if not args.no_cpu_baseline:
             import oracle as O

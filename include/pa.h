@@ -85,8 +85,9 @@ enum {
                                   where = sequence*max_blocks_per_seq + logical block */
     PA_DEV_BAD_SEQLENS = 5,    /* prefill: cu_seqlens not monotone or Lq > Lk;
                                   where = sequence index */
-    PA_DEV_SMEM_ALIGN = 6      /* a kernel could not align its shared-memory tiles
+    PA_DEV_SMEM_ALIGN = 6,     /* a kernel could not align its shared-memory tiles
                                   (no work done); where = bytes of padding needed */
+    PA_DEV_BAD_TEMPERATURE = 7 /* sampler: temperature not > 1e-10; where = row */
 };
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -254,6 +255,31 @@ PA_API pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_strid
                                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                    int32_t block_size, int32_t num_blocks, float softmax_scale,
                                    int32_t causal, pa_stream_t stream);
+
+/*
+ * pa_sample_gumbel -- sample one token per row by the Gumbel-max trick.
+ * [NV12 §12.2 "采样器": Sampler.forward and the Gumbel-max derivation]
+ *
+ *   token[b] = argmax_i softmax(float(logits[b]) / T_b)_i / max(E[b,i], 1e-10)
+ *
+ * computed in fp32; the lowest index wins among equal maxima.  E ~ Exp(1),
+ * one independent draw per (row, vocabulary entry), is drawn by the caller
+ * (e.g. torch.empty(...).exponential_(1)), which owns the random state.
+ *   out_tokens        int32 [batch].
+ *   logits            [batch, vocab] bf16 (logits_is_fp32 = 0) or fp32 (1);
+ *                     row b at logits + b*logits_row_stride elements; the
+ *                     stride is a multiple of 8 (bf16) or 4 (fp32) elements.
+ *   temperatures      fp32 [batch], each > 1e-10; a row whose temperature is
+ *                     not gets token -1 and PA_DEV_BAD_TEMPERATURE.
+ *   exp_noise         fp32 [batch, vocab], row stride noise_row_stride (a
+ *                     multiple of 4 elements).
+ *   batch <= 65535.  A row with no finite candidate (all logits -inf or NaN)
+ *   gets token 0.  Base pointers 16-byte aligned.  One kernel, a programmatic
+ *   dependent launch; each row is read once (HBM-bound).
+ */
+PA_API pa_status pa_sample_gumbel(int32_t *out_tokens, const void *logits, int64_t logits_row_stride,
+                                  int32_t logits_is_fp32, const float *temperatures, const float *exp_noise,
+                                  int64_t noise_row_stride, int32_t batch, int32_t vocab, pa_stream_t stream);
 
 /*
  * pa_set_checked -- enable (1) or disable (0) extra device checks for calls

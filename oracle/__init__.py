@@ -2,8 +2,10 @@
 
 Only the tests, the smoke check and the benchmark's CPU-baseline leg may
 import this package.  The product library never loads it, and the two share
-no code.  The arithmetic lives in ``pa_oracle.c`` (plain C, double
-precision); this module compiles it with gcc and marshals numpy arrays.
+no code.  The attention and store arithmetic lives in ``pa_oracle.c``
+(plain C, double precision); this module compiles it with gcc and marshals
+numpy arrays.  The sampler, whose page fixes fp32, is ``sampler.py`` (numpy
+float32).
 """
 from __future__ import annotations
 

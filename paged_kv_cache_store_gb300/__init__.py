@@ -10,7 +10,7 @@ libpa.so has not been built (see build.py).
 Entry points (same names as the C ABI without the ``pa_`` prefix):
   store_kvcache, slot_mapping_decode, slot_mapping_prefill,
   decode_workspace_size, decode, decode_static, prefill_varlen,
-  set_checked, get_device_error.
+  sample_gumbel, set_checked, get_device_error.
 """
 from __future__ import annotations
 
@@ -24,7 +24,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpa.so")
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_DEVICE_CHECK = range(6)
-PA_DEV_TIMEOUT, PA_DEV_BAD_SLOT, PA_DEV_BAD_CONTEXT, PA_DEV_BAD_BLOCK, PA_DEV_BAD_SEQLENS, PA_DEV_SMEM_ALIGN = range(1, 7)
+(PA_DEV_TIMEOUT, PA_DEV_BAD_SLOT, PA_DEV_BAD_CONTEXT, PA_DEV_BAD_BLOCK, PA_DEV_BAD_SEQLENS, PA_DEV_SMEM_ALIGN,
+ PA_DEV_BAD_TEMPERATURE) = range(1, 8)
 
 # Every symbol include/pa.h declares, with its ctypes signature.
 _i32, _i64, _sz, _f32, _vp = C.c_int32, C.c_int64, C.c_size_t, C.c_float, C.c_void_p
@@ -42,6 +43,7 @@ SIGNATURES = {
                                    _i32, _f32, _vp]),
     "pa_prefill_varlen": (C.c_int, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _i32, _vp, _i32, _vp, _vp, _i32,
                                     _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp]),
+    "pa_sample_gumbel": (C.c_int, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _i32, _i32, _vp]),
     "pa_set_checked": (C.c_int, [_i32]),
     "pa_get_device_error": (C.c_int, [_vp, C.POINTER(_i32), C.POINTER(_i64)]),
 }
@@ -246,6 +248,29 @@ def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen
                                    cu_seqlens_q.numel() - 1, int(max_seqlen_q), int(max_seqlen_k), hq, hkv,
                                    d, B, nb, float(softmax_scale), 1 if causal else 0, _stream(stream)),
            "pa_prefill_varlen")
+    return out
+
+
+def sample_gumbel(logits, temperatures, exp_noise, out=None, stream=None):
+    """One token per row: argmax softmax(logits / T) / max(E, 1e-10) (Gumbel-max).
+    logits [batch, vocab] bf16 or fp32 (rows may be strided); temperatures
+    fp32 [batch]; exp_noise fp32 [batch, vocab] of Exp(1) draws (the caller's
+    random state).  Returns int32 [batch]."""
+    if logits.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("logits must be bfloat16 or float32")
+    _need(temperatures, torch.float32, "temperatures")
+    _need(exp_noise, torch.float32, "exp_noise")
+    batch, vocab = logits.shape
+    if tuple(exp_noise.shape) != (batch, vocab) or tuple(temperatures.shape) != (batch,):
+        raise ValueError("exp_noise must be [batch, vocab] and temperatures [batch]")
+    if logits.stride(1) != 1 or exp_noise.stride(1) != 1 or not temperatures.is_contiguous():
+        raise ValueError("rows must be contiguous")
+    if out is None:
+        out = torch.empty(batch, dtype=torch.int32, device=logits.device)
+    _check(lib().pa_sample_gumbel(_ptr(out), _ptr(logits), logits.stride(0), 1 if logits.dtype == torch.float32 else 0,
+                                  _ptr(temperatures), _ptr(exp_noise), exp_noise.stride(0), batch, vocab,
+                                  _stream(stream)),
+           "pa_sample_gumbel")
     return out
 
 

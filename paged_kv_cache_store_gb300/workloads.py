@@ -272,3 +272,57 @@ def prefill_config(idx: int = 5) -> PrefillInputs:
     k = np.minimum(k, (lk + BLOCK_SIZE - 1) // BLOCK_SIZE - 1)
     return make_prefill("varlen prefill 16 seqs h32/8 Lk~U[128,2048] 0..3 cached blocks",
                         5, lk, k, 32, 8)
+
+
+# ----------------------------------------------------------------------------
+# Sampler inputs: logits of one decode step and the Exp(1) draws of the
+# Gumbel-max sampler.  Vocabulary 151936 (the Qwen3 vocabulary), logits
+# N(0, 2^2) rounded to bf16, temperatures ~ U[0.5, 1.2], one Exp(1) draw per
+# (row, token) in fp32 (the caller's random state in the sampler's contract).
+
+QWEN3_VOCAB = 151936
+
+
+def exponential_f32(seed: int, tag: int, shape) -> np.ndarray:
+    """Exp(1) samples in float32, drawn in fixed chunks from PCG64 streams
+    keyed by (seed, tag, chunk) like normal_bf16."""
+    n = int(np.prod(shape)) if len(shape) else 1
+    out = np.empty(n, dtype=np.float32)
+
+    def fill(j):
+        s, e = j * _CHUNK, min(n, (j + 1) * _CHUNK)
+        ss = np.random.SeedSequence(entropy=seed, spawn_key=(tag, j))
+        g = np.random.Generator(np.random.PCG64(ss))
+        out[s:e] = g.standard_exponential(e - s, dtype=np.float32)
+
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+    if nchunks <= 1:
+        for j in range(nchunks):
+            fill(j)
+    else:
+        list(_pool().map(fill, range(nchunks)))
+    return out.reshape(shape)
+
+
+@dataclass
+class SamplerInputs:
+    name: str
+    batch: int
+    vocab: int
+    logits: np.ndarray        # uint16 bf16 bits [batch, vocab]
+    temperatures: np.ndarray  # float32 [batch]
+    exp_noise: np.ndarray     # float32 [batch, vocab], Exp(1)
+
+
+def make_sampler(name: str, seed: int, batch: int, vocab: int, logit_std: float = 2.0) -> SamplerInputs:
+    z = normal_bf16(seed, 20, (batch, vocab))
+    logits = f32_to_bf16_bits(bf16_bits_to_f32(z) * np.float32(logit_std))
+    rng = np.random.default_rng(seed + 1000)
+    temps = rng.uniform(0.5, 1.2, size=batch).astype(np.float32)
+    return SamplerInputs(name, batch, vocab, logits, temps, exponential_f32(seed, 21, (batch, vocab)))
+
+
+def sampler_config(batch: int = 64) -> SamplerInputs:
+    """Sampling after a decode step: `batch` rows over the Qwen3 vocabulary."""
+    return make_sampler(f"gumbel-max sampler, batch {batch}, vocab {QWEN3_VOCAB}, bf16 logits", 6 + batch,
+                        batch, QWEN3_VOCAB)

@@ -141,3 +141,24 @@ def test_prefill_argument_checks(L):
     assert _prefill(L, bt=None, tk=0) == pa.PA_ERR_INVALID_ARG        # contiguous k/v without total_k
     assert _prefill(L, bt=None, tk=100, kvs=8 * 128 - 8) == pa.PA_ERR_INVALID_ARG
     assert _prefill(L, ns=1 << 20, mq=1 << 20) == pa.PA_ERR_UNSUPPORTED  # tiles overflow int32
+
+
+def _sample(L, **kw):
+    p = C.c_void_p(256)
+    a = dict(out=p, lg=p, ls=1024, fp32=0, t=p, e=p, es=1024, b=4, v=1000, stream=None)
+    a.update(kw)
+    return L.pa_sample_gumbel(a["out"], a["lg"], a["ls"], a["fp32"], a["t"], a["e"], a["es"], a["b"], a["v"],
+                              a["stream"])
+
+
+def test_sample_argument_checks(L):
+    assert _sample(L, b=0) == pa.PA_OK
+    assert _sample(L, b=-1) == pa.PA_ERR_INVALID_ARG
+    assert _sample(L, v=0) == pa.PA_ERR_INVALID_ARG
+    assert _sample(L, out=None) == pa.PA_ERR_INVALID_ARG
+    assert _sample(L, fp32=2) == pa.PA_ERR_INVALID_ARG
+    assert _sample(L, ls=999) == pa.PA_ERR_INVALID_ARG       # stride below vocab
+    assert _sample(L, ls=1004) == pa.PA_ERR_INVALID_ARG      # bf16 rows must stay 16-byte aligned
+    assert _sample(L, es=1002) == pa.PA_ERR_INVALID_ARG
+    assert _sample(L, lg=C.c_void_p(258)) == pa.PA_ERR_INVALID_ARG
+    assert _sample(L, b=70000) == pa.PA_ERR_UNSUPPORTED
