@@ -6,16 +6,18 @@
 // with E[b, i] ~ Exp(1) drawn independently per entry by the caller, in fp32;
 // among equal maxima the lowest index wins (first maximum).
 //
-// How (GB300 design): the softmax normaliser is one positive number per row,
-// so it never changes the argmax and is not computed.  Each thread keeps, for
-// the elements it reads, a running max m of x = logit * log2(e) / T and the
-// best candidate as a fraction n / d with n = 2^(x - m) and d = max(E, 1e-10)
-// (two candidates compare by cross-multiplication, so no division per
-// element); when m grows, n is rescaled.  Partial results combine by the same
-// rule across a warp (shuffles), a CTA (shared memory) and the CTAs of a
-// thread-block cluster that splits the row (distributed shared memory, into
-// the cluster's first CTA).  One pass over HBM: every logit (2 or 4 bytes)
-// and every noise value (4 bytes) is read once with 16-byte loads.
+// How (GB300 design): the page's own derivation turns the division by E into
+// a subtraction of log E under the argmax; with the softmax normaliser (one
+// positive number per row) dropped as well, the token is the argmax of
+//     key_i = logit_i * log2(e) / T - log2(max(E_i, 1e-10)),
+// which orders the entries exactly as p_i / E_i does (log2 is increasing).
+// So each thread keeps only its best (key, index): one lg2 and one fma per
+// element, no running max and no rescaling.  Partial results combine by max
+// key (lower index on equal keys) across a warp (shuffles), a CTA (shared
+// memory) and the CTAs of a thread-block cluster that splits the row
+// (distributed shared memory, into the cluster's first CTA).  One pass over
+// HBM: every logit (2 or 4 bytes) and every draw (4 bytes) is read once with
+// 16-byte loads.
 #include <math.h>
 
 #include "pa_internal.cuh"
@@ -26,40 +28,42 @@ namespace {
 constexpr int SAMPLE_THREADS = 256;
 constexpr unsigned FULLM = 0xffffffffu;
 constexpr float E_MIN = 1e-10f;  // the page's clamp of the exponential draws
+#ifndef SAMPLE_MAX_CLUSTER
+#define SAMPLE_MAX_CLUSTER 8
+#endif
+constexpr int MAX_CLUSTER = SAMPLE_MAX_CLUSTER;  // CTAs per row (a cluster)
 
-// Partial argmax of a row: max m (log2 units), best value n / d, its index.
-struct __align__(16) Best {  // 16 bytes: one vector store into the cluster's first CTA
-    float m, n, d;
+// Partial argmax of a row: best key and its index (-inf and INT_MAX when
+// nothing finite was seen; NaN keys never win).
+struct __align__(8) Best {  // 8 bytes: one vector store into the cluster's first CTA
+    float key;
     int idx;
 };
 
-// Combines two partial results (the larger n/d after bringing both to the
-// larger m; equal values go to the lower index).
-__device__ __forceinline__ Best combine(Best a, Best b) {
-    const float m = fmaxf(a.m, b.m);
-    const float na = (a.m == m) ? a.n : a.n * exp2f(a.m - m);
-    const float nb = (b.m == m) ? b.n : b.n * exp2f(b.m - m);
-    const float lhs = na * b.d, rhs = nb * a.d;
-    const bool take_b = (rhs > lhs) || (rhs == lhs && b.idx < a.idx);
-    Best r;
-    r.m = m;
-    r.n = take_b ? nb : na;
-    r.d = take_b ? b.d : a.d;
-    r.idx = take_b ? b.idx : a.idx;
-    return r;
+__device__ __forceinline__ bool better(float ka, int ia, float kb, int ib) {
+    return ka > kb || (ka == kb && ia < ib);
 }
 
-__device__ __forceinline__ void consider(Best &s, float x, float e, int i) {
-    if (x > s.m) {  // new running max: rescale the best fraction
-        s.n = (s.m == -INFINITY) ? s.n : s.n * exp2f(s.m - x);
-        s.m = x;
-    }
-    const float n = exp2f(x - s.m), d = fmaxf(e, E_MIN);
-    if (n * s.d > s.n * d) {  // strictly better; later elements have higher indices
-        s.n = n;
-        s.d = d;
-        s.idx = i;
-    }
+__device__ __forceinline__ Best combine(Best a, Best b) { return better(b.key, b.idx, a.key, a.idx) ? b : a; }
+
+__device__ __forceinline__ float key_of(float logit, float k, float e) {
+    return fmaf(logit, k, -__log2f(fmaxf(e, E_MIN)));
+}
+
+// Read-once streaming loads (no L1 allocation).
+__device__ __forceinline__ float4 ldg_stream(const float4 *p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint4 ldg_stream_u4(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -72,7 +76,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_gumbel_kernel(
     DevError *err) {
     pdl_wait_then_release();
     __shared__ Best part[SAMPLE_THREADS / 32];
-    __shared__ Best cl[8];  // used in the cluster's first CTA
+    __shared__ Best cl[MAX_CLUSTER];  // used in the cluster's first CTA
     const int b = blockIdx.y;
     const uint32_t S = gridDim.x, rank = blockIdx.x;  // cluster = the S CTAs of a row
     const float T = __ldg(temperatures + b);
@@ -81,30 +85,62 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_gumbel_kernel(
     // This CTA's chunk of the row, a multiple of 8 elements except at the end.
     const int chunk = ((vocab + (int)S - 1) / (int)S + 7) & ~7;
     const int lo = min(vocab, (int)rank * chunk), hi = min(vocab, lo + chunk);
-    Best s = {-INFINITY, -1.f, 1.f, 0x7fffffff};
+    Best s = {-INFINITY, 0x7fffffff};
     if (!bad_t) {
         const float *er = noise + (int64_t)b * noise_stride;
         const int nvec = (hi - lo) / 8;
-        for (int v = threadIdx.x; v < nvec; v += SAMPLE_THREADS) {
-            const int i = lo + v * 8;
-            const float4 e0 = __ldg(reinterpret_cast<const float4 *>(er + i));
-            const float4 e1 = __ldg(reinterpret_cast<const float4 *>(er + i + 4));
-            float x[8];
-            if (FP32) {
-                const float *lr = static_cast<const float *>(logits) + (int64_t)b * logits_stride;
-                const float4 a0 = __ldg(reinterpret_cast<const float4 *>(lr + i));
-                const float4 a1 = __ldg(reinterpret_cast<const float4 *>(lr + i + 4));
-                x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w;
-                x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
-            } else {
-                const uint16_t *lr = static_cast<const uint16_t *>(logits) + (int64_t)b * logits_stride;
-                const uint4 w = __ldg(reinterpret_cast<const uint4 *>(lr + i));
-                x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-                x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
-            }
-            const float e[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+        // Two 8-element groups per step, all loads issued first (48 bytes
+        // each in flight per thread).
+        for (int v0 = threadIdx.x; v0 < nvec; v0 += 2 * SAMPLE_THREADS) {
+            float x[2][8], e[2][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) consider(s, x[j] * k, e[j], i + j);
+            for (int h = 0; h < 2; ++h) {
+                const int v = v0 + h * SAMPLE_THREADS;
+                const int i = lo + min(v, nvec - 1) * 8;  // a duplicate group past the end is ignored below
+                const float4 e0 = ldg_stream(reinterpret_cast<const float4 *>(er + i));
+                const float4 e1 = ldg_stream(reinterpret_cast<const float4 *>(er + i + 4));
+                e[h][0] = e0.x; e[h][1] = e0.y; e[h][2] = e0.z; e[h][3] = e0.w;
+                e[h][4] = e1.x; e[h][5] = e1.y; e[h][6] = e1.z; e[h][7] = e1.w;
+                if (FP32) {
+                    const float *lr = static_cast<const float *>(logits) + (int64_t)b * logits_stride;
+                    const float4 a0 = ldg_stream(reinterpret_cast<const float4 *>(lr + i));
+                    const float4 a1 = ldg_stream(reinterpret_cast<const float4 *>(lr + i + 4));
+                    x[h][0] = a0.x; x[h][1] = a0.y; x[h][2] = a0.z; x[h][3] = a0.w;
+                    x[h][4] = a1.x; x[h][5] = a1.y; x[h][6] = a1.z; x[h][7] = a1.w;
+                } else {
+                    const uint16_t *lr = static_cast<const uint16_t *>(logits) + (int64_t)b * logits_stride;
+                    const uint4 w = ldg_stream_u4(reinterpret_cast<const uint4 *>(lr + i));
+                    x[h][0] = bf16_lo(w.x); x[h][1] = bf16_hi(w.x); x[h][2] = bf16_lo(w.y); x[h][3] = bf16_hi(w.y);
+                    x[h][4] = bf16_lo(w.z); x[h][5] = bf16_hi(w.z); x[h][6] = bf16_lo(w.w); x[h][7] = bf16_hi(w.w);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int v = v0 + h * SAMPLE_THREADS;
+                if (v >= nvec) break;
+                const int i = lo + v * 8;
+                // The 8 keys are independent; a tree picks the best (lowest
+                // index among equals), then it is merged into the running best.
+                float kk[8];
+                int ii[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    kk[j] = key_of(x[h][j], k, e[h][j]);
+                    ii[j] = i + j;
+                }
+#pragma unroll
+                for (int w = 1; w < 8; w <<= 1)
+#pragma unroll
+                    for (int j = 0; j < 8; j += 2 * w)
+                        if (better(kk[j + w], ii[j + w], kk[j], ii[j])) {
+                            kk[j] = kk[j + w];
+                            ii[j] = ii[j + w];
+                        }
+                if (better(kk[0], ii[0], s.key, s.idx)) {
+                    s.key = kk[0];
+                    s.idx = ii[0];
+                }
+            }
         }
         for (int i = lo + nvec * 8 + threadIdx.x; i < hi; i += SAMPLE_THREADS) {  // ragged end of the row
             float x;
@@ -114,16 +150,18 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_gumbel_kernel(
                 const uint16_t h = static_cast<const uint16_t *>(logits)[(int64_t)b * logits_stride + i];
                 x = __uint_as_float((uint32_t)h << 16);
             }
-            consider(s, x * k, er[i], i);
+            const float kx = key_of(x, k, er[i]);
+            if (better(kx, i, s.key, s.idx)) {
+                s.key = kx;
+                s.idx = i;
+            }
         }
     }
     // Warp, then CTA.
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         Best t;
-        t.m = __shfl_xor_sync(FULLM, s.m, o);
-        t.n = __shfl_xor_sync(FULLM, s.n, o);
-        t.d = __shfl_xor_sync(FULLM, s.d, o);
+        t.key = __shfl_xor_sync(FULLM, s.key, o);
         t.idx = __shfl_xor_sync(FULLM, s.idx, o);
         s = combine(s, t);
     }
@@ -135,8 +173,8 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_gumbel_kernel(
         // Into slot `rank` of the cluster's first CTA.
         uint32_t dst;
         asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(smem_addr(&cl[rank])), "r"(0u));
-        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(__float_as_uint(s.m)),
-                     "r"(__float_as_uint(s.n)), "r"(__float_as_uint(s.d)), "r"((uint32_t)s.idx)
+        asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(dst), "r"(__float_as_uint(s.key)),
+                     "r"((uint32_t)s.idx)
                      : "memory");
     }
     // Every thread of every CTA of the cluster arrives; the first CTA then
@@ -159,7 +197,7 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_gumbel_kernel(
 // batch, at most 8 (a portable cluster) and at least 2048 elements per CTA.
 int ctas_per_row(int batch, int vocab, int sms) {
     int S = 1;
-    while (S < 8 && (int64_t)batch * S < 4LL * sms && vocab / (2 * S) >= 2048) S *= 2;
+    while (S < MAX_CLUSTER && (int64_t)batch * S < 4LL * sms && vocab / (2 * S) >= 2048) S *= 2;
     return S;
 }
 
@@ -168,6 +206,13 @@ pa_status launch_sample(int32_t *out, const void *logits, int64_t logits_stride,
                         const float *noise, int64_t noise_stride, int32_t batch, int32_t vocab,
                         cudaStream_t stream) {
     const int S = ctas_per_row(batch, vocab, sm_count());
+    if (MAX_CLUSTER > 8) {
+        static bool done = false;
+        if (!done) {
+            cudaFuncSetAttribute(sample_gumbel_kernel<FP32>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            done = true;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)S, (unsigned)batch);
     cfg.blockDim = dim3(SAMPLE_THREADS);

@@ -1,7 +1,8 @@
 """GPU parity: pa_sample_gumbel against the fp32 sampler oracle, through the
 C ABI.  The decision is an argmax taken in fp32 on both sides, by formulas
-that round differently (the kernel never normalises the softmax and compares
-fractions by cross-multiplication), so: every row's token must equal the
+that round differently (the kernel compares log2-space keys and never
+normalises the softmax; the oracle divides probabilities), so: every row's
+token must equal the
 oracle's, except where the oracle's best and the kernel's pick are within a
 float32 rounding of each other (checked in float64), which is then counted
 and must stay rare.  Cases: the Qwen3 vocabulary at decode batch sizes,
