@@ -281,6 +281,72 @@ PA_API pa_status pa_sample_gumbel(int32_t *out_tokens, const void *logits, int64
                                   int32_t logits_is_fp32, const float *temperatures, const float *exp_noise,
                                   int64_t noise_row_stride, int32_t batch, int32_t vocab, pa_stream_t stream);
 
+/* --------------------------------------------------------------------------
+ * Host block manager: the pool's allocator and prefix cache, whose block
+ * tables the kernels above consume.  Host code only (no GPU, no CUDA calls).
+ * [NV12 §12.8 "BlockManager: 分页 KV Cache + Prefix Caching";
+ *  VS §1.1 (the four fields), §1.2.4 (a traced allocation), §1.2.5 (prefix hits)]
+ *
+ * State: num_blocks blocks of block_size tokens, each with a reference count,
+ * the chained hash of its prefix (or none) and its token ids; a FIFO queue of
+ * free block ids (taken from the front, returned to the back); the set of
+ * used ids; a map from prefix hash to block id.  The chained hash of block i
+ * of a sequence is XXH64 (seed 0) of [hash of block i-1 as 8 little-endian
+ * bytes, omitted for i = 0] followed by the block's token ids as 64-bit
+ * little-endian integers (pa_bm_block_hash).  Sequences are kept in the
+ * manager and named by the id pa_bm_seq_add returns.
+ *
+ * pa_bm_can_allocate  number of leading full blocks (never the last block)
+ *                     found in the prefix cache with identical tokens, or -1
+ *                     if the free queue is shorter than the blocks still
+ *                     needed (cached blocks in use need none); -2: bad args.
+ * pa_bm_allocate      give the sequence its blocks: the first
+ *                     num_cached_blocks from the cache (one more reference,
+ *                     or taken back from the free queue), then fresh ones
+ *                     from the front of the queue (a fresh block loses its
+ *                     old map entry); num_cached_tokens = cached * block_size.
+ * pa_bm_deallocate    drop one reference per block, last block first; blocks
+ *                     at zero go to the back of the free queue keeping their
+ *                     hash (so a later prefix hit can take them back).
+ * pa_bm_can_append    1 if a decode step of the sequence can get the block it
+ *                     needs (one exactly when len % block_size == 1), else 0.
+ * pa_bm_may_append    take that block if needed.
+ * pa_bm_hash_blocks   register the blocks filled by a step of
+ *                     num_scheduled_tokens tokens after num_cached_tokens:
+ *                     blocks [cached / B, (cached + scheduled) / B).  The
+ *                     caller then advances num_cached_tokens
+ *                     (pa_bm_seq_set_num_cached_tokens) and appends generated
+ *                     tokens (pa_bm_seq_append_token).
+ * pa_bm_block_tables  int32 [num_seqs, max_blocks_per_seq] block tables, -1
+ *                     past each sequence's blocks (the kernels' format).
+ * Queries return counts (or -2 for bad arguments); errors set
+ * pa_last_error_message.  A manager is not thread-safe.
+ */
+typedef struct pa_block_manager pa_block_manager;
+PA_API pa_status pa_bm_create(int32_t num_blocks, int32_t block_size, pa_block_manager **out);
+PA_API void pa_bm_destroy(pa_block_manager *bm);
+PA_API pa_status pa_bm_seq_add(pa_block_manager *bm, const int64_t *token_ids, int32_t num_tokens, int32_t *seq_id);
+PA_API pa_status pa_bm_seq_append_token(pa_block_manager *bm, int32_t seq, int64_t token_id);
+PA_API pa_status pa_bm_seq_set_num_cached_tokens(pa_block_manager *bm, int32_t seq, int32_t num_cached_tokens);
+PA_API pa_status pa_bm_seq_info(const pa_block_manager *bm, int32_t seq, int32_t *num_tokens,
+                                int32_t *num_cached_tokens, int32_t *num_table_blocks);
+PA_API int32_t pa_bm_can_allocate(const pa_block_manager *bm, int32_t seq);
+PA_API pa_status pa_bm_allocate(pa_block_manager *bm, int32_t seq, int32_t num_cached_blocks);
+PA_API pa_status pa_bm_deallocate(pa_block_manager *bm, int32_t seq);
+PA_API int32_t pa_bm_can_append(const pa_block_manager *bm, int32_t seq);
+PA_API pa_status pa_bm_may_append(pa_block_manager *bm, int32_t seq);
+PA_API pa_status pa_bm_hash_blocks(pa_block_manager *bm, int32_t seq, int32_t num_scheduled_tokens);
+PA_API int32_t pa_bm_seq_block_table(const pa_block_manager *bm, int32_t seq, int32_t *out, int32_t capacity);
+PA_API pa_status pa_bm_block_tables(const pa_block_manager *bm, const int32_t *seq_ids, int32_t num_seqs,
+                                    int32_t *out, int32_t max_blocks_per_seq);
+PA_API int32_t pa_bm_free_block_ids(const pa_block_manager *bm, int32_t *out, int32_t capacity);
+PA_API pa_status pa_bm_block_info(const pa_block_manager *bm, int32_t block_id, int32_t *ref_count,
+                                  int32_t *has_hash, uint64_t *hash, int32_t *num_token_ids);
+PA_API int32_t pa_bm_lookup_hash(const pa_block_manager *bm, uint64_t hash);
+PA_API int32_t pa_bm_num_hashes(const pa_block_manager *bm);
+PA_API uint64_t pa_bm_block_hash(const int64_t *token_ids, int32_t num_tokens, int32_t has_prefix, uint64_t prefix);
+PA_API uint64_t pa_bm_xxh64(const void *data, size_t len, uint64_t seed);
+
 /*
  * pa_set_checked -- enable (1) or disable (0) extra device checks for calls
  * made after it on any thread: block ids outside [0, num_blocks) are then

@@ -10,7 +10,8 @@ libpa.so has not been built (see build.py).
 Entry points (same names as the C ABI without the ``pa_`` prefix):
   store_kvcache, slot_mapping_decode, slot_mapping_prefill,
   decode_workspace_size, decode, decode_static, prefill_varlen,
-  sample_gumbel, set_checked, get_device_error.
+  sample_gumbel, set_checked, get_device_error;
+  block_manager.BlockManager wraps the host block manager (pa_bm_*).
 """
 from __future__ import annotations
 
@@ -45,6 +46,28 @@ SIGNATURES = {
                                     _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp]),
     "pa_sample_gumbel": (C.c_int, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _i32, _i32, _vp]),
     "pa_set_checked": (C.c_int, [_i32]),
+    # host block manager
+    "pa_bm_create": (C.c_int, [_i32, _i32, C.POINTER(_vp)]),
+    "pa_bm_destroy": (None, [_vp]),
+    "pa_bm_seq_add": (C.c_int, [_vp, _vp, _i32, C.POINTER(_i32)]),
+    "pa_bm_seq_append_token": (C.c_int, [_vp, _i32, _i64]),
+    "pa_bm_seq_set_num_cached_tokens": (C.c_int, [_vp, _i32, _i32]),
+    "pa_bm_seq_info": (C.c_int, [_vp, _i32, C.POINTER(_i32), C.POINTER(_i32), C.POINTER(_i32)]),
+    "pa_bm_can_allocate": (_i32, [_vp, _i32]),
+    "pa_bm_allocate": (C.c_int, [_vp, _i32, _i32]),
+    "pa_bm_deallocate": (C.c_int, [_vp, _i32]),
+    "pa_bm_can_append": (_i32, [_vp, _i32]),
+    "pa_bm_may_append": (C.c_int, [_vp, _i32]),
+    "pa_bm_hash_blocks": (C.c_int, [_vp, _i32, _i32]),
+    "pa_bm_seq_block_table": (_i32, [_vp, _i32, _vp, _i32]),
+    "pa_bm_block_tables": (C.c_int, [_vp, _vp, _i32, _vp, _i32]),
+    "pa_bm_free_block_ids": (_i32, [_vp, _vp, _i32]),
+    "pa_bm_block_info": (C.c_int, [_vp, _i32, C.POINTER(_i32), C.POINTER(_i32), C.POINTER(C.c_uint64),
+                                   C.POINTER(_i32)]),
+    "pa_bm_lookup_hash": (_i32, [_vp, C.c_uint64]),
+    "pa_bm_num_hashes": (_i32, [_vp]),
+    "pa_bm_block_hash": (C.c_uint64, [_vp, _i32, _i32, C.c_uint64]),
+    "pa_bm_xxh64": (C.c_uint64, [_vp, _sz, C.c_uint64]),
     "pa_get_device_error": (C.c_int, [_vp, C.POINTER(_i32), C.POINTER(_i64)]),
 }
 

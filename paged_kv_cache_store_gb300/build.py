@@ -1,6 +1,7 @@
 """Builds libpa.so (the CUDA library behind include/pa.h) in the package directory.
 
-nvcc compiles every csrc/*.cu for sm_103a (in parallel), then links one
+nvcc compiles every csrc/*.cu for sm_103a and every csrc/*.cpp (host code)
+with the host compiler (in parallel), then links one
 shared library with the CUDA runtime linked statically, so the only runtime
 dependency is the driver.  Only the extern "C" entry points are exported.
 """
@@ -39,9 +40,9 @@ def _stale(target: str, deps) -> bool:
 
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(ROOT, "include", "pa.h")]
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(BUILD, os.path.splitext(os.path.basename(s))[0] + ".o") for s in srcs]
     nv = nvcc()
 
     def compile_one(pair):
