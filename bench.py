@@ -41,7 +41,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attn tokens/s and HBM GB/s vs GB300 peak; prefill TFLOP/s"
 WORKLOAD = ("qwen3-0.6b decode step, 1 layer: batch 64, 16 q / 8 kv heads, head_dim 128, block_size 256, "
             "context_lens ~ U[1,4096], pool = 1.2x blocks needed, random block permutation, "
-            "slot mapping + store_kvcache + split-KV decode")
+            "store of the new token fused into the split-KV decode kernel (pa_decode_store)")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -320,20 +320,23 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     L2 = "flushed (256 MiB write) before every timed step; KV pool 621 MiB > L2"
 
-    def step():
+    def step():  # one kernel: the decode kernel stores the new K/V rows, then attends
+        pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out, new_k=nk, new_v=nv)
+
+    def step_unfused():  # the same work as three launches
         pa.slot_mapping_decode(bt, ctx, inp.block_size, out=slots)
         pa.store_kvcache(nk, nv, kc, vc, slots)
         pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out)
 
     for _ in range(max(3, args.warmup)):
         step()
+        step_unfused()
     torch.cuda.synchronize()
     code, where = pa.get_device_error()
     if code:
         raise RuntimeError(f"device error {code} at {where}")
 
-    # Headline: whole steps, back to back on the stream (the three kernels are
-    # programmatic dependent launches, so nothing may sit between them).
+    # Headline: whole steps, L2 flushed before each.
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if ws > 1:
         dist.barrier()
@@ -356,8 +359,19 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = ws * inp.batch * args.steps / (total_ms / 1000.0)
 
+    # The same step as three launches (slot mapping, store, decode: programmatic
+    # dependent launches back to back), for comparison.
+    uev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in uev:
+        flush.zero_()
+        a.record(stream)
+        step_unfused()
+        b.record(stream)
+    torch.cuda.synchronize()
+    unfused_ms = sum(a.elapsed_time(b) for a, b in uev) / args.steps
+
     # Per-kernel durations for the roofline: events around the store and the
-    # decode launch (same inputs, L2 flushed before each step).
+    # decode launch of the unfused step (same inputs, L2 flushed before each).
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     for i in range(args.steps):
         flush.zero_()
@@ -431,7 +445,9 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": alg_bytes, "decode_ms": dec_avg,
                          "store_ms": sum(store_ms) / len(store_ms)},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": args.steps,
+            "unfused_step": {"ms_per_step": unfused_ms, "kernels": "slot_mapping_decode + store_kvcache + decode",
+                             "tokens_per_s": ws * inp.batch / (unfused_ms / 1000.0)},
             "clocks": clk.summary(),
             "prefill": prefill,
             "sampler": sampler,

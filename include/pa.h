@@ -199,6 +199,30 @@ PA_API pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const
                     pa_stream_t stream);
 
 /*
+ * pa_decode_store -- pa_decode that first stores the step's new token.
+ * [NV12 §12.6: store_kvcache then attention, fused]
+ *
+ * For every sequence b with ctx = context_lens[b] > 0, the new token's K and
+ * V rows (new_k[b], new_v[b]: Hkv*D bf16 each, row stride in elements) are
+ * written to slot block_tables[b][(ctx-1)/B]*B + (ctx-1)%B of k_cache /
+ * v_cache -- the token at position ctx-1, which the query is -- and the
+ * attention then reads them like every other key.  The write is done inside
+ * the decode kernel by the warp that copies the sequence's last tile (one
+ * kv head's 256-byte row each), so the step needs neither a slot mapping
+ * nor a separate store launch.  Afterwards the caches hold exactly what
+ * pa_slot_mapping_decode + pa_store_kvcache would have written.  Other
+ * arguments, the workspace contract and the outputs are those of pa_decode;
+ * new_k / new_v 16-byte aligned.
+ */
+PA_API pa_status pa_decode_store(void *out, const void *q, int64_t q_row_stride, const void *new_k,
+                                 int64_t new_k_row_stride, const void *new_v, int64_t new_v_row_stride,
+                                 void *k_cache, void *v_cache, const int32_t *block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int32_t num_blocks, float softmax_scale, void *workspace,
+                                 size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_decode_static -- pa_decode for callers that cannot allocate device memory.
  * (An addition of this library: the source pages have no counterpart.)
  *

@@ -42,6 +42,8 @@ SIGNATURES = {
                             _i32, _f32, _vp, _sz, _vp]),
     "pa_decode_static": (C.c_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                    _i32, _f32, _vp]),
+    "pa_decode_store": (C.c_int, [_vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
+                                  _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]),
     "pa_prefill_varlen": (C.c_int, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _i32, _vp, _i32, _vp, _vp, _i32,
                                     _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp]),
     "pa_sample_gumbel": (C.c_int, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _i32, _i32, _vp]),
@@ -195,10 +197,12 @@ def decode_workspace(num_q_heads, num_kv_heads, head_dim, device="cuda"):
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, workspace=None, out=None,
-           stream=None):
+           stream=None, new_k=None, new_v=None):
     """Paged decode attention.  q [batch, Hq, D] bf16 (rows may be strided);
     caches [num_blocks, B, Hkv, D]; block_tables int32 [batch, max_blocks];
-    context_lens int32 [batch].  Returns out [batch, Hq, D] bf16."""
+    context_lens int32 [batch].  Returns out [batch, Hq, D] bf16.  With
+    new_k / new_v ([batch, Hkv, D] bf16, rows may be strided) the kernel first
+    stores them at position context_lens-1 (pa_decode_store)."""
     _need(q, torch.bfloat16, "q")
     _need(k_cache, torch.bfloat16, "k_cache")
     _need(v_cache, torch.bfloat16, "v_cache")
@@ -215,6 +219,15 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, 
         workspace = decode_workspace(hq, hkv, d, q.device)
     if out is None:
         out = torch.empty(batch, hq, d, dtype=torch.bfloat16, device=q.device)
+    if new_k is not None or new_v is not None:
+        _need(new_k, torch.bfloat16, "new_k")
+        _need(new_v, torch.bfloat16, "new_v")
+        _check(lib().pa_decode_store(_ptr(out), _ptr(q), _row_stride(q, "q"), _ptr(new_k), _row_stride(new_k, "new_k"),
+                                     _ptr(new_v), _row_stride(new_v, "new_v"), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(block_tables), mb, _ptr(context_lens), batch, hq, hkv, d, B, nb,
+                                     float(softmax_scale), _ptr(workspace), workspace.numel(), _stream(stream)),
+               "pa_decode_store")
+        return out
     _check(lib().pa_decode(_ptr(out), _ptr(q), _row_stride(q, "q"), _ptr(k_cache), _ptr(v_cache),
                            _ptr(block_tables), mb, _ptr(context_lens), batch, hq, hkv, d, B, nb,
                            float(softmax_scale), _ptr(workspace), workspace.numel(), _stream(stream)),

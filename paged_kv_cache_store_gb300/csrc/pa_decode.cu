@@ -124,6 +124,11 @@ struct DecodeArgs {
     int *ws_ctr;        // [2]                     chunk ranges taken, CTAs done taking
     DevError *err;
     int32_t checked;
+    // Fused store (pa_decode_store): the new token's K and V rows, written to
+    // their slots by the producer that loads the sequence's last tile.
+    const uint2 *new_k, *new_v;  // null: plain decode
+    int64_t new_k_stride, new_v_stride;  // in 8-byte units
+    uint2 *k_cache, *v_cache;
 };
 
 __device__ __forceinline__ int clamp_ctx(const DecodeArgs &a, int b, bool report) {
@@ -483,6 +488,20 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                             win = fetch(cur, lb);
                         }
                         const int blk = __shfl_sync(FULL, win, lb - wbase);
+                        const int ctx = ctx_s[cur.b];
+                        if (a.new_k && t == cur.nt - 1 && ps <= ctx - 1 && ctx - 1 < ps + a.box_rows &&
+                            blk >= 0 && blk < a.num_blocks) {
+                            // Fused store: this box holds the new token (position ctx-1).  Write its
+                            // kv head's row (128 bf16 = 32 lanes x 8 bytes) to the slot first, then make
+                            // the write visible to the tile copy (generic -> async proxy).
+                            const long long slot = (long long)blk * a.block_size + (ctx - 1) % a.block_size;
+                            const uint2 *src = (isk ? a.new_k + cur.b * a.new_k_stride : a.new_v + cur.b * a.new_v_stride) +
+                                               cur.g * (D / 4);
+                            uint2 *dstc = (isk ? a.k_cache : a.v_cache) + (slot * a.Hkv + cur.g) * (D / 4);
+                            dstc[lane] = __ldg(src + lane);
+                            asm volatile("fence.proxy.async.global;" ::: "memory");
+                            __syncwarp();
+                        }
                         if (lane == 0) {
                             if (isk && a.checked && (blk < 0 || blk >= a.num_blocks))
                                 record_error(a.err, PA_DEV_BAD_BLOCK, (long long)cur.b * a.max_blocks + lb);
@@ -876,12 +895,17 @@ size_t pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32
     return ws_layout(G).total;
 }
 
-pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *k_cache,
-                    const void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
-                    const int32_t *context_lens, int32_t batch, int32_t num_q_heads,
-                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                    float softmax_scale, void *workspace, size_t workspace_bytes, pa_stream_t stream) {
-    using namespace pa;
+}  // extern "C"
+
+namespace pa {
+namespace {
+
+pa_status decode_impl(void *out, const void *q, int64_t q_row_stride, void *k_cache, void *v_cache,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                      int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                      int32_t num_blocks, float softmax_scale, void *workspace, size_t workspace_bytes,
+                      const void *new_k, int64_t new_k_row_stride, const void *new_v, int64_t new_v_row_stride,
+                      pa_stream_t stream) {
     if (batch < 0) return fail(PA_ERR_INVALID_ARG, "batch < 0");
     if (batch == 0) return PA_OK;
     if (batch > kMaxBatch) return fail(PA_ERR_UNSUPPORTED, "batch %d > %d", batch, kMaxBatch);
@@ -946,6 +970,12 @@ pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *
     A.ws_ctr = reinterpret_cast<int *>(ws + W.ctr_off);
     A.err = device_error_ptr();
     A.checked = checked_mode() ? 1 : 0;
+    A.new_k = static_cast<const uint2 *>(new_k);
+    A.new_v = static_cast<const uint2 *>(new_v);
+    A.new_k_stride = new_k_row_stride / 4;
+    A.new_v_stride = new_v_row_stride / 4;
+    A.k_cache = static_cast<uint2 *>(k_cache);
+    A.v_cache = static_cast<uint2 *>(v_cache);
 
     const int sms = std::min(sm_count(), kMaxGrid);
     if (sms <= 0) return fail(PA_ERR_CUDA, "no CUDA device");
@@ -956,6 +986,41 @@ pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *
         case 4: return launch<4>(A, tk, tv, sms, s);
         default: return launch<8>(A, tk, tv, sms, s);
     }
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" {
+
+pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const void *k_cache,
+                    const void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *context_lens, int32_t batch, int32_t num_q_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                    float softmax_scale, void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+    return pa::decode_impl(out, q, q_row_stride, const_cast<void *>(k_cache), const_cast<void *>(v_cache),
+                           block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, num_kv_heads,
+                           head_dim, block_size, num_blocks, softmax_scale, workspace, workspace_bytes, nullptr, 0,
+                           nullptr, 0, stream);
+}
+
+pa_status pa_decode_store(void *out, const void *q, int64_t q_row_stride, const void *new_k,
+                          int64_t new_k_row_stride, const void *new_v, int64_t new_v_row_stride, void *k_cache,
+                          void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *context_lens, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t block_size, int32_t num_blocks, float softmax_scale,
+                          void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+    using namespace pa;
+    if (batch > 0) {
+        if (!new_k || !new_v) return fail(PA_ERR_INVALID_ARG, "null new_k/new_v");
+        if (!aligned16(new_k) || !aligned16(new_v)) return fail(PA_ERR_INVALID_ARG, "new_k/new_v must be 16-byte aligned");
+        const int64_t row = (int64_t)num_kv_heads * D;
+        if (new_k_row_stride < row || new_v_row_stride < row || new_k_row_stride % 8 || new_v_row_stride % 8)
+            return fail(PA_ERR_INVALID_ARG, "new_k/new_v row strides must be >= num_kv_heads*head_dim and multiples of 8");
+    }
+    return decode_impl(out, q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, softmax_scale, workspace,
+                       workspace_bytes, new_k, new_k_row_stride, new_v, new_v_row_stride, stream);
 }
 
 }  // extern "C"

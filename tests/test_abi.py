@@ -162,3 +162,23 @@ def test_sample_argument_checks(L):
     assert _sample(L, es=1002) == pa.PA_ERR_INVALID_ARG
     assert _sample(L, lg=C.c_void_p(258)) == pa.PA_ERR_INVALID_ARG
     assert _sample(L, b=70000) == pa.PA_ERR_UNSUPPORTED
+
+
+def test_decode_store_argument_checks(L):
+    p = C.c_void_p(256)
+
+    def call(**kw):
+        a = dict(out=p, q=p, qs=2048, nk=p, nks=1024, nv=p, nvs=1024, k=p, v=p, bt=p, mb=16, ctx=p, batch=4,
+                 hq=16, hkv=8, d=128, B=256, nb=64, scale=0.088, ws=p, wsb=1 << 30, stream=None)
+        a.update(kw)
+        return L.pa_decode_store(a["out"], a["q"], a["qs"], a["nk"], a["nks"], a["nv"], a["nvs"], a["k"], a["v"],
+                                 a["bt"], a["mb"], a["ctx"], a["batch"], a["hq"], a["hkv"], a["d"], a["B"], a["nb"],
+                                 a["scale"], a["ws"], a["wsb"], a["stream"])
+
+    assert call(batch=0) == pa.PA_OK
+    assert call(nk=None) == pa.PA_ERR_INVALID_ARG
+    assert call(nv=C.c_void_p(264)) == pa.PA_ERR_INVALID_ARG      # unaligned
+    assert call(nks=1000) == pa.PA_ERR_INVALID_ARG                # stride below Hkv*D
+    assert call(nvs=1028) == pa.PA_ERR_INVALID_ARG                # not a multiple of 8
+    assert call(hq=24) == pa.PA_ERR_UNSUPPORTED                   # decode's own checks still apply
+    assert call(ws=None, wsb=0) == pa.PA_ERR_WORKSPACE

@@ -182,3 +182,58 @@ def test_decode_one_workspace_serves_every_gqa_group():
         assert pa.get_device_error() == (0, 0)
         want = O.decode(inp.q, inp.k_cache, inp.v_cache, inp.block_tables, inp.context_lens, inp.scale)
         assert_close(host_f64(out), want, f"shared workspace {hq}/8")
+
+
+def run_gpu_fused(inp, strided=False):
+    """pa_decode_store: the kernel stores the token's K/V itself, then decodes."""
+    kc, vc = dev_bf16(inp.k_cache), dev_bf16(inp.v_cache)
+    bt, ctx = dev_i32(inp.block_tables), dev_i32(inp.context_lens)
+    nk, nv = dev_bf16(inp.new_k), dev_bf16(inp.new_v)
+    if strided:  # K and V as column slices of one fused [batch, 2*Hkv*D] tensor
+        both = torch.cat([nk.reshape(inp.batch, -1), nv.reshape(inp.batch, -1)], dim=1)
+        half = nk[0].numel()
+        nk = both[:, :half].view(inp.batch, inp.num_kv_heads, inp.head_dim)
+        nv = both[:, half:].view(inp.batch, inp.num_kv_heads, inp.head_dim)
+    out = pa.decode(dev_bf16(inp.q), kc, vc, bt, ctx, inp.scale, new_k=nk, new_v=nv)
+    code, where = pa.get_device_error()
+    assert code == 0, (code, where)
+    return out, kc, vc
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8), (8, 8), (64, 8)])
+def test_decode_store_fused_edge_lengths(hq, hkv):
+    """The fused store leaves the caches exactly as store_kvcache would, and the
+    attention sees the new token."""
+    inp = make_decode(f"fused {hq}/{hkv}", 300 + hq, len(EDGE_CTX), hq, hkv, EDGE_CTX)
+    out, kc, vc = run_gpu_fused(inp, strided=(hq == 32))
+    want, okc, ovc = run_oracle_step(inp)
+    assert np.array_equal(host_bits(kc), okc) and np.array_equal(host_bits(vc), ovc)
+    assert_close(host_f64(out), want, f"fused decode {hq}/{hkv}")
+
+
+@pytest.mark.parametrize("B", [16, 64, 256])
+def test_decode_store_fused_block_sizes_and_zero_rows(B):
+    ctx = [1, B - 1, B, B + 1, 0, 3 * B + 7]
+    inp = make_decode(f"fused B={B}", 400 + B, len(ctx), 32, 8, [max(c, 1) for c in ctx], block_size=B)
+    inp.context_lens[:] = ctx
+    out, kc, vc = run_gpu_fused(inp)
+    # ctx == 0 rows store nothing (as a -1 slot would), the others one row.
+    okc, ovc = inp.k_cache.copy(), inp.v_cache.copy()
+    slots = np.array([O.decode_slot(inp.block_tables[b], B, c) if c > 0 else -1 for b, c in enumerate(ctx)], np.int32)
+    O.store_kvcache(inp.new_k, inp.new_v, okc, ovc, slots)
+    assert np.array_equal(host_bits(kc), okc) and np.array_equal(host_bits(vc), ovc)
+    want = O.decode(inp.q, okc, ovc, inp.block_tables, inp.context_lens, inp.scale)
+    assert_close(host_f64(out), want, f"fused B={B}")
+
+
+def test_decode_store_fused_workload_full_size():
+    """The qwen3-0.6b decode workload through the fused path: caches bit-exact,
+    sampled rows against the oracle, and the same output as the unfused step."""
+    inp = decode_config(2)
+    out, kc, vc = run_gpu_fused(inp)
+    out2, kc2, vc2 = run_gpu_step(inp)
+    assert torch.equal(kc, kc2) and torch.equal(vc, vc2)
+    assert torch.equal(out, out2)
+    rows = np.arange(0, inp.batch * inp.num_q_heads, 37)
+    want, _, _ = run_oracle_step(inp, rows=rows)
+    assert_close(host_f64(out).reshape(-1, 128)[rows], want, "fused workload")
