@@ -265,7 +265,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     return false;
 }
 
-template <int G>
+// STORE: the fused store of pa_decode_store (a separate instantiation, so the
+// plain decode's producer loop carries none of it).
+template <int G, bool STORE>
 __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeArgs a) {
@@ -463,6 +465,9 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                     }
                     ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
                 }
+                // Fused store: the position of the new token when this segment ends
+                // with the sequence's last tile (-1: nothing to store here).
+                const int store_p = (STORE && cur.t_end == cur.nt) ? cur.p_end - 1 : -1;
                 for (int t = cur.t_begin; ok && t < cur.t_end; ++t) {
                     const int tg = (int)((cur.pos + (t - cur.t_begin)) % C::NGRP);  // consumer group of the tile
                     const uint32_t n = tg ? n1++ : n0++;
@@ -488,13 +493,11 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                             win = fetch(cur, lb);
                         }
                         const int blk = __shfl_sync(FULL, win, lb - wbase);
-                        const int ctx = ctx_s[cur.b];
-                        if (a.new_k && t == cur.nt - 1 && ps <= ctx - 1 && ctx - 1 < ps + a.box_rows &&
-                            blk >= 0 && blk < a.num_blocks) {
+                        if (STORE && store_p >= ps && store_p < ps + a.box_rows && blk >= 0 && blk < a.num_blocks) {
                             // Fused store: this box holds the new token (position ctx-1).  Write its
                             // kv head's row (128 bf16 = 32 lanes x 8 bytes) to the slot first, then make
                             // the write visible to the tile copy (generic -> async proxy).
-                            const long long slot = (long long)blk * a.block_size + (ctx - 1) % a.block_size;
+                            const long long slot = (long long)blk * a.block_size + store_p % a.block_size;
                             const uint2 *src = (isk ? a.new_k + cur.b * a.new_k_stride : a.new_v + cur.b * a.new_v_stride) +
                                                cur.g * (D / 4);
                             uint2 *dstc = (isk ? a.k_cache : a.v_cache) + (slot * a.Hkv + cur.g) * (D / 4);
@@ -842,24 +845,29 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     }
 }
 
-int g_attr_done[64][4] = {};
+int g_attr_done[64][8] = {};
 
-template <int G>
+template <int G, bool STORE>
 pa_status launch(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
                  cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
-    const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+    const int gi = (G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3) + (STORE ? 4 : 0);
     if (dev >= 0 && dev < 64 && !g_attr_done[dev][gi]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<G, STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)Cfg<G>::smem_bytes(kMaxBatch));
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_kernel)");
         g_attr_done[dev][gi] = 1;
     }
     // Programmatic dependent launch: the grid may start while the previous
     // kernel on the stream finishes; it reads nothing before griddepcontrol.wait.
-    return launch_pdl(decode_kernel<G>, dim3((unsigned)grid), dim3(Cfg<G>::NTHREADS), Cfg<G>::smem_bytes(a.batch),
-                      st, "decode_kernel", tk, tv, a);
+    return launch_pdl(decode_kernel<G, STORE>, dim3((unsigned)grid), dim3(Cfg<G>::NTHREADS),
+                      Cfg<G>::smem_bytes(a.batch), st, "decode_kernel", tk, tv, a);
+}
+
+template <int G>
+pa_status launch_g(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int grid, cudaStream_t st) {
+    return a.new_k ? launch<G, true>(a, tk, tv, grid, st) : launch<G, false>(a, tk, tv, grid, st);
 }
 
 // Workspace: the two tail counters and the per-range arrival counters first
@@ -981,10 +989,10 @@ pa_status decode_impl(void *out, const void *q, int64_t q_row_stride, void *k_ca
     if (sms <= 0) return fail(PA_ERR_CUDA, "no CUDA device");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (G) {
-        case 1: return launch<1>(A, tk, tv, sms, s);
-        case 2: return launch<2>(A, tk, tv, sms, s);
-        case 4: return launch<4>(A, tk, tv, sms, s);
-        default: return launch<8>(A, tk, tv, sms, s);
+        case 1: return launch_g<1>(A, tk, tv, sms, s);
+        case 2: return launch_g<2>(A, tk, tv, sms, s);
+        case 4: return launch_g<4>(A, tk, tv, sms, s);
+        default: return launch_g<8>(A, tk, tv, sms, s);
     }
 }
 
