@@ -2,11 +2,12 @@
 //
 // store: [NV12 §12.6 "Triton KV Cache Store Kernel"] each token whose slot
 // is not negative copies its Hkv*D K values to k_cache[slot*Hkv*D ...] and
-// its V values to v_cache.  It is a pure copy: 16-byte vector loads and
-// stores, one CTA per (token, K-or-V) row so a row's 2 KiB (Hkv=8, D=128)
-// go out as fully coalesced 512-byte warp transactions.  HBM-bound at
-// 8 KiB of traffic per stored token (2 KiB read + 2 KiB write for each of K
-// and V).
+// its V values to v_cache.  It is a pure copy: a warp copies one (token,
+// K-or-V) row at a time (2 KiB at Hkv=8, D=128) with 16-byte non-allocating
+// loads, up to four per lane in flight before their stores, so each row
+// moves as fully coalesced 512-byte warp transactions; a grid of at most
+// eight CTAs per SM strides over the rows.  HBM-bound at 8 KiB of traffic per
+// stored token (2 KiB read + 2 KiB write for each of K and V).
 //
 // All three kernels are programmatic dependent launches: they start by
 // waiting for the preceding work on the stream (griddepcontrol.wait) and
@@ -20,27 +21,45 @@
 namespace pa {
 namespace {
 
-__global__ void __launch_bounds__(128) store_kvcache_kernel(
+constexpr int STORE_THREADS = 256;
+
+__device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__global__ void __launch_bounds__(STORE_THREADS) store_kvcache_kernel(
     const uint4 *__restrict__ key, int64_t key_stride16, const uint4 *__restrict__ value,
     int64_t value_stride16, uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
-    const int32_t *__restrict__ slot_mapping, int32_t row16, int64_t num_slots, DevError *err) {
+    const int32_t *__restrict__ slot_mapping, int32_t row16, int64_t num_slots, int32_t num_tokens,
+    DevError *err) {
     pdl_wait_then_release();
-    const int64_t token = blockIdx.x;
-    const bool is_v = blockIdx.y != 0;
-    const int32_t slot = __ldg(slot_mapping + token);
-    if (slot < 0) return;  // padding
-    if (slot >= num_slots) {
-        if (threadIdx.x == 0 && !is_v) record_error(err, PA_DEV_BAD_SLOT, token);
-        return;
-    }
-    const uint4 *src = is_v ? value + token * value_stride16 : key + token * key_stride16;
-    uint4 *dst = (is_v ? v_cache : k_cache) + static_cast<int64_t>(slot) * row16;
-    for (int j = threadIdx.x; j < row16; j += blockDim.x) {
-        uint4 v;
-        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                     : "l"(src + j));
-        dst[j] = v;
+    const int lane = threadIdx.x & 31;
+    const int64_t nrows = 2LL * num_tokens;  // row r: token r / 2, K (even) or V (odd)
+    const int64_t wstride = (int64_t)gridDim.x * (STORE_THREADS / 32);
+    for (int64_t r = (int64_t)blockIdx.x * (STORE_THREADS / 32) + (threadIdx.x >> 5); r < nrows; r += wstride) {
+        const int64_t token = r >> 1;
+        const bool is_v = (r & 1) != 0;
+        const int32_t slot = __ldg(slot_mapping + token);
+        if (slot < 0) continue;  // padding
+        if (slot >= num_slots) {
+            if (lane == 0 && !is_v) record_error(err, PA_DEV_BAD_SLOT, token);
+            continue;
+        }
+        const uint4 *src = is_v ? value + token * value_stride16 : key + token * key_stride16;
+        uint4 *dst = (is_v ? v_cache : k_cache) + static_cast<int64_t>(slot) * row16;
+        for (int j0 = lane; j0 < row16; j0 += 128) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (j0 + 32 * u < row16) v[u] = ld_stream16(src + j0 + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (j0 + 32 * u < row16) dst[j0 + 32 * u] = v[u];
+        }
     }
 }
 
@@ -116,13 +135,16 @@ pa_status pa_store_kvcache(const void *key, int64_t key_row_stride, const void *
     if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
         return fail(PA_ERR_INVALID_ARG, "key/value/cache pointers must be 16-byte aligned");
     const int32_t row16 = static_cast<int32_t>(row / 8);
-    const dim3 grid(static_cast<unsigned>(num_tokens), 2);
-    const int threads = row16 >= 128 ? 128 : ((row16 + 31) / 32) * 32;
-    return launch_pdl(store_kvcache_kernel, grid, dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream),
-                      "store_kvcache_kernel", static_cast<const uint4 *>(key), (int64_t)(key_row_stride / 8),
-                      static_cast<const uint4 *>(value), (int64_t)(value_row_stride / 8),
-                      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, row16,
-                      num_slots, device_error_ptr());
+    const int sms = sm_count();
+    if (sms <= 0) return fail(PA_ERR_CUDA, "no CUDA device");
+    // One warp per row and step; at most 8 CTAs of 8 warps per SM.
+    const int64_t rows = 2LL * num_tokens, warps = STORE_THREADS / 32;
+    const int64_t grid = std::min<int64_t>((rows + warps - 1) / warps, 8LL * sms);
+    return launch_pdl(store_kvcache_kernel, dim3(static_cast<unsigned>(grid)), dim3(STORE_THREADS), 0,
+                      reinterpret_cast<cudaStream_t>(stream), "store_kvcache_kernel", static_cast<const uint4 *>(key),
+                      (int64_t)(key_row_stride / 8), static_cast<const uint4 *>(value),
+                      (int64_t)(value_row_stride / 8), static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
+                      slot_mapping, row16, num_slots, num_tokens, device_error_ptr());
 }
 
 pa_status pa_slot_mapping_decode(int32_t *slot_mapping, const int32_t *block_tables,
