@@ -75,7 +75,11 @@ constexpr int OFF_FLAGS = OFF_TMEM + 8;
 constexpr int OFF_BID = OFF_FLAGS + 16;  // block ids of the current unit, per producer warp
 constexpr int NBID = 32;
 constexpr int OFF_NU = OFF_BID + 2 * NBID * 4;  // two Unit slots (the softmax's next unit)
-constexpr int SMEM_USED = OFF_NU + 2 * 48;
+// The CTA-wide unit schedule: (query tile, sequence) groups sorted by their
+// number of KV tiles, longest first (used when there are at most SCHED_MAX).
+constexpr int SCHED_MAX = 512;
+constexpr int OFF_SCHED = OFF_NU + 2 * 48;  // uint16_t [SCHED_MAX]
+constexpr int SMEM_USED = OFF_SCHED + SCHED_MAX * 2;
 // Slack for aligning the dynamic shared-memory base to the 1 KiB the swizzled
 // tiles need (the base is normally aligned already; the kernel checks).
 constexpr int SMEM_SLACK = 256;
@@ -96,7 +100,7 @@ struct PrefillArgs {
     const int32_t *cu_k;
     const int32_t *bt;
     int32_t max_blocks, num_seqs, Hq, group, mtiles;
-    int32_t block_size, box_rows, box_halves, paged, causal, num_blocks, checked;
+    int32_t block_size, box_rows, box_halves, paged, causal, num_blocks, checked, sorted;
     float scale_log2;
     DevError *err;
 };
@@ -163,13 +167,29 @@ struct Unit {
 static_assert(sizeof(Unit) <= 48, "next-unit slot");
 static_assert(QST == 2, "the next-unit ring reuses a slot with the Q buffer of the same parity");
 
-__device__ __forceinline__ Unit unit_of(const PrefillArgs &a, int t) {
+// A group is (query tile mt, sequence s), numbered (mtiles-1-mt) * num_seqs
+// + s: the query tiles from the highest down, then the sequences.
+// KV tiles of group (mt, s); 0 when the query tile is empty or the lengths
+// are invalid.
+__device__ __forceinline__ int group_tiles(const PrefillArgs &a, int mt, int s) {
+    const int Lq = __ldg(a.cu_q + s + 1) - __ldg(a.cu_q + s);
+    const int Lk = __ldg(a.cu_k + s + 1) - __ldg(a.cu_k + s);
+    const bool bad = Lq < 0 || Lk < Lq || (a.paged && Lk > a.max_blocks * a.block_size);
+    if (bad || mt * BM >= Lq) return 0;
+    const int last_row = min(mt * BM + BM, Lq) - 1;
+    const int key_end = a.causal ? min(Lk, Lk - Lq + last_row + 1) : Lk;
+    return (key_end + BN - 1) / BN;
+}
+
+// Unit t.  Sorted schedule: t = rank * Hq + q head, where rank indexes the
+// groups sorted longest first.  Otherwise t = ((mtiles-1-mt) * num_seqs + s)
+// * Hq + q head (empty query tiles included; next_valid_unit skips them).
+__device__ __forceinline__ Unit unit_of(const PrefillArgs &a, const uint16_t *sched, int t) {
     Unit U;
-    const int per = a.num_seqs * a.Hq;
-    const int mt = a.mtiles - 1 - t / per;
-    const int rem = t % per;
-    U.s = rem / a.Hq;
-    U.h = rem % a.Hq;
+    const int grp = a.sorted ? (int)sched[t / a.Hq] : t / a.Hq;
+    const int mt = a.mtiles - 1 - grp / a.num_seqs;
+    U.s = grp % a.num_seqs;
+    U.h = t % a.Hq;
     U.m0 = mt * BM;
     U.q0 = __ldg(a.cu_q + U.s);
     U.Lq = __ldg(a.cu_q + U.s + 1) - U.q0;
@@ -189,7 +209,8 @@ __device__ __forceinline__ Unit unit_of(const PrefillArgs &a, int t) {
     return U;
 }
 
-// First unit >= t (stepping by gridDim.x) whose query rows exist.  The warp
+// First unit >= t (stepping by gridDim.x) whose query rows exist (unsorted
+// schedule).  The warp
 // tests 32 candidates per round of loads and takes the first by ballot, so
 // skipping the many empty high query tiles costs one load latency per 32.
 // Every lane must call it; every role gets the same answer.
@@ -207,6 +228,19 @@ __device__ __forceinline__ int next_valid_unit(const PrefillArgs &a, int t, int 
         if (m) return base + (__ffs(m) - 1) * (int)gridDim.x;
     }
     return nunits;
+}
+
+// Unit number k of this CTA (prev: its unit number k - 1), nunits after the
+// last.  Sorted schedule: round k of gridDim.x consecutive units goes to the
+// CTAs in ascending order when k is even and descending when k is odd, so
+// every CTA gets a long and a short unit in each pair of rounds.  Warp-
+// collective; every role gets the same sequence.
+__device__ __forceinline__ int cta_unit(const PrefillArgs &a, int nsorted, int k, int prev, int nunits, int lane) {
+    if (a.sorted) {
+        const long long t = (long long)k * gridDim.x + ((k & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
+        return t < nsorted ? (int)t : nunits;
+    }
+    return next_valid_unit(a, k == 0 ? (int)blockIdx.x : prev + (int)gridDim.x, nunits, lane);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -238,16 +272,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_alloc(tmem_slot, TMEM_COLS);
         tmem_relinquish();
     }
+    uint16_t *sched = reinterpret_cast<uint16_t *>(smem + OFF_SCHED);
+    int nsorted = 0;  // groups of the sorted schedule
+    if (a.sorted) {
+        // Rank every (query tile, sequence) group by (KV tiles descending,
+        // group id ascending); the K ring holds the keys until the copies start.
+        const int ng = a.mtiles * a.num_seqs;
+        uint64_t *key = reinterpret_cast<uint64_t *>(smem + OFF_K);
+        for (int g = threadIdx.x; g < ng; g += NTHREADS) {
+            const int mt = a.mtiles - 1 - g / a.num_seqs, s = g % a.num_seqs;
+            const int n = group_tiles(a, mt, s);
+            key[g] = n > 0 ? ((uint64_t)n << 32) | (uint32_t)(0xffffffffu - (uint32_t)g) : 0ull;
+            if (n == 0 && mt == 0 && blockIdx.x == 0) {
+                const int Lq = __ldg(a.cu_q + s + 1) - __ldg(a.cu_q + s);
+                const int Lk = __ldg(a.cu_k + s + 1) - __ldg(a.cu_k + s);
+                if (Lq < 0 || Lk < Lq || (a.paged && Lk > a.max_blocks * a.block_size))
+                    record_error(a.err, PA_DEV_BAD_SEQLENS, s);
+            }
+        }
+        __syncthreads();
+        // Every thread scans all keys at least once (which also counts the
+        // non-empty groups); a group's rank is the number of larger keys.
+        for (int g = threadIdx.x, first = 1; first || g < ng; g += NTHREADS, first = 0) {
+            const uint64_t mine = g < ng ? key[g] : 0ull;
+            int rank = 0, nz = 0;
+            for (int j = 0; j < ng; ++j) {
+                const uint64_t kj = key[j];
+                rank += kj > mine;
+                nz += kj != 0ull;
+            }
+            if (first) nsorted = nz;
+            if (mine != 0ull) sched[rank] = (uint16_t)g;
+        }
+        // The K ring's first bytes are written by TMA next: order these
+        // generic-proxy accesses before them.
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    nsorted *= a.Hq;  // units of the sorted schedule
     // Unit i goes to slot i & 1; a slot is rewritten only after the softmax read
     // it (the Q.K thread cannot start unit i+2 before the softmax has released
     // the Q buffer of unit i), so a reader is never two phases behind.
     Unit *nu = reinterpret_cast<Unit *>(smem + OFF_NU);
 
-    // Every role walks the same units t = blockIdx.x, +gridDim.x, ... and the
+    // Every role walks the same units (cta_unit) and the
     // same global KV-tile counter g, so ring stages and barrier phases agree.
     if (warp == W_QK || warp == W_V) {
         // ------------------------------------------------------------ TMA producers
@@ -265,9 +336,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int R = a.box_rows;
         uint32_t g = 0, u = 0, nq = 0;  // KV tiles, units and Q copies issued by this warp
         bool ok = true;
-        for (int t = next_valid_unit(a, blockIdx.x, nunits, lane); ok && t < nunits;
-             t = next_valid_unit(a, t + gridDim.x, nunits, lane)) {
-            const Unit U = unit_of(a, t);
+        for (int k = 0, t = cta_unit(a, nsorted, 0, 0, nunits, lane); ok && t < nunits;
+             ++k, t = cta_unit(a, nsorted, k, t, nunits, lane)) {
+            const Unit U = unit_of(a, sched, t);
             const int32_t *bt = a.bt + (int64_t)U.s * a.max_blocks;
             if (U.valid && a.paged) {
                 // The warp fetches the unit's first NBID block ids at once.
@@ -387,11 +458,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_arrive(&bar[B_NU + (i & 1)]);
             return true;
         };
-        // All lanes walk the units (next_valid_unit is warp-collective); lane 0
+        // All lanes walk the units (cta_unit is warp-collective); lane 0
         // waits and issues.
-        for (int t = next_valid_unit(a, blockIdx.x, nunits, lane); ok && t < nunits;
-             t = next_valid_unit(a, t + gridDim.x, nunits, lane)) {
-            const Unit U = unit_of(a, t);
+        for (int k = 0, t = cta_unit(a, nsorted, 0, 0, nunits, lane); ok && t < nunits;
+             ++k, t = cta_unit(a, nsorted, k, t, nunits, lane)) {
+            const Unit U = unit_of(a, sched, t);
             if (!U.valid) continue;
             if (lane == 0) {
                 if (is_qk) {
@@ -668,6 +739,7 @@ extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_s
     A.causal = causal ? 1 : 0;
     A.num_blocks = num_blocks;
     A.checked = checked_mode() ? 1 : 0;
+    A.sorted = (int64_t)A.mtiles * num_seqs <= SCHED_MAX ? 1 : 0;
     A.scale_log2 = softmax_scale * 1.4426950408889634f;
     A.err = device_error_ptr();
 
