@@ -167,3 +167,27 @@ def test_prefill_repeat_runs_bitwise_identical():
         else:
             assert torch.equal(bits, ref), f"run {it} differs"
     assert pa.get_device_error() == (0, 0)
+
+
+def test_prefill_schedules_agree():
+    """Up to 512 (query tile, sequence) groups the kernel deals units out
+    longest first; above that, in query-tile order.  A larger max_seqlen_q
+    hint (allowed: it only bounds the lengths) switches to the second order
+    on the same inputs: the outputs must be bit-identical, and match the
+    oracle."""
+    lk = [130, 700, 260, 1025, 77, 513, 300, 900, 128, 640, 999, 20, 400, 256, 1300, 90]
+    c = [0, 256, 3, 512, 0, 129, 44, 0, 0, 300, 768, 0, 17, 0, 256, 0]
+    p = make_prefill("sched", 31, lk, None, 16, 8, cached_tokens=c)
+    kc, vc = dev_bf16(p.k_cache), dev_bf16(p.v_cache)
+    bt, cq, ck = dev_i32(p.block_tables), dev_i32(p.cu_seqlens_q), dev_i32(p.cu_seqlens_k)
+    slots = pa.slot_mapping_prefill(bt, cq, ck, p.block_size, total_q=p.total_q)
+    pa.store_kvcache(dev_bf16(p.new_k), dev_bf16(p.new_v), kc, vc, slots)
+    q = dev_bf16(p.q)
+    mq, mk = int(p.seqlens_q.max()), int(p.seqlens_k.max())
+    assert -(-mq // 128) * p.num_seqs <= 512 < 40 * p.num_seqs
+    sorted_out = pa.prefill_varlen(q, kc, vc, cq, ck, mq, mk, p.scale, block_tables=bt)
+    plain_out = pa.prefill_varlen(q, kc, vc, cq, ck, 40 * 128, mk, p.scale, block_tables=bt)
+    assert pa.get_device_error() == (0, 0)
+    assert torch.equal(sorted_out, plain_out)
+    want, _, _ = oracle_prefill(p)
+    assert_close(host_f64(sorted_out), want)
