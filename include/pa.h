@@ -207,9 +207,10 @@ PA_API pa_status pa_decode(void *out, const void *q, int64_t q_row_stride, const
  * written to slot block_tables[b][(ctx-1)/B]*B + (ctx-1)%B of k_cache /
  * v_cache -- the token at position ctx-1, which the query is -- and the
  * attention then reads them like every other key.  The write is done inside
- * the decode kernel by the warp that copies the sequence's last tile (one
- * kv head's 256-byte row each), so the step needs neither a slot mapping
- * nor a separate store launch.  Afterwards the caches hold exactly what
+ * the decode kernel by the consumer warp that owns the token's key in the
+ * sequence's last tile: it puts the row into that landed tile and into the
+ * slot (one kv head's 256-byte row each), so the step needs neither a slot
+ * mapping nor a separate store launch.  Afterwards the caches hold exactly what
  * pa_slot_mapping_decode + pa_store_kvcache would have written.  Other
  * arguments, the workspace contract and the outputs are those of pa_decode;
  * new_k / new_v 16-byte aligned.

@@ -124,8 +124,9 @@ struct DecodeArgs {
     int *ws_ctr;        // [2]                     chunk ranges taken, CTAs done taking
     DevError *err;
     int32_t checked;
-    // Fused store (pa_decode_store): the new token's K and V rows, written to
-    // their slots by the producer that loads the sequence's last tile.
+    // Fused store (pa_decode_store): the new token's K and V rows, patched into
+    // the landed tile and written to their slots by the consumer warp that
+    // owns the token's key in the sequence's last tile.
     const uint2 *new_k, *new_v;  // null: plain decode
     int64_t new_k_stride, new_v_stride;  // in 8-byte units
     uint2 *k_cache, *v_cache;
@@ -246,6 +247,10 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint2 v) {
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
@@ -266,7 +271,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 }
 
 // STORE: the fused store of pa_decode_store (a separate instantiation, so the
-// plain decode's producer loop carries none of it).
+// plain decode carries none of it).
 template <int G, bool STORE>
 __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -465,9 +470,6 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                     }
                     ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
                 }
-                // Fused store: the position of the new token when this segment ends
-                // with the sequence's last tile (-1: nothing to store here).
-                const int store_p = (STORE && cur.t_end == cur.nt) ? cur.p_end - 1 : -1;
                 for (int t = cur.t_begin; ok && t < cur.t_end; ++t) {
                     const int tg = (int)((cur.pos + (t - cur.t_begin)) % C::NGRP);  // consumer group of the tile
                     const uint32_t n = tg ? n1++ : n0++;
@@ -493,18 +495,6 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                             win = fetch(cur, lb);
                         }
                         const int blk = __shfl_sync(FULL, win, lb - wbase);
-                        if (STORE && store_p >= ps && store_p < ps + a.box_rows && blk >= 0 && blk < a.num_blocks) {
-                            // Fused store: this box holds the new token (position ctx-1).  Write its
-                            // kv head's row (128 bf16 = 32 lanes x 8 bytes) to the slot first, then make
-                            // the write visible to the tile copy (generic -> async proxy).
-                            const long long slot = (long long)blk * a.block_size + store_p % a.block_size;
-                            const uint2 *src = (isk ? a.new_k + cur.b * a.new_k_stride : a.new_v + cur.b * a.new_v_stride) +
-                                               cur.g * (D / 4);
-                            uint2 *dstc = (isk ? a.k_cache : a.v_cache) + (slot * a.Hkv + cur.g) * (D / 4);
-                            dstc[lane] = __ldg(src + lane);
-                            asm volatile("fence.proxy.async.global;" ::: "memory");
-                            __syncwarp();
-                        }
                         if (lane == 0) {
                             if (isk && a.checked && (blk < 0 || blk >= a.num_blocks))
                                 record_error(a.err, PA_DEV_BAD_BLOCK, (long long)cur.b * a.max_blocks + lb);
@@ -740,6 +730,31 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&qempty[k & 1]);
+            // Fused store: the new token (position ctx-1) is key kn of the
+            // sequence's last tile, owned by one warp of one group.  That warp
+            // loads its K and V rows now and, when the tile has landed, writes
+            // them over the cache's (stale) rows in shared memory and into the
+            // cache slot.  Nothing in this launch copies that slot, so no proxy
+            // fence is needed on the global side.
+            int st_t = -1, st_kn = 0;
+            long long st_slot = 0;
+            uint2 st_k = make_uint2(0, 0), st_v = make_uint2(0, 0);
+            if (STORE && sg.t_end == sg.nt) {
+                const int pn = sg.p_end - 1, tn = pn / TILE, kn = pn % TILE;
+                if ((int)((sg.pos + (tn - sg.t_begin)) % C::NGRP) == grp && kn / KPW == wig) {
+                    const int blk = __ldg(a.block_tables + (int64_t)sg.b * a.max_blocks + pn / a.block_size);
+                    if (blk >= 0 && blk < a.num_blocks) {  // else the box reads as zeros, as unfused
+                        st_t = tn;
+                        st_kn = kn;
+                        st_slot = (long long)blk * a.block_size + pn % a.block_size;
+                        st_k = __ldg(a.new_k + sg.b * a.new_k_stride + sg.g * (D / 4) + lane);
+                        st_v = __ldg(a.new_v + sg.b * a.new_v_stride + sg.g * (D / 4) + lane);
+                    }
+                }
+            }
+            // Lane l holds bytes 8l..8l+7 of the row: 16-byte column l/2 of row kn.
+            const uint32_t st_off = key_off(st_kn) + ((lane >> 4) & 1) * half_stride +
+                                    ((uint32_t)(((lane >> 1) & 7) ^ (st_kn & 7)) << 4) + (lane & 1) * 8;
             float m_ref = -INFINITY, l_part = 0.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -753,6 +768,12 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                     const uint32_t ks = smem_addr(smem + stage * C::STAGE_BYTES);
                     const uint32_t vs = ks + TILE * ROW_BYTES;
                     const int nvalid = min(TILE, sg.p_end - t * TILE);
+                    const bool st_here = STORE && t == st_t;
+                    if (st_here) {
+                        st_shared_v2(ks + st_off, st_k);
+                        a.k_cache[(st_slot * a.Hkv + sg.g) * (D / 4) + lane] = st_k;
+                        __syncwarp();
+                    }
                     // ---- S = Q.K^T for this warp's 16 keys: two n-tiles of 8 keys
                     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     #pragma unroll
@@ -806,6 +827,11 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                             }
                             __syncwarp();
                         }
+                        if (st_here) {
+                            st_shared_v2(vs + st_off, st_v);
+                            a.v_cache[(st_slot * a.Hkv + sg.g) * (D / 4) + lane] = st_v;
+                            __syncwarp();
+                        }
     #pragma unroll
                         for (int j = 0; j < 16; j += 2) {
                             const int chunk = j + (mi >> 1);
@@ -816,9 +842,9 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                             mma16816(o[j], pa0, 0u, pa2, 0u, b0, b1);
                             mma16816(o[j + 1], pa0, 0u, pa2, 0u, b2, b3);
                         }
-                        // The zeroed rows are rewritten by the next TMA copy into this
-                        // stage: order the generic-proxy stores before it.
-                        if (ragged) fence_proxy_async_smem();
+                        // The zeroed or patched rows are rewritten by the next TMA copy
+                        // into this stage: order the generic-proxy stores before it.
+                        if (ragged || st_here) fence_proxy_async_smem();
                     }
                 }
                 __syncwarp();
