@@ -102,7 +102,12 @@ struct Cfg {
     static constexpr int OFF_FLAGS = OFF_BAR + NBAR * 8;   // [0]: abort
     static constexpr int OFF_TK = OFF_FLAGS + 16;          // Ticket [NTK]
     static constexpr int OFF_WSUM = OFF_TK + NTK * 32;     // scan scratch [NWARPS] uint32
-    static constexpr int OFF_CUM = OFF_WSUM + 64;          // per-head tile prefix sum [batch + 1] uint32
+    // Rows the consumers' ldmatrix reads instead of a tile row: per consumer
+    // warp the new token's K and V rows (fused store), then one zero row for
+    // keys past the context.  Never written by TMA.
+    static constexpr int OFF_SIDE = OFF_WSUM + 64;
+    static constexpr int OFF_ZERO = OFF_SIDE + 2 * NCW * ROW_BYTES;
+    static constexpr int OFF_CUM = OFF_ZERO + ROW_BYTES;   // per-head tile prefix sum [batch + 1] uint32
     __host__ __device__ static constexpr size_t off_ctx(int batch) { return OFF_CUM + 4 * (size_t)(batch + 1); }  // [batch] int
     __host__ __device__ static constexpr size_t smem_bytes(int batch) { return off_ctx(batch) + 4 * (size_t)batch + 1024; }
     static_assert(smem_bytes(kMaxBatch) <= 232448, "shared memory budget");
@@ -321,6 +326,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     // Inputs may come from the kernel this one was launched behind.
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
+    if (threadIdx.x < ROW_BYTES / 16) st_shared_zero16(smem_addr(smem + C::OFF_ZERO) + 16 * threadIdx.x);
     // Per-sequence tile counts and their exclusive prefix sum: each thread
     // takes a run of `per` sequences, then a block-wide scan of the run sums.
     {
@@ -708,8 +714,14 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
         return (uint32_t)((kk / br) * (br * ROW_BYTES) + (kk % br) * 128);
     };
     const uint32_t half_stride = (uint32_t)br * 128;
-    const uint32_t qk_row = key_off(wig * KPW + (mi >> 1) * 8 + r8);  // ldmatrix row of this lane in Q.K
-    const uint32_t pv_row = key_off(wig * KPW + (mi & 1) * 8 + r8);   // ... and in P.V
+    const int qk_key = wig * KPW + (mi >> 1) * 8 + r8;  // tile key whose row this lane addresses in Q.K
+    const int pv_key = wig * KPW + (mi & 1) * 8 + r8;   // ... and in P.V
+    const uint32_t qk_row = key_off(qk_key);
+    const uint32_t pv_row = key_off(pv_key);
+    // Unswizzled 256-byte rows outside the tiles (16-byte column c at 16c).
+    const uint32_t side_k = smem_addr(smem + C::OFF_SIDE) + 2 * warp * ROW_BYTES;
+    const uint32_t side_v = side_k + ROW_BYTES;
+    const uint32_t zero_row = smem_addr(smem + C::OFF_ZERO);
     float *slot_base = reinterpret_cast<float *>(smem + C::OFF_SLOT);
 
     uint32_t qa[8][2];  // A fragments of q: [k step][cols 2*t4.. and 2*t4+8..] of row g4
@@ -732,10 +744,10 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
             if (lane == 0) mbar_arrive(&qempty[k & 1]);
             // Fused store: the new token (position ctx-1) is key kn of the
             // sequence's last tile, owned by one warp of one group.  That warp
-            // loads its K and V rows now and, when the tile has landed, writes
-            // them over the cache's (stale) rows in shared memory and into the
-            // cache slot.  Nothing in this launch copies that slot, so no proxy
-            // fence is needed on the global side.
+            // loads its K and V rows now; at that tile it puts them in its side
+            // rows, where its ldmatrix reads them in place of the cache's
+            // (stale) rows, and writes them to the cache slot.  Nothing in this
+            // launch copies that slot, so no proxy fence is needed.
             int st_t = -1, st_kn = 0;
             long long st_slot = 0;
             uint2 st_k = make_uint2(0, 0), st_v = make_uint2(0, 0);
@@ -752,9 +764,6 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                     }
                 }
             }
-            // Lane l holds bytes 8l..8l+7 of the row: 16-byte column l/2 of row kn.
-            const uint32_t st_off = key_off(st_kn) + ((lane >> 4) & 1) * half_stride +
-                                    ((uint32_t)(((lane >> 1) & 7) ^ (st_kn & 7)) << 4) + (lane & 1) * 8;
             float m_ref = -INFINITY, l_part = 0.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -769,18 +778,22 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                     const uint32_t vs = ks + TILE * ROW_BYTES;
                     const int nvalid = min(TILE, sg.p_end - t * TILE);
                     const bool st_here = STORE && t == st_t;
-                    if (st_here) {
-                        st_shared_v2(ks + st_off, st_k);
+                    if (st_here) {  // lane l holds bytes 8l..8l+7 of each row
+                        st_shared_v2(side_k + 8 * lane, st_k);
+                        st_shared_v2(side_v + 8 * lane, st_v);
                         a.k_cache[(st_slot * a.Hkv + sg.g) * (D / 4) + lane] = st_k;
+                        a.v_cache[(st_slot * a.Hkv + sg.g) * (D / 4) + lane] = st_v;
                         __syncwarp();
                     }
+                    const bool k_side = st_here && qk_key == st_kn;
                     // ---- S = Q.K^T for this warp's 16 keys: two n-tiles of 8 keys
                     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const int chunk = 2 * kk + (mi & 1);  // 16-byte column of the row
                         const uint32_t ad =
-                            ks + qk_row + (chunk >> 3) * half_stride + ((uint32_t)((chunk & 7) ^ r8) << 4);
+                            k_side ? side_k + 16 * chunk
+                                   : ks + qk_row + (chunk >> 3) * half_stride + ((uint32_t)((chunk & 7) ^ r8) << 4);
                         uint32_t b0, b1, b2, b3;
                         ldsm_x4(ad, b0, b1, b2, b3);
                         mma16816(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
@@ -816,35 +829,21 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                     const uint32_t pa0 = pack_bf16(p[0], p[1]), pa2 = pack_bf16(p[2], p[3]);
                     // ---- O += P.V once the V tile has landed
                     if (wait_or_abort(&vfull[stage], ph, flags, a, 230 + warp)) {
-                        const bool ragged = nvalid < (wig + 1) * KPW;
-                        if (ragged) {
-                            // Rows past the context may hold anything (NaN included): zero
-                            // them so that p = 0 contributes exactly nothing.
-                            for (int c = lane; c < KPW * 16; c += 32) {
-                                const int kk = wig * KPW + (c >> 4);
-                                if (kk >= nvalid)
-                                    st_shared_zero16(vs + key_off(kk) + ((c >> 3) & 1) * half_stride + (c & 7) * 16);
-                            }
-                            __syncwarp();
-                        }
-                        if (st_here) {
-                            st_shared_v2(vs + st_off, st_v);
-                            a.v_cache[(st_slot * a.Hkv + sg.g) * (D / 4) + lane] = st_v;
-                            __syncwarp();
-                        }
+                        // Rows past the context may hold anything (NaN included) and
+                        // 0 * NaN is not 0: their lanes read the zero row instead.
+                        const bool v_alt = pv_key >= nvalid || (st_here && pv_key == st_kn);
+                        const uint32_t v_alt_row = pv_key >= nvalid ? zero_row : side_v;
     #pragma unroll
                         for (int j = 0; j < 16; j += 2) {
                             const int chunk = j + (mi >> 1);
                             const uint32_t ad =
-                                vs + pv_row + (chunk >> 3) * half_stride + ((uint32_t)((chunk & 7) ^ r8) << 4);
+                                v_alt ? v_alt_row + 16 * chunk
+                                      : vs + pv_row + (chunk >> 3) * half_stride + ((uint32_t)((chunk & 7) ^ r8) << 4);
                             uint32_t b0, b1, b2, b3;
                             ldsm_x4_t(ad, b0, b1, b2, b3);
                             mma16816(o[j], pa0, 0u, pa2, 0u, b0, b1);
                             mma16816(o[j + 1], pa0, 0u, pa2, 0u, b2, b3);
                         }
-                        // The zeroed or patched rows are rewritten by the next TMA copy
-                        // into this stage: order the generic-proxy stores before it.
-                        if (ragged || st_here) fence_proxy_async_smem();
                     }
                 }
                 __syncwarp();
