@@ -472,6 +472,41 @@ def run_ours(args):
     return 0
 
 
+def run_profile_case(args):
+    """A reduced decode workload for captures that replay each launch many
+    times (ncu --set full): the Qwen3-0.6B shape (batch 64, 16 q / 8 kv
+    heads, fused store) with context lengths ~ U[1, 1536], about 190 MB of
+    K/V (more than the 129 MB L2, a fraction of the full case).  Runs
+    `warmup` then `steps` fused decode steps with an L2 flush before each."""
+    import torch
+    import paged_kv_cache_store_gb300 as pa
+    from paged_kv_cache_store_gb300.workloads import make_decode
+    rng = np.random.default_rng(1002)
+    inp = make_decode("qwen3-0.6b decode b64 h16/8 ctx~U[1,1536]", 2, 64, 16, 8, rng.integers(1, 1537, size=64))
+    dev = torch.device("cuda", 0)
+
+    def to_dev(a, bf=False):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf else np.ascontiguousarray(a))
+        return (t.view(torch.bfloat16) if bf else t).to(dev)
+
+    kc, vc, q = to_dev(inp.k_cache, True), to_dev(inp.v_cache, True), to_dev(inp.q, True)
+    nk, nv = to_dev(inp.new_k, True), to_dev(inp.new_v, True)
+    bt, ctx = to_dev(inp.block_tables), to_dev(inp.context_lens)
+    out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
+    wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup + args.steps):
+        flush.zero_()
+        pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out, new_k=nk, new_v=nv)
+    torch.cuda.synchronize()
+    code, where = pa.get_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} at {where}")
+    print(f"profile case: {inp.batch} seqs, {int(inp.context_lens.sum())} context tokens, "
+          f"{args.warmup + args.steps} fused decode launches")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -481,11 +516,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--profile-case", choices=["decode-small"], default=None,
+                    help="run only a reduced case for a multi-pass ncu capture (no JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_case:
+        return run_profile_case(args)
     return run_ours(args)
 
 
