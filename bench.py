@@ -144,6 +144,24 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, dev, ws: int) -> float:
+    """The largest of every rank's x (all ranks get it); x itself when alone.
+    The job's time is its slowest rank's."""
+    if ws <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ws: int, units_per_rank: int, steps: int, total_ms: float) -> float:
+    """Whole-job units/s: every rank processed units_per_rank per step (weak
+    scaling), and the job took the slowest rank's total_ms."""
+    return ws * units_per_rank * steps / (total_ms / 1000.0)
+
+
 def time_oracle_step(inp, O, budget_s: float):
     """Runs the oracle's step (slot mapping, store, decode) on the workload for
     about budget_s seconds; returns (tokens/s, steps)."""
@@ -354,13 +372,9 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev, ws)
     ms_per_step = total_ms / args.steps
-    value = ws * inp.batch * args.steps / (total_ms / 1000.0)
+    value = job_throughput(ws, inp.batch, args.steps, total_ms)
 
     # The same step as three launches (slot mapping, store, decode: programmatic
     # dependent launches back to back), for comparison.
@@ -411,11 +425,8 @@ def run_ours(args):
         if i >= 2:
             e2e_ev[i - 2][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
-    t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_value = ws * inp.batch * args.steps / (float(t.item()) / 1000.0)
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), dev, ws)
+    e2e_value = job_throughput(ws, inp.batch, args.steps, e2e_ms)
 
     code, where = pa.get_device_error()
     if code:
