@@ -261,6 +261,28 @@ def measure_prefill(args, dev, stream, flush, bf16_peak):
     if code:
         raise RuntimeError(f"device error {code} at {where}")
     pre_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / len(evs)
+    step3_ms = sum(e[0].elapsed_time(e[2]) for e in evs) / len(evs)
+    # The same step as one launch: the fused store + prefill (cooperative).
+    wsf = pa.prefill_store_workspace(dev)
+
+    def fused():
+        pa.prefill_varlen(q, kc, vc, cq, ck, mq, mk, p.scale, block_tables=bt, out=out, new_k=nk, new_v=nv,
+                          workspace=wsf)
+
+    for _ in range(3):
+        fused()
+    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a_, b_ in fev:
+        flush.zero_()
+        a_.record(stream)
+        fused()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    code, where = pa.get_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} at {where}")
+    fused_ms = sum(a_.elapsed_time(b_) for a_, b_ in fev) / len(fev)
     slotmap_store_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)
     store_ms = sum(e[3].elapsed_time(e[1]) for e in evs) / len(evs)
     flops = 4 * p.head_dim * p.num_q_heads * prefill_pairs(p)
@@ -270,6 +292,7 @@ def measure_prefill(args, dev, stream, flush, bf16_peak):
     return {"workload": "varlen causal prefill, 16 seqs, 32 q / 8 kv heads, Lk ~ U[128,2048], 0..3 cached "
                         "blocks per seq, block_size 256 (suffix stored via slot_mapping first)",
             "total_q": p.total_q, "ms_prefill": pre_ms, "ms_slotmap_store": slotmap_store_ms, "ms_store": store_ms,
+            "ms_step_3_launches": step3_ms, "ms_step_fused": fused_ms,
             "algorithmic_flops": flops,
             "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": tflops, "peak": bf16_peak,
                          "unit": "TFLOP/s", "frac": tflops / bf16_peak, "traffic": None},

@@ -282,6 +282,43 @@ PA_API pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_strid
                                    int32_t causal, pa_stream_t stream);
 
 /*
+ * pa_prefill_store_varlen -- pa_prefill_varlen (paged) that first stores the
+ * uncached suffix.  [NV12 §12.6: store_kvcache then flash_attn_varlen_func,
+ * fused; PA3 §4: the slot of position p is block_table[p/B]*B + p%B]
+ *
+ * new_k / new_v hold the suffix tokens' K and V rows in cu_seqlens_q order
+ * ([total_q, Hkv, D] bf16, row strides in elements, multiples of 8, 16-byte
+ * aligned): token t of sequence s sits at position (Lk - Lq) + (t -
+ * cu_seqlens_q[s]), Lq / Lk its query / key lengths.  Each row is written to
+ * that position's slot of k_cache / v_cache, exactly what
+ * pa_slot_mapping_prefill + pa_store_kvcache would write (a block id outside
+ * [0, num_blocks) is recorded as PA_DEV_BAD_SLOT with where = t, and that row
+ * is not written); then the attention of pa_prefill_varlen runs over the
+ * pool, with the same arguments and output.  block_tables is required.
+ *
+ * One launch: the CTAs copy the rows, meet at a grid barrier, then attend.
+ * The launch is cooperative (its CTAs must be resident together, one per
+ * SM); if the device cannot run it so, the call returns PA_ERR_CUDA.
+ *
+ * workspace: >= pa_prefill_store_workspace_size() bytes of device memory,
+ * 8-byte aligned, zero-filled before first use; the call leaves it as it
+ * found it, so it serves any number of calls on one stream (not concurrent
+ * calls).  If the grid barrier gives up (PA_DEV_TIMEOUT, where = 440) no
+ * attention runs in that CTA; zero the workspace again before the next call.
+ */
+PA_API size_t pa_prefill_store_workspace_size(void);
+PA_API pa_status pa_prefill_store_varlen(void *out, const void *q, int64_t q_row_stride, int32_t total_q,
+                                         const void *new_k, int64_t new_k_row_stride, const void *new_v,
+                                         int64_t new_v_row_stride, void *k_cache, void *v_cache,
+                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                         int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t block_size, int32_t num_blocks, float softmax_scale,
+                                         int32_t causal, void *workspace, size_t workspace_bytes,
+                                         pa_stream_t stream);
+
+/*
  * pa_sample_gumbel -- sample one token per row by the Gumbel-max trick.
  * [NV12 §12.2 "采样器": Sampler.forward and the Gumbel-max derivation]
  *

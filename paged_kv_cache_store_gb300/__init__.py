@@ -46,6 +46,10 @@ SIGNATURES = {
                                   _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]),
     "pa_prefill_varlen": (C.c_int, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _i32, _vp, _i32, _vp, _vp, _i32,
                                     _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp]),
+    "pa_prefill_store_workspace_size": (C.c_size_t, []),
+    "pa_prefill_store_varlen": (C.c_int, [_vp, _vp, _i64, _i32, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp,
+                                          _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp,
+                                          C.c_size_t, _vp]),
     "pa_sample_gumbel": (C.c_int, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _i32, _i32, _vp]),
     "pa_set_checked": (C.c_int, [_i32]),
     # host block manager
@@ -258,10 +262,20 @@ def decode_static(q, k_cache, v_cache, block_tables, context_lens, softmax_scale
     return out
 
 
+def prefill_store_workspace(device="cuda"):
+    """Zero-filled workspace for prefill_varlen(..., new_k=, new_v=) (a grid
+    barrier's counter; the call leaves it as found, reusable on one stream)."""
+    n = int(lib().pa_prefill_store_workspace_size())
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
 def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, softmax_scale=None,
-                   block_tables=None, causal=True, out=None, stream=None):
+                   block_tables=None, causal=True, out=None, stream=None, new_k=None, new_v=None, workspace=None):
     """Varlen prefill attention.  q [total_q, Hq, D]; with block_tables, k/v are
-    the caches [num_blocks, B, Hkv, D]; without, contiguous [total_k, Hkv, D]."""
+    the caches [num_blocks, B, Hkv, D]; without, contiguous [total_k, Hkv, D].
+    With new_k / new_v ([total_q, Hkv, D], the uncached suffix in q's order;
+    block_tables required) the same launch first stores them into the caches
+    (pa_prefill_store_varlen)."""
     _need(q, torch.bfloat16, "q")
     _need(k, torch.bfloat16, "k")
     _need(v, torch.bfloat16, "v")
@@ -279,6 +293,22 @@ def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen
         softmax_scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty(tq, hq, d, dtype=torch.bfloat16, device=q.device)
+    if new_k is not None or new_v is not None:
+        if new_k is None or new_v is None or block_tables is None:
+            raise ValueError("the fused store needs new_k, new_v and block_tables")
+        _need(new_k, torch.bfloat16, "new_k")
+        _need(new_v, torch.bfloat16, "new_v")
+        if new_k.shape[0] != tq or new_v.shape[0] != tq:
+            raise ValueError("new_k / new_v need one row per query token")
+        if workspace is None:
+            workspace = prefill_store_workspace(q.device)
+        _check(lib().pa_prefill_store_varlen(
+            _ptr(out), _ptr(q), _row_stride(q, "q"), tq, _ptr(new_k), _row_stride(new_k, "new_k"), _ptr(new_v),
+            _row_stride(new_v, "new_v"), _ptr(k), _ptr(v), _ptr(block_tables), mb, _ptr(cu_seqlens_q),
+            _ptr(cu_seqlens_k), cu_seqlens_q.numel() - 1, int(max_seqlen_q), int(max_seqlen_k), hq, hkv, d, B, nb,
+            float(softmax_scale), 1 if causal else 0, _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(stream)), "pa_prefill_store_varlen")
+        return out
     _check(lib().pa_prefill_varlen(_ptr(out), _ptr(q), _row_stride(q, "q"), tq, _ptr(k), _ptr(v), kv_stride, tk,
                                    _ptr(block_tables), mb, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
                                    cu_seqlens_q.numel() - 1, int(max_seqlen_q), int(max_seqlen_k), hq, hkv,

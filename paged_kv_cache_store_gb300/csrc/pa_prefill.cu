@@ -67,7 +67,8 @@ constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
 enum {
     B_QFULL = 0, B_QEMPTY = B_QFULL + QST, B_KFULL = B_QEMPTY + QST, B_KEMPTY = B_KFULL + KST,
     B_VFULL = B_KEMPTY + KST, B_VEMPTY = B_VFULL + VST, B_SFULL = B_VEMPTY + VST, B_PFULL = B_SFULL + NSB,
-    B_PDONE = B_PFULL + NSB, B_OEMPTY = B_PDONE + NSB, B_DRAIN, B_DRAIN2,
+    B_PDONE = B_PFULL + NSB, B_OEMPTY = B_PDONE + NSB, B_DRAIN, B_DRAIN2, B_SUFFIX /* [2] fused store's loads */,
+    B_SUFFIX2,
     B_NU /* [2] next-unit slots, Q.K thread -> softmax */, NBAR = B_NU + 2
 };
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
@@ -103,7 +104,138 @@ struct PrefillArgs {
     int32_t block_size, box_rows, box_halves, paged, causal, num_blocks, checked, sorted;
     float scale_log2;
     DevError *err;
+    // Fused store (pa_prefill_store_varlen): the suffix rows to copy into
+    // the caches before any tile is loaded, and the grid barrier that
+    // separates the copies from the loads.
+    const uint4 *new_k, *new_v;
+    int64_t new_k_stride16, new_v_stride16;  // rows, in 16-byte units
+    uint4 *k_cache, *v_cache;
+    int32_t row16, total_q;
+    unsigned *gbar;  // [0] arrivals, [1] generation
 };
+
+// Every CTA of the (cooperative, hence co-resident) grid arrives; returns
+// when all have, or false after kWaitLimitNs.  The last to arrive resets the
+// count and moves the generation on, which releases the others; the counter
+// is left as it was found, so the next launch can use it.
+__device__ bool grid_barrier(unsigned *bar, unsigned n) {
+    volatile unsigned *gen = bar + 1;
+    const unsigned g = *gen;
+    __threadfence();
+    if (atomicAdd(bar, 1u) == n - 1) {
+        atomicExch(bar, 0u);
+        __threadfence();
+        atomicAdd(bar + 1, 1u);
+        return true;
+    }
+    const unsigned long long t0 = globaltimer_ns();
+    while (*gen == g) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(64);
+    }
+    __threadfence();
+    return true;
+}
+
+// Copies each suffix token's K and V rows (Hkv*D bf16) to its slot.  Row 2t
+// is token t's K, 2t+1 its V; CTA b takes a contiguous share of the rows.
+// The rows stream through the CTA's shared memory (free until the first
+// tile is loaded) with bulk copies: warp 0's lanes each load a few rows of a
+// batch (one cp.async.bulk per row, completing on one mbarrier), then store
+// them to their slots (one bulk store per row).  The slot of token t of
+// sequence s is that of position (Lk - Lq) + (t - cu_q[s]) through the block
+// table, as pa_slot_mapping_prefill gives it; a block id outside the pool is
+// recorded as PA_DEV_BAD_SLOT and the row is not written, as
+// pa_store_kvcache does.  Returns false if a batch's loads did not land in
+// time (recorded; the caller skips the rest of the kernel).
+__device__ __forceinline__ int64_t suffix_slot(const PrefillArgs &a, int t, bool is_v) {
+    int lo = 0, hi = a.num_seqs - 1;  // the sequence of token t: the last s with cu_q[s] <= t
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    const int q0 = __ldg(a.cu_q + lo), Lq = __ldg(a.cu_q + lo + 1) - q0;
+    const int Lk = __ldg(a.cu_k + lo + 1) - __ldg(a.cu_k + lo);
+    if (Lq < 0 || Lk < Lq || t >= q0 + Lq || Lk > a.max_blocks * a.block_size) return -1;  // recorded by the units
+    const int p = (Lk - Lq) + (t - q0);
+    const int blk = __ldg(a.bt + (int64_t)lo * a.max_blocks + p / a.block_size);
+    if (blk < 0 || blk >= a.num_blocks) {
+        if (!is_v) record_error(a.err, PA_DEV_BAD_SLOT, t);
+        return -1;
+    }
+    return (int64_t)blk * a.block_size + p % a.block_size;
+}
+
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem), "r"(bytes)
+                 : "memory");
+}
+
+constexpr int SUFFIX_ROWS_PER_LANE = 2;  // rows a lane moves per batch
+
+// Two halves of the staging memory alternate: while one batch's rows are
+// stored out, the next batch's loads land in the other half.
+__device__ bool store_suffix(const PrefillArgs &a, uint8_t *staging, uint32_t staging_bytes, uint64_t *bar,
+                             int lane) {
+    const uint32_t row_bytes = (uint32_t)a.row16 * 16;
+    const int batch = min((int)(staging_bytes / 2 / row_bytes), 32 * SUFFIX_ROWS_PER_LANE);
+    const uint32_t half_bytes = (uint32_t)batch * row_bytes;
+    const long long nrows = 2LL * a.total_q;
+    const long long per = (nrows + gridDim.x - 1) / gridDim.x;
+    const long long r_begin = (long long)blockIdx.x * per, r_end = min(nrows, r_begin + per);
+    const int nb = (int)((max(0LL, r_end - r_begin) + batch - 1) / batch);
+    const uint32_t st0 = smem_addr(staging);
+    int64_t slot[2][SUFFIX_ROWS_PER_LANE];
+    // Batch k: rows r_begin + k*batch + lane + 32i into half k & 1, completing on bar[k & 1].
+    auto load = [&](int k) {
+        const long long b0 = r_begin + (long long)k * batch;
+        int valid = 0;
+#pragma unroll
+        for (int i = 0; i < SUFFIX_ROWS_PER_LANE; ++i) {
+            const long long r = b0 + lane + 32 * i;
+            slot[k & 1][i] = -1;
+            if (lane + 32 * i < batch && r < r_end) slot[k & 1][i] = suffix_slot(a, (int)(r >> 1), (r & 1) != 0);
+            valid += slot[k & 1][i] >= 0;
+        }
+        const int total = __reduce_add_sync(0xffffffffu, valid);
+        if (lane == 0) mbar_arrive_expect_tx(&bar[k & 1], (uint32_t)total * row_bytes);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < SUFFIX_ROWS_PER_LANE; ++i) {
+            if (slot[k & 1][i] < 0) continue;
+            const long long r = b0 + lane + 32 * i;
+            const int t = (int)(r >> 1);
+            const uint4 *src = (r & 1) ? a.new_v + t * a.new_v_stride16 : a.new_k + t * a.new_k_stride16;
+            bulk_load(staging + (k & 1) * half_bytes + (lane + 32 * i) * row_bytes, src, row_bytes, &bar[k & 1]);
+        }
+    };
+    bool ok = true;
+    if (nb > 0) load(0);
+    for (int k = 0; k < nb; ++k) {
+        if (k + 1 < nb) {
+            bulk_wait_read0();  // batch k-1's stores have read the half batch k+1 is loaded into
+            __syncwarp();
+            load(k + 1);
+        }
+        // Every lane waits: the rows it stores were loaded by other lanes' copies too.
+        if (!mbar_wait(&bar[k & 1], (k >> 1) & 1u) && !mbar_wait(&bar[k & 1], (k >> 1) & 1u)) {
+            record_error(a.err, PA_DEV_TIMEOUT, 441);
+            ok = false;
+            break;
+        }
+        const long long b0 = r_begin + (long long)k * batch;
+#pragma unroll
+        for (int i = 0; i < SUFFIX_ROWS_PER_LANE; ++i) {
+            if (slot[k & 1][i] < 0) continue;
+            const long long r = b0 + lane + 32 * i;
+            bulk_store((((r & 1) ? a.v_cache : a.k_cache) + slot[k & 1][i] * a.row16),
+                       st0 + (k & 1) * half_bytes + (lane + 32 * i) * row_bytes, row_bytes);
+        }
+        bulk_commit_group();
+    }
+    bulk_wait0();  // the rows are in global memory and the staging memory is free
+    return __all_sync(0xffffffffu, ok);
+}
 
 // Bounded wait; the abort flag is only read once the barrier is not yet complete.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *flags, DevError *err,
@@ -243,6 +375,7 @@ __device__ __forceinline__ int cta_unit(const PrefillArgs &a, int nsorted, int k
     return next_valid_unit(a, k == 0 ? (int)blockIdx.x : prev + (int)gridDim.x, nunits, lane);
 }
 
+template <bool STORE>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
@@ -308,6 +441,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // generic-proxy accesses before them.
         fence_proxy_async_smem();
     }
+    if (STORE) {
+        // Fused store: the suffix rows go to the caches first; the grid
+        // barrier makes every CTA's copies visible before any tile is loaded
+        // (proxy fences on both sides of it).
+        if (warp == 0 && !store_suffix(a, smem + OFF_Q, OFF_BAR - OFF_Q, &bar[B_SUFFIX], lane) && lane == 0)
+            flags[0] = 1;
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncthreads();
+        if (threadIdx.x == 0 && !grid_barrier(a.gbar, gridDim.x)) {
+            record_error(a.err, PA_DEV_TIMEOUT, 440);
+            flags[0] = 1;  // every role skips its work
+        }
+        __syncthreads();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -320,7 +468,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // Every role walks the same units (cta_unit) and the
     // same global KV-tile counter g, so ring stages and barrier phases agree.
-    if (warp == W_QK || warp == W_V) {
+    if (STORE && flags[0]) {
+        // The grid barrier gave up: no role starts (nothing was issued yet).
+    } else if (warp == W_QK || warp == W_V) {
         // ------------------------------------------------------------ TMA producers
         const bool is_k = warp == W_QK;
         const CUtensorMap *tm = is_k ? &tmk : &tmv;
@@ -662,21 +812,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
-int g_attr_done[64] = {};
+int g_attr_done[64][2] = {};
 
-}  // namespace
-}  // namespace pa
+// The fused store's inputs (null: plain prefill).
+struct SuffixStore {
+    const void *new_k, *new_v;
+    int64_t new_k_row_stride, new_v_row_stride;  // elements
+    unsigned *gbar;
+};
 
-extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_stride, int32_t total_q,
-                                       const void *k, const void *v, int64_t kv_row_stride, int32_t total_k,
-                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
-                                       const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs,
-                                       int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_q_heads,
-                                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                       int32_t num_blocks, float softmax_scale, int32_t causal,
-                                       pa_stream_t stream) {
-    using namespace pa;
-    (void)max_seqlen_k;
+pa_status prefill_impl(void *out, const void *q, int64_t q_row_stride, int32_t total_q, const void *k,
+                       const void *v, int64_t kv_row_stride, int32_t total_k, const int32_t *block_tables,
+                       int32_t max_blocks_per_seq, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                       int32_t num_seqs, int32_t max_seqlen_q, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t num_blocks, float softmax_scale,
+                       int32_t causal, const SuffixStore *store, pa_stream_t stream) {
     if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
     if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PA_OK;
     if (!out || !q || !k || !v || !cu_seqlens_q || !cu_seqlens_k) return fail(PA_ERR_INVALID_ARG, "null pointer");
@@ -742,6 +892,15 @@ extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_s
     A.sorted = (int64_t)A.mtiles * num_seqs <= SCHED_MAX ? 1 : 0;
     A.scale_log2 = softmax_scale * 1.4426950408889634f;
     A.err = device_error_ptr();
+    A.new_k = store ? static_cast<const uint4 *>(store->new_k) : nullptr;
+    A.new_v = store ? static_cast<const uint4 *>(store->new_v) : nullptr;
+    A.new_k_stride16 = store ? store->new_k_row_stride / 8 : 0;
+    A.new_v_stride16 = store ? store->new_v_row_stride / 8 : 0;
+    A.k_cache = store ? static_cast<uint4 *>(const_cast<void *>(k)) : nullptr;
+    A.v_cache = store ? static_cast<uint4 *>(const_cast<void *>(v)) : nullptr;
+    A.row16 = num_kv_heads * D / 8;
+    A.total_q = total_q;
+    A.gbar = store ? store->gbar : nullptr;
 
     const int64_t ntiles = (int64_t)A.mtiles * num_seqs * num_q_heads;
     const int sms = sm_count();
@@ -749,12 +908,82 @@ extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_s
     const int64_t grid = std::min<int64_t>(ntiles, sms);  // persistent: one CTA per SM
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !g_attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_BYTES);
+    const int fi = store ? 1 : 0;
+    if (dev >= 0 && dev < 64 && !g_attr_done[dev][fi]) {
+        cudaError_t e = store ? cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     (int)SMEM_BYTES)
+                              : cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     (int)SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_kernel)");
-        g_attr_done[dev] = 1;
+        g_attr_done[dev][fi] = 1;
     }
-    prefill_kernel<<<(unsigned)grid, NTHREADS, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, A);
+    if (!store) {
+        prefill_kernel<false><<<(unsigned)grid, NTHREADS, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
+            tq, tk, tv, to, A);
+        return check_launch("prefill_kernel");
+    }
+    // The fused store's CTAs wait on one another at the grid barrier: a
+    // cooperative launch guarantees they are resident together (one per SM).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel<true>, tq, tk, tv, to, A);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill_kernel (cooperative)");
     return check_launch("prefill_kernel");
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_prefill_varlen(void *out, const void *q, int64_t q_row_stride, int32_t total_q,
+                                       const void *k, const void *v, int64_t kv_row_stride, int32_t total_k,
+                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int32_t num_seqs,
+                                       int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                       int32_t num_blocks, float softmax_scale, int32_t causal,
+                                       pa_stream_t stream) {
+    (void)max_seqlen_k;
+    return pa::prefill_impl(out, q, q_row_stride, total_q, k, v, kv_row_stride, total_k, block_tables,
+                            max_blocks_per_seq, cu_seqlens_q, cu_seqlens_k, num_seqs, max_seqlen_q, num_q_heads,
+                            num_kv_heads, head_dim, block_size, num_blocks, softmax_scale, causal, nullptr, stream);
+}
+
+extern "C" size_t pa_prefill_store_workspace_size(void) { return 256; }
+
+extern "C" pa_status pa_prefill_store_varlen(void *out, const void *q, int64_t q_row_stride, int32_t total_q,
+                                             const void *new_k, int64_t new_k_row_stride, const void *new_v,
+                                             int64_t new_v_row_stride, void *k_cache, void *v_cache,
+                                             const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                             int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                             int32_t block_size, int32_t num_blocks, float softmax_scale,
+                                             int32_t causal, void *workspace, size_t workspace_bytes,
+                                             pa_stream_t stream) {
+    using namespace pa;
+    (void)max_seqlen_k;
+    if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
+    if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PA_OK;
+    if (!block_tables) return fail(PA_ERR_INVALID_ARG, "the fused store needs block_tables (a paged pool)");
+    if (!new_k || !new_v) return fail(PA_ERR_INVALID_ARG, "null pointer");
+    if (num_kv_heads <= 0) return fail(PA_ERR_INVALID_ARG, "num_kv_heads must be positive");
+    const int64_t row = (int64_t)num_kv_heads * D;
+    if (new_k_row_stride < row || new_v_row_stride < row || new_k_row_stride % 8 || new_v_row_stride % 8)
+        return fail(PA_ERR_INVALID_ARG, "new K/V row strides must be >= num_kv_heads*head_dim and multiples of 8");
+    if (!aligned16(new_k) || !aligned16(new_v)) return fail(PA_ERR_INVALID_ARG, "new_k/new_v must be 16-byte aligned");
+    if (!workspace || workspace_bytes < pa_prefill_store_workspace_size())
+        return fail(PA_ERR_WORKSPACE, "workspace missing or smaller than pa_prefill_store_workspace_size()");
+    if (reinterpret_cast<uintptr_t>(workspace) % 8) return fail(PA_ERR_INVALID_ARG, "workspace must be 8-byte aligned");
+    SuffixStore st{new_k, new_v, new_k_row_stride, new_v_row_stride, static_cast<unsigned *>(workspace)};
+    return prefill_impl(out, q, q_row_stride, total_q, k_cache, v_cache, 0, 0, block_tables, max_blocks_per_seq,
+                        cu_seqlens_q, cu_seqlens_k, num_seqs, max_seqlen_q, num_q_heads, num_kv_heads, head_dim,
+                        block_size, num_blocks, softmax_scale, causal, &st, stream);
 }

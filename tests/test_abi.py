@@ -182,3 +182,33 @@ def test_decode_store_argument_checks(L):
     assert call(nvs=1028) == pa.PA_ERR_INVALID_ARG                # not a multiple of 8
     assert call(hq=24) == pa.PA_ERR_UNSUPPORTED                   # decode's own checks still apply
     assert call(ws=None, wsb=0) == pa.PA_ERR_WORKSPACE
+
+
+def _prefill_store(L, **kw):
+    p = C.c_void_p(256)
+    a = dict(out=p, q=p, qs=32 * 128, tq=100, nk=p, nks=8 * 128, nv=p, nvs=8 * 128, kc=p, vc=p, bt=p, mb=8,
+             cq=p, ck=p, ns=2, mq=64, mk=512, hq=32, hkv=8, d=128, B=256, nb=16, scale=0.088, causal=1,
+             ws=p, wsb=256, stream=None)
+    a.update(kw)
+    return L.pa_prefill_store_varlen(a["out"], a["q"], a["qs"], a["tq"], a["nk"], a["nks"], a["nv"], a["nvs"],
+                                     a["kc"], a["vc"], a["bt"], a["mb"], a["cq"], a["ck"], a["ns"], a["mq"],
+                                     a["mk"], a["hq"], a["hkv"], a["d"], a["B"], a["nb"], a["scale"],
+                                     a["causal"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_prefill_store_argument_checks(L):
+    """Every case fails (or has nothing to do) before any launch."""
+    assert L.pa_prefill_store_workspace_size() >= 8
+    assert _prefill_store(L, ns=0) == pa.PA_OK
+    assert _prefill_store(L, tq=0) == pa.PA_OK
+    assert _prefill_store(L, bt=None) == pa.PA_ERR_INVALID_ARG     # the fused store needs a paged pool
+    assert _prefill_store(L, nk=None) == pa.PA_ERR_INVALID_ARG
+    assert _prefill_store(L, nvs=8 * 128 - 8) == pa.PA_ERR_INVALID_ARG  # shorter than a row
+    assert _prefill_store(L, nks=8 * 128 + 4) == pa.PA_ERR_INVALID_ARG  # not a multiple of 8
+    assert _prefill_store(L, nv=C.c_void_p(264)) == pa.PA_ERR_INVALID_ARG  # unaligned
+    assert _prefill_store(L, ws=None) == pa.PA_ERR_WORKSPACE
+    assert _prefill_store(L, wsb=4) == pa.PA_ERR_WORKSPACE
+    assert _prefill_store(L, ws=C.c_void_p(260)) == pa.PA_ERR_INVALID_ARG  # workspace not 8-byte aligned
+    assert _prefill_store(L, hq=12) == pa.PA_ERR_INVALID_ARG   # the prefill's own checks follow
+    assert _prefill_store(L, d=64) == pa.PA_ERR_UNSUPPORTED
+    assert _prefill_store(L, B=24) == pa.PA_ERR_UNSUPPORTED

@@ -191,3 +191,62 @@ def test_prefill_schedules_agree():
     assert torch.equal(sorted_out, plain_out)
     want, _, _ = oracle_prefill(p)
     assert_close(host_f64(sorted_out), want)
+
+
+def fused_vs_unfused(p, ws=None):
+    """The fused store + prefill against slot mapping + store + prefill on
+    copies of the same pool: identical outputs and identical caches."""
+    bt, cq, ck = dev_i32(p.block_tables), dev_i32(p.cu_seqlens_q), dev_i32(p.cu_seqlens_k)
+    q, nk, nv = dev_bf16(p.q), dev_bf16(p.new_k), dev_bf16(p.new_v)
+    mq, mk = int(p.seqlens_q.max()), int(p.seqlens_k.max())
+    kc1, vc1 = dev_bf16(p.k_cache), dev_bf16(p.v_cache)
+    slots = pa.slot_mapping_prefill(bt, cq, ck, p.block_size, total_q=p.total_q)
+    pa.store_kvcache(nk, nv, kc1, vc1, slots)
+    ref = pa.prefill_varlen(q, kc1, vc1, cq, ck, mq, mk, p.scale, block_tables=bt)
+    kc2, vc2 = dev_bf16(p.k_cache), dev_bf16(p.v_cache)
+    got = pa.prefill_varlen(q, kc2, vc2, cq, ck, mq, mk, p.scale, block_tables=bt, new_k=nk, new_v=nv, workspace=ws)
+    assert pa.get_device_error() == (0, 0)
+    assert torch.equal(got, ref)
+    assert torch.equal(kc2, kc1) and torch.equal(vc2, vc1)
+    return got
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_prefill_fused_store_equals_store_then_prefill(case):
+    lk, c = CASES[case]
+    p = make_prefill(case, 41, lk, None, 16, 8, cached_tokens=c)
+    got = fused_vs_unfused(p)
+    want, _, _ = oracle_prefill(p)
+    assert_close(host_f64(got), want)
+
+
+def test_prefill_fused_store_workspace_reused():
+    """One workspace serves consecutive calls: the grid barrier leaves its
+    counter at zero and only moves its generation on."""
+    ws = pa.prefill_store_workspace()
+    for seed, lk, c in ((5, [300, 40, 700], [0, 0, 256]), (6, [129, 1025], [17, 512]), (7, [64], [0])):
+        p = make_prefill("ws", seed, lk, None, 8, 2, cached_tokens=c)
+        fused_vs_unfused(p, ws)
+    words = ws.view(torch.int32).cpu().tolist()
+    assert words[0] == 0 and words[1] > 0
+
+
+def test_prefill_fused_store_bad_block_recorded_not_written():
+    p = make_prefill("bad", 9, [300, 200], None, 16, 8, cached_tokens=[0, 0])
+    bt = p.block_tables.copy()
+    bt[1, 0] = p.k_cache.shape[0] + 3  # sequence 1's first block id is outside the pool
+    kc, vc = dev_bf16(p.k_cache), dev_bf16(p.v_cache)
+    pa.get_device_error()
+    pa.prefill_varlen(dev_bf16(p.q), kc, vc, dev_i32(p.cu_seqlens_q), dev_i32(p.cu_seqlens_k), 300, 300, p.scale,
+                      block_tables=dev_i32(bt), new_k=dev_bf16(p.new_k), new_v=dev_bf16(p.new_v))
+    code, where = pa.get_device_error()
+    assert code == pa.PA_DEV_BAD_SLOT and 300 <= where < 300 + p.block_size  # a token of sequence 1
+    # Sequence 0's rows are stored; sequence 1's are not; nothing else changed.
+    for cache, new, orig in ((kc, p.new_k, p.k_cache), (vc, p.new_v, p.v_cache)):
+        want = orig.copy().reshape(-1, 8 * 128)
+        want[O.slot_mapping(p.block_tables[0], p.block_size, 0, 300)] = new[:300].reshape(300, -1)
+        assert np.array_equal(host_bits(cache).reshape(-1, 8 * 128), want)
+
+
+def test_prefill_fused_store_workload_full_size():
+    fused_vs_unfused(prefill_config(5))
