@@ -35,6 +35,10 @@
 //  * On the last KV tile the P.V thread zeroes the V rows between the last
 //    needed key and the next multiple of 16 (stale or unloaded data; P is 0
 //    there but 0 * NaN is not) and skips the 16-key steps past it.
+//  * Fused store (prefill_kernel<true>, pa_prefill_store_varlen): before any
+//    tile is loaded, the CTAs of a cooperative launch copy the uncached
+//    suffix rows into their cache slots (bulk copies through the unused ring
+//    memory) and meet at a grid barrier; then everything runs as above.
 //  * Every mbarrier wait is bounded; a timeout records PA_DEV_TIMEOUT and
 //    the roles skip to the CTA-wide teardown.
 // TMEM: S/P buffers at columns 0, 128 and 256, O = 384..511.
