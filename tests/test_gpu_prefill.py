@@ -250,3 +250,23 @@ def test_prefill_fused_store_bad_block_recorded_not_written():
 
 def test_prefill_fused_store_workload_full_size():
     fused_vs_unfused(prefill_config(5))
+
+
+def test_prefill_fused_store_barrier_timeout_is_recorded():
+    """Failure detection without a fault: with the workspace's arrival count
+    seeded far from the grid size no CTA is ever the last to arrive, so every
+    CTA's bounded wait at the grid barrier runs out (after ~1 s), records
+    PA_DEV_TIMEOUT at site 440 and skips its units.  The context stays
+    usable: after zeroing the workspace the same call gives the right
+    answer."""
+    p = make_prefill("timeout", 12, [300, 129], None, 8, 2, cached_tokens=[0, 17])
+    ws = pa.prefill_store_workspace()
+    ws.view(torch.int32)[0] = 1 << 30
+    kc, vc = dev_bf16(p.k_cache), dev_bf16(p.v_cache)
+    bt, cq, ck = dev_i32(p.block_tables), dev_i32(p.cu_seqlens_q), dev_i32(p.cu_seqlens_k)
+    q, nk, nv = dev_bf16(p.q), dev_bf16(p.new_k), dev_bf16(p.new_v)
+    pa.get_device_error()
+    pa.prefill_varlen(q, kc, vc, cq, ck, 300, 300, p.scale, block_tables=bt, new_k=nk, new_v=nv, workspace=ws)
+    assert pa.get_device_error() == (pa.PA_DEV_TIMEOUT, 440)
+    ws.zero_()
+    fused_vs_unfused(p, ws)
