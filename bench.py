@@ -522,6 +522,111 @@ def run_ours(args):
     return 0
 
 
+def run_report(args):
+    """The per-configuration results table (markdown on stdout): decode
+    configurations 1-4 run the fused store + decode step, configuration 5 the
+    varlen prefill (and its fused store + prefill step).  Device time: median
+    of `steps` calls, CUDA events, L2 flushed before each.  Parity: against
+    the oracle on the same inputs (all outputs for decode; 2048 sampled
+    (token, head) rows for prefill).  Oracle time: one single-threaded oracle
+    step (for prefill, the sampled rows, extrapolated by their share of the
+    visible (query, key) pairs)."""
+    import torch
+    import oracle as O
+    import paged_kv_cache_store_gb300 as pa
+    from paged_kv_cache_store_gb300.workloads import decode_config, prefill_config, bf16_bits_to_f32
+    O.lib()
+    dev = torch.device("cuda", 0)
+    hbm, bf16_peak, kind = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def to(a, bf=False):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf else np.ascontiguousarray(a))
+        return (t.view(torch.bfloat16) if bf else t).to(dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a_, b_ in ev:
+            flush.zero_()
+            a_.record()
+            fn()
+            b_.record()
+        torch.cuda.synchronize()
+        code, where = pa.get_device_error()
+        if code:
+            raise RuntimeError(f"device error {code} at {where}")
+        return float(np.median([a_.elapsed_time(b_) for a_, b_ in ev]))
+
+    def host(t):
+        return bf16_bits_to_f32(t.cpu().view(torch.int16).numpy().view(np.uint16)).astype(np.float64)
+
+    traffic = recorded_traffic("decode_kernel<2, store>", "qwen3-0.6b")
+    lines = ["| Config | GPU time | tokens/s (decode, 1 layer) | GB/s (algorithmic) | TFLOP/s | % roofline "
+             "| ncu DRAM GB/s | Oracle 1-thread | Parity (max / mean abs) |", "|" + "---|" * 9]
+    for cfg in (1, 2, 3, 4):
+        inp = decode_config(cfg)
+        kc, vc, q = to(inp.k_cache, True), to(inp.v_cache, True), to(inp.q, True)
+        nk, nv = to(inp.new_k, True), to(inp.new_v, True)
+        bt, ctx = to(inp.block_tables), to(inp.context_lens)
+        out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
+        wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev)
+        ms = timed(lambda: pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out, new_k=nk, new_v=nv))
+        t0 = time.perf_counter()
+        okc, ovc = inp.k_cache.copy(), inp.v_cache.copy()
+        slots = np.array([O.decode_slot(inp.block_tables[b], inp.block_size, int(inp.context_lens[b]))
+                          for b in range(inp.batch)], np.int32)
+        O.store_kvcache(inp.new_k, inp.new_v, okc, ovc, slots)
+        want = O.decode(inp.q, okc, ovc, inp.block_tables, inp.context_lens, inp.scale)
+        oracle_s = time.perf_counter() - t0
+        err = np.abs(host(out) - want)
+        row = inp.num_kv_heads * inp.head_dim * 2
+        alg = int(inp.context_lens.astype(np.int64).sum()) * row * 2 + 2 * inp.batch * inp.num_q_heads * \
+            inp.head_dim * 2 + 2 * inp.batch * row * 2
+        gbs = alg / (ms / 1000.0) / 1e9
+        note = " (logical; shared blocks counted per sequence)" if cfg == 3 else ""
+        ncu = f"{traffic / (ms / 1000.0) / 1e9:.0f} ({traffic / 1e6:.1f} MB)" if cfg == 2 and traffic else "—"
+        lines.append(f"| {cfg} {inp.name} | {ms * 1000:.1f} us | {inp.batch / (ms / 1000.0):,.0f} | "
+                     f"{gbs:,.0f}{note} | — | {100 * gbs / hbm:.1f} % of {hbm:.0f} ({kind}) | {ncu} | "
+                     f"{oracle_s:.2f} s ({inp.batch / oracle_s:,.0f} tokens/s) | {err.max():.2e} / {err.mean():.2e} |")
+        del kc, vc
+        torch.cuda.empty_cache()
+    p = prefill_config(5)
+    kc, vc, q = to(p.k_cache, True), to(p.v_cache, True), to(p.q, True)
+    nk, nv = to(p.new_k, True), to(p.new_v, True)
+    bt, cq, ck = to(p.block_tables), to(p.cu_seqlens_q), to(p.cu_seqlens_k)
+    out = torch.empty(p.total_q, p.num_q_heads, p.head_dim, dtype=torch.bfloat16, device=dev)
+    mq, mk = int(p.seqlens_q.max()), int(p.seqlens_k.max())
+    slots = pa.slot_mapping_prefill(bt, cq, ck, p.block_size, total_q=p.total_q)
+    pa.store_kvcache(nk, nv, kc, vc, slots)
+    ms = timed(lambda: pa.prefill_varlen(q, kc, vc, cq, ck, mq, mk, p.scale, block_tables=bt, out=out))
+    wsf = pa.prefill_store_workspace(dev)
+    ms_fused = timed(lambda: pa.prefill_varlen(q, kc, vc, cq, ck, mq, mk, p.scale, block_tables=bt, out=out,
+                                               new_k=nk, new_v=nv, workspace=wsf))
+    pairs = prefill_pairs(p)
+    flops = 4 * p.head_dim * p.num_q_heads * pairs
+    okc, ovc = p.k_cache.copy(), p.v_cache.copy()
+    oslots = np.concatenate([O.slot_mapping(p.block_tables[s], p.block_size, int(p.seqlens_k[s] - p.seqlens_q[s]),
+                                            int(p.seqlens_k[s])) for s in range(p.num_seqs)])
+    O.store_kvcache(p.new_k, p.new_v, okc, ovc, oslots)
+    rows = np.sort(np.random.default_rng(5).choice(p.total_q * p.num_q_heads, 2048, replace=False))
+    t0 = time.perf_counter()
+    want = O.prefill(p.q, okc, ovc, p.cu_seqlens_q, p.cu_seqlens_k, p.scale, block_tables=p.block_tables,
+                     rows=rows)
+    oracle_s = time.perf_counter() - t0
+    seq_of = np.searchsorted(p.cu_seqlens_q, rows // p.num_q_heads, side="right") - 1
+    keys = (p.seqlens_k - p.seqlens_q)[seq_of] + (rows // p.num_q_heads - p.cu_seqlens_q[seq_of]) + 1
+    oracle_full = oracle_s * (pairs * p.num_q_heads) / float(keys.sum())
+    err = np.abs(host(out).reshape(-1, p.head_dim)[rows] - want)
+    tf = flops / (ms / 1000.0) / 1e12
+    lines.append(f"| 5 {p.name} | {ms * 1000:.1f} us (fused store + prefill: {ms_fused * 1000:.1f} us) | — | — | "
+                 f"{tf:.0f} | {100 * tf / bf16_peak:.1f} % of {bf16_peak:.0f} ({kind}) | — | "
+                 f"~{oracle_full:.0f} s (2048 rows in {oracle_s:.1f} s) | {err.max():.2e} / {err.mean():.2e} |")
+    print("\n".join(lines))
+    return 0
+
+
 def run_profile_case(args):
     """A reduced decode workload for captures that replay each launch many
     times (ncu --set full): the Qwen3-0.6B shape (batch 64, 16 q / 8 kv
@@ -566,6 +671,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--report", action="store_true",
+                    help="print the per-configuration results table (markdown) instead of the JSON line")
     ap.add_argument("--profile-case", choices=["decode-small"], default=None,
                     help="run only a reduced case for a multi-pass ncu capture (no JSON line)")
     args = ap.parse_args()
@@ -575,6 +682,8 @@ def main():
         return run_reference(args)
     if args.profile_case:
         return run_profile_case(args)
+    if args.report:
+        return run_report(args)
     return run_ours(args)
 
 
