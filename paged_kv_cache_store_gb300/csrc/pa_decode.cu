@@ -69,6 +69,7 @@ constexpr int kMaxGrid = 256;     // CTAs of the persistent grid (min(SMs, this)
 constexpr int kMaxRanges = 2 * kMaxGrid;  // a head and a tail range per CTA
 constexpr int kTailShift = 3;  // a CTA's tail range is 1/8 of its share
 constexpr int NTK = 4;            // tickets in flight (ranges handed from the K warp to the others)
+constexpr int kMinTilesPerCta = 8;  // grid = min(SMs, tile bound / this)
 constexpr unsigned FULL = 0xffffffffu;
 
 template <int G>
@@ -1012,12 +1013,19 @@ pa_status decode_impl(void *out, const void *q, int64_t q_row_stride, void *k_ca
 
     const int sms = std::min(sm_count(), kMaxGrid);
     if (sms <= 0) return fail(PA_ERR_CUDA, "no CUDA device");
+    // Small batches get fewer CTAs, so that a range still holds several tiles
+    // (every range boundary inside a (sequence, kv head) pair costs a partial
+    // and a merge).  The bound on the tiles comes from the table width, the
+    // only size known on the host.
+    const int64_t tiles_bound =
+        (int64_t)batch * num_kv_heads * (((int64_t)max_blocks_per_seq * block_size + TILE - 1) / TILE);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, (tiles_bound + kMinTilesPerCta - 1) / kMinTilesPerCta));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (G) {
-        case 1: return launch_g<1>(A, tk, tv, sms, s);
-        case 2: return launch_g<2>(A, tk, tv, sms, s);
-        case 4: return launch_g<4>(A, tk, tv, sms, s);
-        default: return launch_g<8>(A, tk, tv, sms, s);
+        case 1: return launch_g<1>(A, tk, tv, grid, s);
+        case 2: return launch_g<2>(A, tk, tv, grid, s);
+        case 4: return launch_g<4>(A, tk, tv, grid, s);
+        default: return launch_g<8>(A, tk, tv, grid, s);
     }
 }
 

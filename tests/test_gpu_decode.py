@@ -105,12 +105,26 @@ def test_decode_pairs_cut_across_many_ctas():
 
 def test_decode_fewer_tiles_than_ctas():
     """Fewer tiles than CTAs: most CTAs get no work, the rest one tile, and a
-    pair of several tiles is merged from one-tile partials."""
+    pair of several tiles is merged from one-tile partials.  (The grid is
+    sized from the table width, so the tables get padding columns to keep it
+    at one CTA per SM.)"""
     for hq, hkv, ctx in [(8, 8, [1]), (16, 8, [130, 5]), (8, 1, [64 * 40 + 3])]:
-        inp = make_decode(f"few {hq}/{hkv}", 14, len(ctx), hq, hkv, ctx)
+        inp = make_decode(f"few {hq}/{hkv}", 14, len(ctx), hq, hkv, ctx, extra_table_cols=320)
         out, _, _ = run_gpu_step(inp)
         want, _, _ = run_oracle_step(inp)
         assert_close(host_f64(out), want, f"few tiles {hq}/{hkv} {ctx}")
+
+
+def test_decode_small_grid_from_narrow_tables():
+    """Narrow tables bound the work, so the grid shrinks (here to a few CTAs,
+    each with several tiles): same results, fused store included."""
+    for hq, hkv, ctx in [(16, 8, [600, 1, 257, 90]), (32, 8, [5, 64]), (8, 2, [1000])]:
+        inp = make_decode(f"narrow {hq}/{hkv}", 15, len(ctx), hq, hkv, ctx)
+        out, _, _ = run_gpu_step(inp)
+        want, _, _ = run_oracle_step(inp)
+        assert_close(host_f64(out), want, f"narrow {hq}/{hkv} {ctx}")
+        fout, fkc, fvc = run_gpu_fused(inp)
+        assert torch.equal(fout, out)
 
 
 def test_decode_repeated_calls_reuse_workspace():
