@@ -193,7 +193,7 @@ def test_prefill_schedules_agree():
     assert_close(host_f64(sorted_out), want)
 
 
-def fused_vs_unfused(p, ws=None):
+def fused_vs_unfused(p, ws=None, causal=True):
     """The fused store + prefill against slot mapping + store + prefill on
     copies of the same pool: identical outputs and identical caches."""
     bt, cq, ck = dev_i32(p.block_tables), dev_i32(p.cu_seqlens_q), dev_i32(p.cu_seqlens_k)
@@ -202,9 +202,10 @@ def fused_vs_unfused(p, ws=None):
     kc1, vc1 = dev_bf16(p.k_cache), dev_bf16(p.v_cache)
     slots = pa.slot_mapping_prefill(bt, cq, ck, p.block_size, total_q=p.total_q)
     pa.store_kvcache(nk, nv, kc1, vc1, slots)
-    ref = pa.prefill_varlen(q, kc1, vc1, cq, ck, mq, mk, p.scale, block_tables=bt)
+    ref = pa.prefill_varlen(q, kc1, vc1, cq, ck, mq, mk, p.scale, block_tables=bt, causal=causal)
     kc2, vc2 = dev_bf16(p.k_cache), dev_bf16(p.v_cache)
-    got = pa.prefill_varlen(q, kc2, vc2, cq, ck, mq, mk, p.scale, block_tables=bt, new_k=nk, new_v=nv, workspace=ws)
+    got = pa.prefill_varlen(q, kc2, vc2, cq, ck, mq, mk, p.scale, block_tables=bt, new_k=nk, new_v=nv, workspace=ws,
+                            causal=causal)
     assert pa.get_device_error() == (0, 0)
     assert torch.equal(got, ref)
     assert torch.equal(kc2, kc1) and torch.equal(vc2, vc1)
@@ -218,6 +219,22 @@ def test_prefill_fused_store_equals_store_then_prefill(case):
     got = fused_vs_unfused(p)
     want, _, _ = oracle_prefill(p)
     assert_close(host_f64(got), want)
+
+
+@pytest.mark.parametrize("B", [16, 48, 512])
+def test_prefill_fused_store_block_sizes(B):
+    """Blocks smaller than a 128-key tile (several boxes per tile) and larger."""
+    p = make_prefill("fbs", 700 + B, [3 * B + 5, B, 260], None, 16, 8, block_size=B, cached_tokens=[B + 1, 0, 17])
+    got = fused_vs_unfused(p)
+    want, _, _ = oracle_prefill(p)
+    assert_close(host_f64(got), want, f"fused, block_size {B}")
+
+
+def test_prefill_fused_store_non_causal():
+    p = make_prefill("fnc", 601, [200, 129, 64], None, 16, 8, cached_tokens=[50, 0, 0])
+    got = fused_vs_unfused(p, causal=False)
+    want, _, _ = oracle_prefill(p, causal=False)
+    assert_close(host_f64(got), want, "fused, non-causal")
 
 
 def test_prefill_fused_store_workspace_reused():
