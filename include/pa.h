@@ -232,15 +232,20 @@ PA_API pa_status pa_decode_store(void *out, const void *q, int64_t q_row_stride,
  * another framework's memory pool, plugins that must not touch the
  * allocator, or hosts that forbid device allocation after start-up.  This
  * entry point allocates nothing.  The split partials go to an 8 MiB scratch
- * array compiled into the library (zero-filled at load, as the workspace
- * contract asks), which holds the workspace of every supported shape; every
+ * array compiled into the library, which holds the workspace of every
+ * supported shape (a shape needing more returns PA_ERR_UNSUPPORTED); every
  * GPU that loads the library holds those 8 MiB until the process exits.
  *   - The first call on a device (with that device current) looks up the
  *     array's device address; make that first call before any stream capture.
+ *   - The partials need no initial value, but the work counters at the
+ *     front of the array must be zero when the kernel starts.  Every call
+ *     therefore clears them first (a cudaMemsetAsync of a few KiB on
+ *     `stream`, which allocates nothing), so a call that stopped on a device
+ *     error (PA_DEV_TIMEOUT) leaves nothing behind that a later call could
+ *     trip on.
  *   - All calls share the one array and it keeps the last call's contents.
- *     Nothing in it has to start at zero: every partial is written before it
- *     is read within the same call.  Calls that may overlap on the GPU (other
- *     streams, other threads) race on it and must be serialised by the caller.
+ *     Calls that may overlap on the GPU (other streams, other threads) race
+ *     on it and must be serialised by the caller.
  */
 PA_API pa_status pa_decode_static(void *out, const void *q, int64_t q_row_stride, const void *k_cache,
                                   const void *v_cache, const int32_t *block_tables,
@@ -248,6 +253,14 @@ PA_API pa_status pa_decode_static(void *out, const void *q, int64_t q_row_stride
                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t block_size, int32_t num_blocks, float softmax_scale,
                                   pa_stream_t stream);
+
+/*
+ * pa_decode_static_scratch -- device address (on the current device) and size
+ * in bytes of the scratch array pa_decode_static uses, for inspection and
+ * tests.  Performs the same once-per-device look-up as pa_decode_static's
+ * first call; allocates nothing.
+ */
+PA_API pa_status pa_decode_static_scratch(void **device_ptr, size_t *bytes);
 
 /*
  * pa_prefill_varlen -- varlen causal attention for prompt (prefill) tokens.

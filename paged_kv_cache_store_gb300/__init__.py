@@ -42,6 +42,7 @@ SIGNATURES = {
                             _i32, _f32, _vp, _sz, _vp]),
     "pa_decode_static": (C.c_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                    _i32, _f32, _vp]),
+    "pa_decode_static_scratch": (C.c_int, [C.POINTER(_vp), C.POINTER(_sz)]),
     "pa_decode_store": (C.c_int, [_vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
                                   _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]),
     "pa_prefill_varlen": (C.c_int, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _i32, _vp, _i32, _vp, _vp, _i32,

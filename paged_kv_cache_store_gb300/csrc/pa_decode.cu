@@ -51,6 +51,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "pa_internal.cuh"
@@ -871,7 +872,10 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     }
 }
 
-int g_attr_done[64][8] = {};
+// Per (device, instantiation): the shared-memory attribute has been set.
+// Two threads making their first call together may both set it (the call is
+// idempotent); the flag itself is an atomic, so there is no data race.
+std::atomic<int> g_attr_done[64][8];
 
 template <int G, bool STORE>
 pa_status launch(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
@@ -879,11 +883,11 @@ pa_status launch(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &
     int dev = 0;
     cudaGetDevice(&dev);
     const int gi = (G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3) + (STORE ? 4 : 0);
-    if (dev >= 0 && dev < 64 && !g_attr_done[dev][gi]) {
+    if (dev >= 0 && dev < 64 && !g_attr_done[dev][gi].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(decode_kernel<G, STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)Cfg<G>::smem_bytes(kMaxBatch));
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_kernel)");
-        g_attr_done[dev][gi] = 1;
+        g_attr_done[dev][gi].store(1, std::memory_order_release);
     }
     // Programmatic dependent launch: the grid may start while the previous
     // kernel on the stream finishes; it reads nothing before griddepcontrol.wait.
@@ -1073,15 +1077,37 @@ pa_status pa_decode_store(void *out, const void *q, int64_t q_row_stride, const 
 // ---------------------------------------------------------------------------
 
 // Split-partial scratch, enough for every shape (the workspace size depends
-// only on the GQA group).  It is loaded with the module, zero-filled as the
-// workspace contract asks, so every GPU that loads this library holds it
-// until the process exits.
+// only on the GQA group).  It is part of the module's device image, so every
+// GPU that loads this library holds it until the process exits.  Its leading
+// bytes are the work counters the kernel needs at zero when it starts; every
+// call clears them first (see pa_decode_static), so no state carries over
+// from an earlier call, not even one that stopped on a device error.
 static constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char pa_static_scratch[kStaticScratchBytes];
 
 namespace {
 std::mutex g_static_mu;
 void *g_static_scratch_addr[64] = {};  // device address of the array, per device
+
+// Device address of the array on the current device (looked up once per
+// device, with that device current: the host-side name of a __device__
+// variable is not a device address).
+pa_status static_scratch(void **out) {
+    using namespace pa;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (g_static_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, pa_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(pa_static_scratch)");
+        g_static_scratch_addr[dev] = p;
+    }
+    *out = g_static_scratch_addr[dev];
+    return PA_OK;
+}
 }  // namespace
 
 extern "C" pa_status pa_decode_static(void *out, const void *q, int64_t q_row_stride, const void *k_cache,
@@ -1098,24 +1124,30 @@ extern "C" pa_status pa_decode_static(void *out, const void *q, int64_t q_row_st
         return pa_decode(out, q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq,
                          context_lens, batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                          softmax_scale, nullptr, 0, stream);
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= 64) return fail(PA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    if (need > kStaticScratchBytes)
+        return fail(PA_ERR_UNSUPPORTED, "decode scratch of %zu bytes exceeds the static %zu", need,
+                    kStaticScratchBytes);
     void *scratch = nullptr;
-    {
-        // Set-up, once per device, with that device current: the host-side name
-        // of the array is not a device address, so ask the runtime for it.
-        std::lock_guard<std::mutex> lk(g_static_mu);
-        if (g_static_scratch_addr[dev] == nullptr) {
-            void *p = nullptr;
-            e = cudaGetSymbolAddress(&p, pa_static_scratch);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(pa_static_scratch)");
-            g_static_scratch_addr[dev] = p;
-        }
-        scratch = g_static_scratch_addr[dev];
-    }
+    pa_status st = static_scratch(&scratch);
+    if (st != PA_OK) return st;
+    // The tail counter and the per-range arrival counters must be zero when
+    // the kernel starts.  A completed call leaves them zero, but a call that
+    // stopped on a device error (a wait that ran out) may not, and the caller
+    // cannot reach this array to clear it: so clear them here, on the same
+    // stream, before every launch (a few KiB; memset allocates nothing).
+    const size_t counters = ws_layout(num_q_heads / num_kv_heads).ml_off;
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, counters, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static decode counters)");
     return pa_decode(out, q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                      batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, softmax_scale, scratch,
                      kStaticScratchBytes, stream);
+}
+
+extern "C" pa_status pa_decode_static_scratch(void **device_ptr, size_t *bytes) {
+    using namespace pa;
+    if (!device_ptr || !bytes) return fail(PA_ERR_INVALID_ARG, "null pointer");
+    pa_status st = static_scratch(device_ptr);
+    if (st != PA_OK) return st;
+    *bytes = kStaticScratchBytes;
+    return PA_OK;
 }

@@ -45,6 +45,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "pa_tcgen05.cuh"
 
@@ -816,7 +817,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
-int g_attr_done[64][2] = {};
+// Per (device, instantiation): the shared-memory attribute has been set
+// (an atomic flag; concurrent first calls may both set the idempotent attribute).
+std::atomic<int> g_attr_done[64][2];
 
 // The fused store's inputs (null: plain prefill).
 struct SuffixStore {
@@ -913,13 +916,13 @@ pa_status prefill_impl(void *out, const void *q, int64_t q_row_stride, int32_t t
     int dev = 0;
     cudaGetDevice(&dev);
     const int fi = store ? 1 : 0;
-    if (dev >= 0 && dev < 64 && !g_attr_done[dev][fi]) {
+    if (dev >= 0 && dev < 64 && !g_attr_done[dev][fi].load(std::memory_order_acquire)) {
         cudaError_t e = store ? cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                      (int)SMEM_BYTES)
                               : cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                      (int)SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_kernel)");
-        g_attr_done[dev][fi] = 1;
+        g_attr_done[dev][fi].store(1, std::memory_order_release);
     }
     if (!store) {
         prefill_kernel<false><<<(unsigned)grid, NTHREADS, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(

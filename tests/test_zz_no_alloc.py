@@ -4,9 +4,13 @@ the allocator, a host that forbids allocation after start-up).  Its split
 scratch is an array built into the library instead of a caller workspace.
 
 The entry point is called through the C ABI twice in a row per shape and
-compared with pa_decode (caller workspace) at the attention tolerance.  This
-file is collected last so a failure here comes after every other test has
-run; it also passes when run alone in a fresh process."""
+compared with pa_decode (caller workspace) at the attention tolerance; the
+device's free memory and torch's allocator are unchanged across the calls;
+and a call after the array's work counters were left non-zero (as a call
+that stopped on a device error can leave them) is still correct, because
+every call clears them first.  This file is collected last so a failure here
+comes after every other test has run; it also passes when run alone in a
+fresh process."""
 import ctypes as C
 
 import numpy as np
@@ -65,4 +69,67 @@ def test_static_scratch_holds_the_largest_shapes():
     assert _static_call(q, kc, vc, bt, ctx, inp.scale, out) == pa.PA_OK
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+    assert pa.get_device_error() == (0, 0)
+
+
+def _scratch():
+    ptr, nbytes = C.c_void_p(), C.c_size_t()
+    assert pa.lib().pa_decode_static_scratch(C.byref(ptr), C.byref(nbytes)) == pa.PA_OK
+    return ptr.value, nbytes.value
+
+
+class _DevBytes:
+    """A view of device bytes for torch.as_tensor (no copy, no allocation)."""
+
+    def __init__(self, ptr, n):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "|u1", "data": (ptr, False),
+                                        "strides": None, "version": 3}
+
+
+def test_static_allocates_nothing():
+    """Free device memory (cudaMemGetInfo) and torch's allocation counters do
+    not move across two calls made after the outputs exist (one call before
+    the measured window does the once-per-device set-up)."""
+    inp = decode_config(2)
+    q, kc, vc = dev_bf16(inp.q), dev_bf16(inp.k_cache), dev_bf16(inp.v_cache)
+    bt, ctx = dev_i32(inp.block_tables), dev_i32(inp.context_lens)
+    ref = pa.decode(q, kc, vc, bt, ctx, inp.scale)
+    outs = [torch.empty_like(ref) for _ in range(2)]
+    assert _static_call(q, kc, vc, bt, ctx, inp.scale, outs[0]) == pa.PA_OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    n_alloc0 = torch.cuda.memory_stats().get("allocation.all.allocated", 0)
+    for out in outs:
+        assert _static_call(q, kc, vc, bt, ctx, inp.scale, out) == pa.PA_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+    assert torch.cuda.memory_stats().get("allocation.all.allocated", 0) == n_alloc0
+    for out in outs:
+        assert torch.equal(out, ref)
+    assert pa.get_device_error() == (0, 0)
+
+
+def test_static_call_after_counters_left_dirty():
+    """The array's leading work counters (tail counter, done counter, one
+    arrival counter per range) are set non-zero, as a call that stopped on a
+    device error can leave them; the next two calls still equal pa_decode
+    (the counters would otherwise skip tail ranges and merge split pairs
+    early, leaving wrong or unwritten rows)."""
+    inp = make_decode("static-dirty", 33, 5, 32, 8, [7000, 3000, 257, 9000, 1200])   # many split pairs
+    q, kc, vc = dev_bf16(inp.q), dev_bf16(inp.k_cache), dev_bf16(inp.v_cache)
+    bt, ctx = dev_i32(inp.block_tables), dev_i32(inp.context_lens)
+    ref = pa.decode(q, kc, vc, bt, ctx, inp.scale)
+    ptr, nbytes = _scratch()
+    assert ptr and nbytes == 8 << 20
+    counters = torch.as_tensor(_DevBytes(ptr, 4096), device="cuda").view(torch.int32)
+    for call in range(2):
+        counters.fill_(3)   # every counter non-zero
+        torch.cuda.synchronize()
+        out = torch.full_like(ref, float("nan"))
+        assert _static_call(q, kc, vc, bt, ctx, inp.scale, out) == pa.PA_OK
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"call {call}"
+        # A completed call leaves its counters at zero.
+        assert int(counters[:64 + 512].abs().sum()) == 0
     assert pa.get_device_error() == (0, 0)
