@@ -1,25 +1,31 @@
 """Benchmark of the paged-KV attention hot path on one GB300 (or N replicas).
 
-A step is one decode step of one attention layer on the Qwen3-0.6B-shaped
-workload (batch 64, 16 q / 8 kv heads, head_dim 128, block_size 256,
-context_lens ~ U{1..4096}, pool sized for all sequences + 20 %, random block
-permutation, bf16 N(0,1)):
-  1. slot mapping of each sequence's newest token (address translation),
-  2. store_kvcache of the 64 new K/V rows,
-  3. split-KV GQA decode attention over all context tokens.
-All inputs are resident in HBM before the timed region; L2 is flushed (a
-256 MiB write) before every timed step.  The printed `value` is decode
-tokens/s (one layer) over all ranks; `e2e` is the same metric through the
-public API with the step's inputs copied from pinned host memory and the
-output copied back inside the timed region.  The decode kernel's own CUDA-
-event time gives the HBM roofline fraction.  The CPU oracle, timed on the
-host cores on a bounded sample, is reported as `cpu_baseline`.
+A step is one decode step of one attention layer on the largest single-GPU
+decode workload, the Qwen3-8B attention shape: batch 256, 32 q / 8 kv heads,
+head_dim 128, block_size 256, context_lens lognormal (median 1024, capped
+8192), sequences 0..127 sharing their first 4 physical blocks (prefix cache,
+ref_count 128), pool = 1.2x the blocks needed, random block permutation, bf16
+N(0,1).  The step is one launch of the fused kernel (pa_decode_store): each
+sequence's new K/V row is stored to its slot and the split-KV GQA decode
+attention reads every context row through the block tables.  All inputs are
+resident in HBM before the timed region; L2 is flushed (a 256 MiB write)
+before every timed step.  `value` is decode tokens/s (one layer) over all
+ranks; `e2e` is the same metric through the public API with the step's
+inputs copied from pinned host memory and the output copied back inside the
+timed region.  The roofline counts the bytes the step must move with every
+physical K/V row once (the 4 shared blocks once, not once per sequence);
+the logical figure (shared rows counted per sequence) is reported beside it.
+
+Sub-records, each with its own roofline: the other decode workloads (tiny,
+Qwen3-0.6B, 32k long context), the varlen prefill with prefix cache, and
+the Gumbel-max sampler.  `cpu_baseline` is the oracle timed on the host's
+cores (single-threaded and on all cores) on the same workload.
 
 `--impl reference` runs the CPU oracle (the only reference this path has) on
 the same workload and prints its own line.
 
-Multi-GPU (torchrun): every rank serves its own batch of 64 sequences with
-its own pool (replicas, weak scaling); no collective is on the data path.
+Multi-GPU (torchrun): every rank serves its own batch with its own pool
+(replicas, weak scaling); no collective is on the data path.
 """
 from __future__ import annotations
 
@@ -39,9 +45,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attn tokens/s and HBM GB/s vs GB300 peak; prefill TFLOP/s"
-WORKLOAD = ("qwen3-0.6b decode step, 1 layer: batch 64, 16 q / 8 kv heads, head_dim 128, block_size 256, "
-            "context_lens ~ U[1,4096], pool = 1.2x blocks needed, random block permutation, "
+HEADLINE_CONFIG = 3
+WORKLOAD = ("qwen3-8b decode step, 1 layer: batch 256, 32 q / 8 kv heads, head_dim 128, block_size 256, "
+            "context_lens lognormal (median 1024, sigma 1, capped 8192), sequences 0..127 share their first 4 "
+            "physical blocks (prefix cache), pool = 1.2x blocks needed, random block permutation, "
             "store of the new token fused into the split-KV decode kernel (pa_decode_store)")
+SUB_DECODE_CONFIGS = (1, 2, 4)
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -63,9 +72,11 @@ def source_digest(files):
 
 
 DECODE_SOURCES = ["paged_kv_cache_store_gb300/csrc/pa_decode.cu", "paged_kv_cache_store_gb300/csrc/pa_internal.cuh"]
+PREFILL_SOURCES = ["paged_kv_cache_store_gb300/csrc/pa_prefill.cu", "paged_kv_cache_store_gb300/csrc/pa_tcgen05.cuh",
+                   "paged_kv_cache_store_gb300/csrc/pa_internal.cuh"]
 
 
-def recorded_traffic(kernel: str, workload_key: str):
+def recorded_traffic(kernel: str, workload_key: str, sources=DECODE_SOURCES):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current source of the kernel; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -74,23 +85,28 @@ def recorded_traffic(kernel: str, workload_key: str):
     with open(p) as f:
         d = json.load(f)
     rec = d.get(kernel, {}).get(workload_key)
-    if not rec or rec.get("source_digest") != source_digest(DECODE_SOURCES):
+    if not rec or rec.get("source_digest") != source_digest(sources):
         return None
     return float(rec["dram_bytes_per_launch"])
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clocks, throttle reasons and utilisation
+    during the timed region (into a temporary CSV, or `path`)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, path: str | None = None):
+        import tempfile
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv") \
-            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/pa_clocks_{os.getpid()}.csv"
+        self.keep = path is not None
+        if path is None:
+            fd, path = tempfile.mkstemp(prefix="pa_clocks_", suffix=".csv")
+            os.close(fd)
+        self.path = path
 
     def __enter__(self):
         try:
@@ -116,25 +132,34 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return None
-        sm, mx, reasons = [], [], set()
+        sm, mx, busy_sm, reasons, n_busy = [], [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for ln in f:
                 c = [x.strip() for x in ln.split(",")]
-                if len(c) < 9:
+                if len(c) < 10:
                     continue
                 try:
-                    sm.append(float(c[1]))
-                    mx.append(float(c[2]))
+                    clk, cmax, util = float(c[1]), float(c[2]), float(c[9])
                 except ValueError:
                     continue
-                for n, v in zip(names, c[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
+                sm.append(clk)
+                mx.append(cmax)
+                if util >= 50.0:  # a sample taken while kernels were running
+                    n_busy += 1
+                    busy_sm.append(clk)
+                    for n, v in zip(names, c[5:9]):
+                        if v.lower() == "active":
+                            reasons.add(n)
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(busy_sm or sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "samples_under_load": n_busy}
 
 
 def dist_env():
@@ -162,20 +187,72 @@ def job_throughput(ws: int, units_per_rank: int, steps: int, total_ms: float) ->
     return ws * units_per_rank * steps / (total_ms / 1000.0)
 
 
-def time_oracle_step(inp, O, budget_s: float):
-    """Runs the oracle's step (slot mapping, store, decode) on the workload for
-    about budget_s seconds; returns (tokens/s, steps)."""
+def decode_bytes(inp):
+    """Algorithmic bytes of one fused store + decode launch.
+
+    Every context row of every (sequence, kv head) is read once, q is read
+    and out written, and each sequence's new K/V row is read and written to
+    its slot.  `unique` counts each physical pool row once (rows of blocks
+    that several sequences share are read from HBM once; their re-reads come
+    from L2); `logical` counts them once per sequence that reads them."""
+    row = inp.num_kv_heads * inp.head_dim * 2 * 2            # K and V of one token, all kv heads
+    ctx = inp.context_lens.astype(np.int64)
+    logical_rows = int(ctx.sum())
+    rows_in_block = {}
+    for b in range(inp.batch):
+        n = int(ctx[b])
+        for j in range((n + inp.block_size - 1) // inp.block_size):
+            blk = int(inp.block_tables[b, j])
+            used = min(inp.block_size, n - j * inp.block_size)
+            rows_in_block[blk] = max(rows_in_block.get(blk, 0), used)
+    unique_rows = sum(rows_in_block.values())
+    qo = 2 * inp.batch * inp.num_q_heads * inp.head_dim * 2
+    new_rows = 2 * inp.batch * row                           # read from new_k/new_v, written to the slot
+    return {"logical": logical_rows * row + qo + new_rows, "unique": unique_rows * row + qo + new_rows,
+            "logical_rows": logical_rows, "unique_rows": unique_rows}
+
+
+def oracle_decode_step(inp, O, threads: int):
+    """One step of the oracle on a decode workload: slot mapping, store of the
+    new rows into copies of the caches, decode attention (on `threads` host
+    threads; 1 = the oracle as it stands)."""
+    from oracle import parallel as OP
+    kc, vc = inp.k_cache.copy(), inp.v_cache.copy()
+    slots = np.array([O.decode_slot(inp.block_tables[b], inp.block_size, int(inp.context_lens[b]))
+                      for b in range(inp.batch)], np.int32)
+    O.store_kvcache(inp.new_k, inp.new_v, kc, vc, slots)
+    if threads == 1:
+        return O.decode(inp.q, kc, vc, inp.block_tables, inp.context_lens, inp.scale)
+    return OP.decode(inp.q, kc, vc, inp.block_tables, inp.context_lens, inp.scale, threads=threads)
+
+
+def time_oracle(inp, O, threads: int, budget_s: float):
+    """Oracle decode steps on the workload for about budget_s seconds (at
+    least one); returns (tokens/s, steps, seconds)."""
     steps, t0 = 0, time.perf_counter()
     while True:
-        kc, vc = inp.k_cache.copy(), inp.v_cache.copy()
-        slots = np.array([O.decode_slot(inp.block_tables[b], inp.block_size, int(inp.context_lens[b]))
-                          for b in range(inp.batch)], np.int32)
-        O.store_kvcache(inp.new_k, inp.new_v, kc, vc, slots)
-        O.decode(inp.q, kc, vc, inp.block_tables, inp.context_lens, inp.scale)
+        oracle_decode_step(inp, O, threads)
         steps += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             return steps * inp.batch / el, steps, el
+
+
+def cpu_baseline(inp, budget_s: float):
+    """The oracle as it stands (float64 C, scalar loops) on the host cores:
+    on all cores (rows split between threads) for about budget_s, and one
+    single-threaded step."""
+    import oracle as O
+    from oracle import parallel as OP
+    O.lib()
+    n = OP.host_threads()
+    tps, steps, el = time_oracle(inp, O, n, budget_s)
+    tps1, steps1, el1 = time_oracle(inp, O, 1, 0.0)
+    return {"value": tps, "unit": "tokens/s", "cores": n, "kind": "oracle",
+            "sample": f"{steps} full steps of the same workload in {el:.1f} s on {n} threads "
+                      f"(rows split between threads, each row by the unchanged float64 oracle)",
+            "single_thread": {"value": tps1, "unit": "tokens/s", "cores": 1,
+                              "sample": f"{steps1} full step(s) in {el1:.1f} s"}}
 
 
 def run_reference(args):
@@ -183,14 +260,16 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle as O
+    from oracle import parallel as OP
     from paged_kv_cache_store_gb300.workloads import decode_config
-    inp = decode_config(2)
+    inp = decode_config(HEADLINE_CONFIG)
     O.lib()
+    n = OP.host_threads()
     for _ in range(args.warmup):
-        time_oracle_step(inp, O, 0.0)
+        oracle_decode_step(inp, O, n)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        time_oracle_step(inp, O, 0.0)
+        oracle_decode_step(inp, O, n)
     el = time.perf_counter() - t0
     value = args.steps * inp.batch / el
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
@@ -198,8 +277,8 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) bf16)",
             "config": {"workload": WORKLOAD, "global_batch": inp.batch, "l2": "n/a (CPU)"},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"full workload, {args.steps} steps"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n, "kind": "oracle",
+                             "sample": f"full workload, {args.steps} steps, rows split over {n} threads"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -215,23 +294,77 @@ def prefill_pairs(p):
     return tot
 
 
+def _to_dev(a, dev, bf=False):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf else np.ascontiguousarray(a))
+    return (t.view(torch.bfloat16) if bf else t).to(dev)
+
+
+def _event_times(fn, steps, stream, flush):
+    """Per-call CUDA-event times (ms) of `steps` calls of fn, L2 flushed before each."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a_, b_ in ev:
+        flush.zero_()
+        a_.record(stream)
+        fn()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    return [a_.elapsed_time(b_) for a_, b_ in ev]
+
+
+def _check_device(pa):
+    code, where = pa.get_device_error()
+    if code:
+        raise RuntimeError(f"device error {code} at {where}")
+
+
+def measure_decode_config(cfg, args, dev, stream, flush, hbm_peak):
+    """A decode workload's fused store + decode step (one launch), L2 flushed
+    before each call: time, tokens/s and its own roofline."""
+    import torch
+    import paged_kv_cache_store_gb300 as pa
+    from paged_kv_cache_store_gb300.workloads import decode_config
+    inp = decode_config(cfg)
+    kc, vc, q = _to_dev(inp.k_cache, dev, True), _to_dev(inp.v_cache, dev, True), _to_dev(inp.q, dev, True)
+    nk, nv = _to_dev(inp.new_k, dev, True), _to_dev(inp.new_v, dev, True)
+    bt, ctx = _to_dev(inp.block_tables, dev), _to_dev(inp.context_lens, dev)
+    out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
+    wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev)
+
+    def step():
+        pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out, new_k=nk, new_v=nv)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    ms = _event_times(step, args.steps, stream, flush)
+    _check_device(pa)
+    ms_avg = sum(ms) / len(ms)
+    by = decode_bytes(inp)
+    gbs = by["unique"] / (ms_avg / 1000.0) / 1e9
+    del kc, vc
+    torch.cuda.empty_cache()
+    return {"workload": inp.name, "batch": inp.batch, "ms": ms_avg, "ms_median": float(np.median(ms)),
+            "tokens_per_s": inp.batch / (ms_avg / 1000.0),
+            "roofline": {"bound": "hbm", "kernel": f"decode_kernel<{inp.num_q_heads // inp.num_kv_heads}, store>",
+                         "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                         "frac_of_nominal_8TBps": gbs / 8000.0, "algorithmic_bytes_per_launch": by["unique"],
+                         "traffic": None},
+            "note": "launch-latency bound (about 1 MB moved)" if cfg == 1 else None}
+
+
 def measure_prefill(args, dev, stream, flush, bf16_peak):
     """The varlen prefill workload: slot mapping + store of the uncached suffix,
-    then causal prefill over the paged pool.  Returns a JSON-able dict."""
+    then causal prefill over the paged pool; and the same step as one fused
+    launch.  Returns a JSON-able dict."""
     import torch
     import paged_kv_cache_store_gb300 as pa
     from paged_kv_cache_store_gb300.workloads import prefill_config
 
     p = prefill_config(5)
-
-    def to_dev(a, bf=False):
-        if bf:
-            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    kc, vc = to_dev(p.k_cache, True), to_dev(p.v_cache, True)
-    q, nk, nv = to_dev(p.q, True), to_dev(p.new_k, True), to_dev(p.new_v, True)
-    bt, cq, ck = to_dev(p.block_tables), to_dev(p.cu_seqlens_q), to_dev(p.cu_seqlens_k)
+    kc, vc = _to_dev(p.k_cache, dev, True), _to_dev(p.v_cache, dev, True)
+    q, nk, nv = _to_dev(p.q, dev, True), _to_dev(p.new_k, dev, True), _to_dev(p.new_v, dev, True)
+    bt, cq, ck = _to_dev(p.block_tables, dev), _to_dev(p.cu_seqlens_q, dev), _to_dev(p.cu_seqlens_k, dev)
     slots = torch.empty(p.total_q, dtype=torch.int32, device=dev)
     out = torch.empty(p.total_q, p.num_q_heads, p.head_dim, dtype=torch.bfloat16, device=dev)
     mq, mk = int(p.seqlens_q.max()), int(p.seqlens_k.max())
@@ -257,9 +390,7 @@ def measure_prefill(args, dev, stream, flush, bf16_peak):
         flush.zero_()
         step(e)
     torch.cuda.synchronize()
-    code, where = pa.get_device_error()
-    if code:
-        raise RuntimeError(f"device error {code} at {where}")
+    _check_device(pa)
     pre_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / len(evs)
     step3_ms = sum(e[0].elapsed_time(e[2]) for e in evs) / len(evs)
     # The same step as one launch: the fused store + prefill (cooperative).
@@ -271,31 +402,23 @@ def measure_prefill(args, dev, stream, flush, bf16_peak):
 
     for _ in range(3):
         fused()
-    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for a_, b_ in fev:
-        flush.zero_()
-        a_.record(stream)
-        fused()
-        b_.record(stream)
-    torch.cuda.synchronize()
-    code, where = pa.get_device_error()
-    if code:
-        raise RuntimeError(f"device error {code} at {where}")
-    fused_ms = sum(a_.elapsed_time(b_) for a_, b_ in fev) / len(fev)
+    fused_ms = sum(_event_times(fused, args.steps, stream, flush)) / args.steps
+    _check_device(pa)
     slotmap_store_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)
     store_ms = sum(e[3].elapsed_time(e[1]) for e in evs) / len(evs)
     flops = 4 * p.head_dim * p.num_q_heads * prefill_pairs(p)
     tflops = flops / (pre_ms / 1000.0) / 1e12
     store_bytes = p.total_q * p.num_kv_heads * p.head_dim * 2 * 4
     del kc, vc
+    torch.cuda.empty_cache()
     return {"workload": "varlen causal prefill, 16 seqs, 32 q / 8 kv heads, Lk ~ U[128,2048], 0..3 cached "
                         "blocks per seq, block_size 256 (suffix stored via slot_mapping first)",
             "total_q": p.total_q, "ms_prefill": pre_ms, "ms_slotmap_store": slotmap_store_ms, "ms_store": store_ms,
             "ms_step_3_launches": step3_ms, "ms_step_fused": fused_ms,
             "algorithmic_flops": flops,
             "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": tflops, "peak": bf16_peak,
-                         "unit": "TFLOP/s", "frac": tflops / bf16_peak, "traffic": None},
+                         "unit": "TFLOP/s", "frac": tflops / bf16_peak, "peak_kind": "burst (timed alone)",
+                         "traffic": recorded_traffic("prefill_kernel<0>", "prefill", PREFILL_SOURCES)},
             "store_gbs": store_bytes / (store_ms / 1000.0) / 1e9}
 
 
@@ -308,24 +431,15 @@ def measure_sampler(args, dev, stream, flush, hbm_peak):
     from paged_kv_cache_store_gb300.workloads import sampler_config
 
     sp = sampler_config(64)
-    lg = torch.from_numpy(np.ascontiguousarray(sp.logits).view(np.int16)).view(torch.bfloat16).to(dev)
+    lg = _to_dev(sp.logits, dev, True)
     temps = torch.from_numpy(sp.temperatures).to(dev)
     noise = torch.from_numpy(sp.exp_noise).to(dev)
     out = torch.empty(sp.batch, dtype=torch.int32, device=dev)
     for _ in range(max(3, args.warmup)):
         pa.sample_gumbel(lg, temps, noise, out=out)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for a, b in evs:
-        flush.zero_()
-        a.record(stream)
-        pa.sample_gumbel(lg, temps, noise, out=out)
-        b.record(stream)
-    torch.cuda.synchronize()
-    code, where = pa.get_device_error()
-    if code:
-        raise RuntimeError(f"device error {code} at {where}")
-    ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    ms = sum(_event_times(lambda: pa.sample_gumbel(lg, temps, noise, out=out), args.steps, stream, flush))
+    ms /= args.steps
+    _check_device(pa)
     alg = sp.batch * sp.vocab * (2 + 4) + sp.batch * (4 + 4)
     gbs = alg / (ms / 1000.0) / 1e9
     return {"workload": sp.name + ", fp32 Exp(1) draws", "ms": ms, "algorithmic_bytes": alg,
@@ -346,23 +460,19 @@ def run_ours(args):
     from paged_kv_cache_store_gb300.workloads import decode_config
 
     dev = torch.device("cuda", local)
-    inp = decode_config(2)
-
-    def to_dev(a, dt):
-        if dt == torch.bfloat16:
-            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    kc, vc = to_dev(inp.k_cache, torch.bfloat16), to_dev(inp.v_cache, torch.bfloat16)
-    q = to_dev(inp.q, torch.bfloat16)
-    nk, nv = to_dev(inp.new_k, torch.bfloat16), to_dev(inp.new_v, torch.bfloat16)
-    bt, ctx = to_dev(inp.block_tables, torch.int32), to_dev(inp.context_lens, torch.int32)
+    hbm, bf16_peak, peak_kind = peaks()
+    inp = decode_config(HEADLINE_CONFIG)
+    kc, vc = _to_dev(inp.k_cache, dev, True), _to_dev(inp.v_cache, dev, True)
+    q = _to_dev(inp.q, dev, True)
+    nk, nv = _to_dev(inp.new_k, dev, True), _to_dev(inp.new_v, dev, True)
+    bt, ctx = _to_dev(inp.block_tables, dev), _to_dev(inp.context_lens, dev)
     slots = torch.empty(inp.batch, dtype=torch.int32, device=dev)
     out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
     wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    L2 = "flushed (256 MiB write) before every timed step; KV pool 621 MiB > L2"
+    by = decode_bytes(inp)
+    L2 = (f"flushed (256 MiB write) before every timed step; K/V pool {kc.numel() * 4 / 2**30:.2f} GiB > L2")
 
     def step():  # one kernel: the decode kernel stores the new K/V rows, then attends
         pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out, new_k=nk, new_v=nv)
@@ -376,24 +486,38 @@ def run_ours(args):
         step()
         step_unfused()
     torch.cuda.synchronize()
-    code, where = pa.get_device_error()
-    if code:
-        raise RuntimeError(f"device error {code} at {where}")
+    _check_device(pa)
 
-    # Headline: whole steps, L2 flushed before each.
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
+    def flushed_steps(n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a_, b_ in ev:
             flush.zero_()
-            ev[i][0].record(stream)
+            a_.record(stream)
             step()
-            ev[i][1].record(stream)
+            b_.record(stream)
+        return ev
+
+    # Clocks: sampled while the same flushed steps run back to back for at
+    # least `sustain_s` (so the sampler sees the GPU under this load), then
+    # through the timed region itself.
+    probe = flushed_steps(8)
+    torch.cuda.synchronize()
+    est = (float(np.median([a.elapsed_time(b) for a, b in probe])) + 0.05) / 1000.0
+    n_sustain = int(math.ceil(args.sustain_s / est))
+    with ClockSampler(local, args.clock_log) as clk:
+        sus = flushed_steps(n_sustain)
         torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
+        # Headline: exactly `steps` whole steps, L2 flushed before each,
+        # bracketed by a barrier and a synchronize on both sides.
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev = flushed_steps(args.steps)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+    _check_device(pa)
+    sus_ms = [a.elapsed_time(b) for a, b in sus]
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(sum(step_ms), dev, ws)
     ms_per_step = total_ms / args.steps
@@ -401,17 +525,8 @@ def run_ours(args):
 
     # The same step as three launches (slot mapping, store, decode: programmatic
     # dependent launches back to back), for comparison.
-    uev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for a, b in uev:
-        flush.zero_()
-        a.record(stream)
-        step_unfused()
-        b.record(stream)
-    torch.cuda.synchronize()
-    unfused_ms = sum(a.elapsed_time(b) for a, b in uev) / args.steps
-
-    # Per-kernel durations for the roofline: events around the store and the
-    # decode launch of the unfused step (same inputs, L2 flushed before each).
+    unfused_ms = sum(_event_times(step_unfused, args.steps, stream, flush)) / args.steps
+    # The plain decode launch alone (store done before it).
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     for i in range(args.steps):
         flush.zero_()
@@ -466,55 +581,52 @@ def run_ours(args):
         raise RuntimeError("end-to-end output differs from the device output")
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), dev, ws)
     e2e_value = job_throughput(ws, inp.batch, args.steps, e2e_ms)
+    _check_device(pa)
+    del kc, vc, flush
+    torch.cuda.empty_cache()
 
-    code, where = pa.get_device_error()
-    if code:
-        raise RuntimeError(f"device error {code} at {where}")
-    prefill = None
-    if not args.no_prefill:
-        del kc, vc
-        torch.cuda.empty_cache()
-        prefill = measure_prefill(args, dev, stream, flush, peaks()[1])
-    sampler = measure_sampler(args, dev, stream, flush, peaks()[0])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    sub = {}
+    for cfg in SUB_DECODE_CONFIGS:
+        sub[f"decode_config{cfg}"] = measure_decode_config(cfg, args, dev, stream, flush, hbm)
+    prefill = None if args.no_prefill else measure_prefill(args, dev, stream, flush, bf16_peak)
+    sampler = measure_sampler(args, dev, stream, flush, hbm)
 
     if rank == 0:
-        hbm, _, peak_kind = peaks()
-        kv_bytes = int(inp.context_lens.astype(np.int64).sum()) * inp.num_kv_heads * inp.head_dim * 2 * 2
-        qo_bytes = 2 * inp.batch * inp.num_q_heads * inp.head_dim * 2
-        # The headline step is one launch of the fused kernel: it reads every
-        # context token's K/V row once, q, and the new rows, and writes out and
-        # the new rows' slots.
-        new_row_bytes = inp.batch * inp.num_kv_heads * inp.head_dim * 2 * 2
-        alg_bytes = kv_bytes + qo_bytes + 2 * new_row_bytes
-        dec_avg = sum(dec_ms) / len(dec_ms)
-        achieved = alg_bytes / (ms_per_step / 1000.0) / 1e9
-        traffic = recorded_traffic("decode_kernel<2, store>", "qwen3-0.6b")
+        achieved = by["unique"] / (ms_per_step / 1000.0) / 1e9
+        achieved_logical = by["logical"] / (ms_per_step / 1000.0) / 1e9
+        traffic = recorded_traffic(f"decode_kernel<{inp.num_q_heads // inp.num_kv_heads}, store>", "qwen3-8b")
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
             "data": "synthetic (seeded N(0,1) bf16, random block tables)",
-            "config": {"workload": WORKLOAD, "global_batch": inp.batch * ws, "seq_len": "U[1,4096]",
+            "config": {"workload": WORKLOAD, "global_batch": inp.batch * ws, "seq_len": "lognormal(1024), cap 8192",
                        "parallelism": f"replicas x{ws}", "l2": L2},
-            "roofline": {"bound": "hbm", "kernel": "decode_kernel<2, store> (pa_decode_store)", "achieved": achieved,
+            "roofline": {"bound": "hbm", "kernel": "decode_kernel<4, store> (pa_decode_store)", "achieved": achieved,
                          "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
                          "frac_of_nominal_8TBps": achieved / 8000.0, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": ms_per_step,
-                         "plain_decode_ms": dec_avg, "store_ms": sum(store_ms) / len(store_ms)},
+                         "algorithmic_bytes_per_launch": by["unique"],
+                         "bytes_basis": "unique: every physical K/V row once (the 4 shared blocks once)",
+                         "logical": {"algorithmic_bytes_per_launch": by["logical"], "achieved": achieved_logical,
+                                     "frac": achieved_logical / hbm,
+                                     "basis": "shared prefix rows counted once per sequence that reads them"},
+                         "launch_ms": ms_per_step, "plain_decode_ms": sum(dec_ms) / len(dec_ms),
+                         "store_ms": sum(store_ms) / len(store_ms)},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps,
+            "sustained": {"steps": n_sustain, "seconds": sum(sus_ms) / 1000.0,
+                          "ms_median": float(np.median(sus_ms)),
+                          "note": "the same flushed step back to back before the timed region, for the clock record"},
             "unfused_step": {"ms_per_step": unfused_ms, "kernels": "slot_mapping_decode + store_kvcache + decode",
                              "tokens_per_s": ws * inp.batch / (unfused_ms / 1000.0)},
             "clocks": clk.summary(),
+            "decode_configs": sub,
             "prefill": prefill,
             "sampler": sampler,
         }
         if not args.no_cpu_baseline:
-            import oracle as O
-            O.lib()
-            tps, steps, el = time_oracle_step(inp, O, args.cpu_seconds)
-            line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                    "sample": f"{steps} full steps of the same workload ({el:.1f} s, 1 thread)"}
+            line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
@@ -527,75 +639,60 @@ def run_report(args):
     configurations 1-4 run the fused store + decode step, configuration 5 the
     varlen prefill (and its fused store + prefill step).  Device time: median
     of `steps` calls, CUDA events, L2 flushed before each.  Parity: against
-    the oracle on the same inputs (all outputs for decode; 2048 sampled
-    (token, head) rows for prefill).  Oracle time: one single-threaded oracle
-    step (for prefill, the sampled rows, extrapolated by their share of the
-    visible (query, key) pairs)."""
+    the oracle on the same inputs, every output row.  Oracle time: one step
+    of the oracle on all host cores (rows split between threads) and, for
+    decode, one single-threaded step."""
     import torch
     import oracle as O
+    from oracle import parallel as OP
     import paged_kv_cache_store_gb300 as pa
     from paged_kv_cache_store_gb300.workloads import decode_config, prefill_config, bf16_bits_to_f32
     O.lib()
+    nthr = OP.host_threads()
     dev = torch.device("cuda", 0)
     hbm, bf16_peak, kind = peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def to(a, bf=False):
-        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf else np.ascontiguousarray(a))
-        return (t.view(torch.bfloat16) if bf else t).to(dev)
+    stream = torch.cuda.current_stream(dev)
 
     def timed(fn):
         for _ in range(3):
             fn()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        for a_, b_ in ev:
-            flush.zero_()
-            a_.record()
-            fn()
-            b_.record()
-        torch.cuda.synchronize()
-        code, where = pa.get_device_error()
-        if code:
-            raise RuntimeError(f"device error {code} at {where}")
-        return float(np.median([a_.elapsed_time(b_) for a_, b_ in ev]))
+        ms = _event_times(fn, args.steps, stream, flush)
+        _check_device(pa)
+        return float(np.median(ms))
 
     def host(t):
         return bf16_bits_to_f32(t.cpu().view(torch.int16).numpy().view(np.uint16)).astype(np.float64)
 
-    traffic = recorded_traffic("decode_kernel<2, store>", "qwen3-0.6b")
-    lines = ["| Config | GPU time | tokens/s (decode, 1 layer) | GB/s (algorithmic) | TFLOP/s | % roofline "
-             "| ncu DRAM GB/s | Oracle 1-thread | Parity (max / mean abs) |", "|" + "---|" * 9]
+    lines = ["| Config | GPU time | tokens/s (decode, 1 layer) | GB/s (algorithmic, unique rows) | TFLOP/s "
+             "| % roofline | Oracle (all cores / 1 thread) | Parity, all rows (max / mean abs) |", "|" + "---|" * 8]
     for cfg in (1, 2, 3, 4):
         inp = decode_config(cfg)
-        kc, vc, q = to(inp.k_cache, True), to(inp.v_cache, True), to(inp.q, True)
-        nk, nv = to(inp.new_k, True), to(inp.new_v, True)
-        bt, ctx = to(inp.block_tables), to(inp.context_lens)
+        kc, vc, q = _to_dev(inp.k_cache, dev, True), _to_dev(inp.v_cache, dev, True), _to_dev(inp.q, dev, True)
+        nk, nv = _to_dev(inp.new_k, dev, True), _to_dev(inp.new_v, dev, True)
+        bt, ctx = _to_dev(inp.block_tables, dev), _to_dev(inp.context_lens, dev)
         out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
         wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev)
         ms = timed(lambda: pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out, new_k=nk, new_v=nv))
         t0 = time.perf_counter()
-        okc, ovc = inp.k_cache.copy(), inp.v_cache.copy()
-        slots = np.array([O.decode_slot(inp.block_tables[b], inp.block_size, int(inp.context_lens[b]))
-                          for b in range(inp.batch)], np.int32)
-        O.store_kvcache(inp.new_k, inp.new_v, okc, ovc, slots)
-        want = O.decode(inp.q, okc, ovc, inp.block_tables, inp.context_lens, inp.scale)
+        want = oracle_decode_step(inp, O, nthr)
         oracle_s = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        oracle_decode_step(inp, O, 1)
+        oracle_1 = time.perf_counter() - t0
         err = np.abs(host(out) - want)
-        row = inp.num_kv_heads * inp.head_dim * 2
-        alg = int(inp.context_lens.astype(np.int64).sum()) * row * 2 + 2 * inp.batch * inp.num_q_heads * \
-            inp.head_dim * 2 + 2 * inp.batch * row * 2
-        gbs = alg / (ms / 1000.0) / 1e9
-        note = " (logical; shared blocks counted per sequence)" if cfg == 3 else ""
-        ncu = f"{traffic / (ms / 1000.0) / 1e9:.0f} ({traffic / 1e6:.1f} MB)" if cfg == 2 and traffic else "—"
+        by = decode_bytes(inp)
+        gbs = by["unique"] / (ms / 1000.0) / 1e9
+        note = f" ({by['logical'] / (ms / 1000.0) / 1e9:,.0f} logical)" if by["logical"] != by["unique"] else ""
         lines.append(f"| {cfg} {inp.name} | {ms * 1000:.1f} us | {inp.batch / (ms / 1000.0):,.0f} | "
-                     f"{gbs:,.0f}{note} | — | {100 * gbs / hbm:.1f} % of {hbm:.0f} ({kind}) | {ncu} | "
-                     f"{oracle_s:.2f} s ({inp.batch / oracle_s:,.0f} tokens/s) | {err.max():.2e} / {err.mean():.2e} |")
+                     f"{gbs:,.0f}{note} | — | {100 * gbs / hbm:.1f} % of {hbm:.0f} ({kind}) | "
+                     f"{oracle_s:.2f} s on {nthr} / {oracle_1:.2f} s | {err.max():.2e} / {err.mean():.2e} |")
         del kc, vc
         torch.cuda.empty_cache()
     p = prefill_config(5)
-    kc, vc, q = to(p.k_cache, True), to(p.v_cache, True), to(p.q, True)
-    nk, nv = to(p.new_k, True), to(p.new_v, True)
-    bt, cq, ck = to(p.block_tables), to(p.cu_seqlens_q), to(p.cu_seqlens_k)
+    kc, vc, q = _to_dev(p.k_cache, dev, True), _to_dev(p.v_cache, dev, True), _to_dev(p.q, dev, True)
+    nk, nv = _to_dev(p.new_k, dev, True), _to_dev(p.new_v, dev, True)
+    bt, cq, ck = _to_dev(p.block_tables, dev), _to_dev(p.cu_seqlens_q, dev), _to_dev(p.cu_seqlens_k, dev)
     out = torch.empty(p.total_q, p.num_q_heads, p.head_dim, dtype=torch.bfloat16, device=dev)
     mq, mk = int(p.seqlens_q.max()), int(p.seqlens_k.max())
     slots = pa.slot_mapping_prefill(bt, cq, ck, p.block_size, total_q=p.total_q)
@@ -604,60 +701,69 @@ def run_report(args):
     wsf = pa.prefill_store_workspace(dev)
     ms_fused = timed(lambda: pa.prefill_varlen(q, kc, vc, cq, ck, mq, mk, p.scale, block_tables=bt, out=out,
                                                new_k=nk, new_v=nv, workspace=wsf))
-    pairs = prefill_pairs(p)
-    flops = 4 * p.head_dim * p.num_q_heads * pairs
+    flops = 4 * p.head_dim * p.num_q_heads * prefill_pairs(p)
     okc, ovc = p.k_cache.copy(), p.v_cache.copy()
     oslots = np.concatenate([O.slot_mapping(p.block_tables[s], p.block_size, int(p.seqlens_k[s] - p.seqlens_q[s]),
                                             int(p.seqlens_k[s])) for s in range(p.num_seqs)])
     O.store_kvcache(p.new_k, p.new_v, okc, ovc, oslots)
-    rows = np.sort(np.random.default_rng(5).choice(p.total_q * p.num_q_heads, 2048, replace=False))
     t0 = time.perf_counter()
-    want = O.prefill(p.q, okc, ovc, p.cu_seqlens_q, p.cu_seqlens_k, p.scale, block_tables=p.block_tables,
-                     rows=rows)
+    want = OP.prefill(p.q, okc, ovc, p.cu_seqlens_q, p.cu_seqlens_k, p.scale, block_tables=p.block_tables)
     oracle_s = time.perf_counter() - t0
-    seq_of = np.searchsorted(p.cu_seqlens_q, rows // p.num_q_heads, side="right") - 1
-    keys = (p.seqlens_k - p.seqlens_q)[seq_of] + (rows // p.num_q_heads - p.cu_seqlens_q[seq_of]) + 1
-    oracle_full = oracle_s * (pairs * p.num_q_heads) / float(keys.sum())
-    err = np.abs(host(out).reshape(-1, p.head_dim)[rows] - want)
+    err = np.abs(host(out) - want)
     tf = flops / (ms / 1000.0) / 1e12
     lines.append(f"| 5 {p.name} | {ms * 1000:.1f} us (fused store + prefill: {ms_fused * 1000:.1f} us) | — | — | "
-                 f"{tf:.0f} | {100 * tf / bf16_peak:.1f} % of {bf16_peak:.0f} ({kind}) | — | "
-                 f"~{oracle_full:.0f} s (2048 rows in {oracle_s:.1f} s) | {err.max():.2e} / {err.mean():.2e} |")
+                 f"{tf:.0f} | {100 * tf / bf16_peak:.1f} % of {bf16_peak:.0f} ({kind}) | "
+                 f"{oracle_s:.1f} s on {nthr} | {err.max():.2e} / {err.mean():.2e} |")
     print("\n".join(lines))
     return 0
 
 
 def run_profile_case(args):
-    """A reduced decode workload for captures that replay each launch many
-    times (ncu --set full): the Qwen3-0.6B shape (batch 64, 16 q / 8 kv
-    heads, fused store) with context lengths ~ U[1, 1536], about 190 MB of
-    K/V (more than the 129 MB L2, a fraction of the full case).  Runs
-    `warmup` then `steps` fused decode steps with an L2 flush before each."""
+    """Small launch sequences for ncu captures (no JSON line).
+
+    decode-small: the Qwen3-0.6B shape (batch 64, 16 q / 8 kv heads, fused
+    store) with context lengths ~ U[1, 1536], about 190 MB of K/V (more than
+    the 129 MB L2, a fraction of the full case), for multi-pass captures.
+    decode-qwen3-8b: the headline workload itself (about 2.4 GB on the
+    device), for single-pass captures (DRAM bytes and duration).
+    prefill: the prefill workload (plain prefill launches after one store).
+    Each runs `warmup` then `steps` launches with an L2 flush before each."""
     import torch
     import paged_kv_cache_store_gb300 as pa
-    from paged_kv_cache_store_gb300.workloads import make_decode
-    rng = np.random.default_rng(1002)
-    inp = make_decode("qwen3-0.6b decode b64 h16/8 ctx~U[1,1536]", 2, 64, 16, 8, rng.integers(1, 1537, size=64))
+    from paged_kv_cache_store_gb300.workloads import make_decode, decode_config, prefill_config
     dev = torch.device("cuda", 0)
-
-    def to_dev(a, bf=False):
-        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf else np.ascontiguousarray(a))
-        return (t.view(torch.bfloat16) if bf else t).to(dev)
-
-    kc, vc, q = to_dev(inp.k_cache, True), to_dev(inp.v_cache, True), to_dev(inp.q, True)
-    nk, nv = to_dev(inp.new_k, True), to_dev(inp.new_v, True)
-    bt, ctx = to_dev(inp.block_tables), to_dev(inp.context_lens)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    if args.profile_case == "prefill":
+        p = prefill_config(5)
+        kc, vc, q = _to_dev(p.k_cache, dev, True), _to_dev(p.v_cache, dev, True), _to_dev(p.q, dev, True)
+        bt, cq, ck = _to_dev(p.block_tables, dev), _to_dev(p.cu_seqlens_q, dev), _to_dev(p.cu_seqlens_k, dev)
+        slots = pa.slot_mapping_prefill(bt, cq, ck, p.block_size, total_q=p.total_q)
+        pa.store_kvcache(_to_dev(p.new_k, dev, True), _to_dev(p.new_v, dev, True), kc, vc, slots)
+        out = torch.empty(p.total_q, p.num_q_heads, p.head_dim, dtype=torch.bfloat16, device=dev)
+        mq, mk = int(p.seqlens_q.max()), int(p.seqlens_k.max())
+        for _ in range(args.warmup + args.steps):
+            flush.zero_()
+            pa.prefill_varlen(q, kc, vc, cq, ck, mq, mk, p.scale, block_tables=bt, out=out)
+        torch.cuda.synchronize()
+        _check_device(pa)
+        print(f"profile case: prefill, {p.total_q} query tokens, {args.warmup + args.steps} launches")
+        return 0
+    if args.profile_case == "decode-small":
+        rng = np.random.default_rng(1002)
+        inp = make_decode("qwen3-0.6b decode b64 h16/8 ctx~U[1,1536]", 2, 64, 16, 8, rng.integers(1, 1537, size=64))
+    else:
+        inp = decode_config(HEADLINE_CONFIG)
+    kc, vc, q = _to_dev(inp.k_cache, dev, True), _to_dev(inp.v_cache, dev, True), _to_dev(inp.q, dev, True)
+    nk, nv = _to_dev(inp.new_k, dev, True), _to_dev(inp.new_v, dev, True)
+    bt, ctx = _to_dev(inp.block_tables, dev), _to_dev(inp.context_lens, dev)
     out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
     wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup + args.steps):
         flush.zero_()
         pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out, new_k=nk, new_v=nv)
     torch.cuda.synchronize()
-    code, where = pa.get_device_error()
-    if code:
-        raise RuntimeError(f"device error {code} at {where}")
-    print(f"profile case: {inp.batch} seqs, {int(inp.context_lens.sum())} context tokens, "
+    _check_device(pa)
+    print(f"profile case: {inp.name}: {inp.batch} seqs, {int(inp.context_lens.sum())} context tokens, "
           f"{args.warmup + args.steps} fused decode launches")
     return 0
 
@@ -669,12 +775,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sustain-s", type=float, default=1.5,
+                    help="seconds of back-to-back flushed steps run under the clock sampler before the timed steps")
+    ap.add_argument("--clock-log", default=None, help="keep the nvidia-smi clock samples in this CSV file")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--report", action="store_true",
                     help="print the per-configuration results table (markdown) instead of the JSON line")
-    ap.add_argument("--profile-case", choices=["decode-small"], default=None,
-                    help="run only a reduced case for a multi-pass ncu capture (no JSON line)")
+    ap.add_argument("--profile-case", choices=["decode-small", "decode-qwen3-8b", "prefill"], default=None,
+                    help="run only a small launch sequence for an ncu capture (no JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
