@@ -106,6 +106,8 @@ struct PrefillArgs {
     const int32_t *cu_k;
     const int32_t *bt;
     int32_t max_blocks, num_seqs, Hq, group, mtiles;
+    int32_t upg;  // work units per (query tile, sequence) group: Hq, or Hq / 2 for paired heads
+    int32_t bn;   // keys per KV tile of the kernel (sizes the sort keys)
     int32_t block_size, box_rows, box_halves, paged, causal, num_blocks, checked, sorted;
     float scale_log2;
     DevError *err;
@@ -315,18 +317,19 @@ __device__ __forceinline__ int group_tiles(const PrefillArgs &a, int mt, int s) 
     if (bad || mt * BM >= Lq) return 0;
     const int last_row = min(mt * BM + BM, Lq) - 1;
     const int key_end = a.causal ? min(Lk, Lk - Lq + last_row + 1) : Lk;
-    return (key_end + BN - 1) / BN;
+    return (key_end + a.bn - 1) / a.bn;
 }
 
-// Unit t.  Sorted schedule: t = rank * Hq + q head, where rank indexes the
+// Unit t.  Sorted schedule: t = rank * upg + q head, where rank indexes the
 // groups sorted longest first.  Otherwise t = ((mtiles-1-mt) * num_seqs + s)
-// * Hq + q head (empty query tiles included; next_valid_unit skips them).
+// * upg + q head (empty query tiles included; next_valid_unit skips them).
+// (The paired kernel reads U.h as the head pair and recomputes the tiles.)
 __device__ __forceinline__ Unit unit_of(const PrefillArgs &a, const uint16_t *sched, int t) {
     Unit U;
-    const int grp = a.sorted ? (int)sched[t / a.Hq] : t / a.Hq;
+    const int grp = a.sorted ? (int)sched[t / a.upg] : t / a.upg;
     const int mt = a.mtiles - 1 - grp / a.num_seqs;
     U.s = grp % a.num_seqs;
-    U.h = t % a.Hq;
+    U.h = t % a.upg;
     U.m0 = mt * BM;
     U.q0 = __ldg(a.cu_q + U.s);
     U.Lq = __ldg(a.cu_q + U.s + 1) - U.q0;
@@ -341,7 +344,7 @@ __device__ __forceinline__ Unit unit_of(const PrefillArgs &a, const uint16_t *sc
         const int c = U.Lk - U.Lq;
         const int last_row = min(U.m0 + BM, U.Lq) - 1;
         U.key_end = a.causal ? min(U.Lk, c + last_row + 1) : U.Lk;
-        U.n_kv = (U.key_end + BN - 1) / BN;
+        U.n_kv = (U.key_end + a.bn - 1) / a.bn;
     }
     return U;
 }
@@ -352,13 +355,13 @@ __device__ __forceinline__ Unit unit_of(const PrefillArgs &a, const uint16_t *sc
 // skipping the many empty high query tiles costs one load latency per 32.
 // Every lane must call it; every role gets the same answer.
 __device__ __forceinline__ int next_valid_unit(const PrefillArgs &a, int t, int nunits, int lane) {
-    const int per = a.num_seqs * a.Hq;
+    const int per = a.num_seqs * a.upg;
     for (int base = t; base < nunits; base += 32 * (int)gridDim.x) {
         const int tt = base + lane * (int)gridDim.x;
         bool v = false;
         if (tt < nunits) {
             const int mt = a.mtiles - 1 - tt / per;
-            const int s = (tt % per) / a.Hq;
+            const int s = (tt % per) / a.upg;
             v = mt * BM < __ldg(a.cu_q + s + 1) - __ldg(a.cu_q + s);
         }
         const unsigned m = __ballot_sync(FULL, v);
@@ -396,7 +399,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + OFF_FLAGS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nunits = a.mtiles * a.num_seqs * a.Hq;
+    const int nunits = a.mtiles * a.num_seqs * a.upg;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NBAR; ++i) {
@@ -465,7 +468,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    nsorted *= a.Hq;  // units of the sorted schedule
+    nsorted *= a.upg;  // units of the sorted schedule
     // Unit i goes to slot i & 1; a slot is rewritten only after the softmax read
     // it (the Q.K thread cannot start unit i+2 before the softmax has released
     // the Q buffer of unit i), so a reader is never two phases behind.
@@ -817,9 +820,462 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
+// ===========================================================================
+// Paired-head prefill (GQA groups of even size).
+//
+// A work unit is one 128-row query tile of one sequence for two q heads of
+// the same kv head (A = head 2p, B = head 2p+1), so each K/V tile is loaded
+// once for both.  The keys come in tiles of 64.  TMEM (512 columns) holds,
+// per head, two S/P buffers of 64 columns and the 128-column O: S(A,0..1) at
+// 0 and 64, S(B,0..1) at 128 and 192, O(A) at 256, O(B) at 384.  Each head has
+// its own softmax warpgroup, so the two heads' exponentials run side by side,
+// and with two S buffers per head the tensor cores compute the scores of the
+// next tile while the softmax works on the current one.
+//  * warp 0 loads Q (both heads' tiles into the unit's pair of Q slots; the
+//    next unit's pair is loaded while this one runs) and the K tiles, warp 2
+//    the V tiles (rings of three 16 KiB stages).
+//  * warp 1 issues S(h, b) = Q(h).K^T (M = 128, N = 64, K = 128: 8 MMAs)
+//    for both heads into buffer b = tile & 1, once the P.V that last read the
+//    buffer has completed; warp 3 issues O(h) += P(h).V (M = 128, N = 128,
+//    K = 64: 4 MMAs, P from TMEM) for both heads once P is published.
+//  * warps 4..7 (head A) and 8..11 (head B): one thread per query row, online
+//    softmax in base 2 over the 64 scores of a tile, lazy rescaling of O (only
+//    when a row max grows by more than 2^8), P as bf16 pairs over the first
+//    32 columns of the S buffer; at the end of a unit O / l -> bf16 into the
+//    head's Q slot (no longer read) -> TMA store (full tiles) or row stores.
+// ===========================================================================
+constexpr int P2_BN = 64;                      // keys per KV tile
+constexpr int P2_KV_BYTES = P2_BN * D * 2;     // 16 KiB
+constexpr int P2_KV_HALF = P2_KV_BYTES / 2;    // [64 rows][64 dims]
+constexpr int P2_NTHREADS = 384;
+constexpr int P2_W_QLK = 0, P2_W_QK = 1, P2_W_V = 2, P2_W_PV = 3, P2_W_SOFT = 4;  // softmax warps 4..11
+constexpr int P2_QS = 4;  // Q slots: unit u uses 2 * (u & 1) (head A) and 2 * (u & 1) + 1 (head B)
+constexpr int P2_KS = 3, P2_VS = 3;
+constexpr int P2_OFF_Q = 0;
+constexpr int P2_OFF_K = P2_OFF_Q + P2_QS * TILE_BYTES;
+constexpr int P2_OFF_V = P2_OFF_K + P2_KS * P2_KV_BYTES;
+constexpr int P2_OFF_BAR = P2_OFF_V + P2_VS * P2_KV_BYTES;
+enum {
+    C_QFULL = 0, C_QEMPTY = C_QFULL + P2_QS, C_KFULL = C_QEMPTY + P2_QS, C_KEMPTY = C_KFULL + P2_KS,
+    C_VFULL = C_KEMPTY + P2_KS, C_VEMPTY = C_VFULL + P2_VS,
+    C_SFULL = C_VEMPTY + P2_VS /* [head][buffer] */, C_PFULL = C_SFULL + 4 /* [head][buffer] */,
+    C_PDONE = C_PFULL + 4 /* [head][buffer] */, C_OEMPTY = C_PDONE + 4 /* [head] */, C_DRAIN = C_OEMPTY + 2,
+    C_DRAIN2, C_SUFFIX /* [2] */, P2_NBAR = C_SUFFIX + 2
+};
+constexpr int P2_OFF_TMEM = P2_OFF_BAR + P2_NBAR * 8;
+constexpr int P2_OFF_FLAGS = P2_OFF_TMEM + 8;
+constexpr int P2_OFF_BID = P2_OFF_FLAGS + 16;         // block ids of the current unit, per loader warp
+constexpr int P2_OFF_SCHED = P2_OFF_BID + 2 * NBID * 4;
+constexpr int P2_SMEM_USED = P2_OFF_SCHED + SCHED_MAX * 2;
+constexpr size_t P2_SMEM_BYTES = P2_SMEM_USED + SMEM_SLACK;
+static_assert(P2_SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(SCHED_MAX * 8 <= P2_KS * P2_KV_BYTES, "the sort keys fit in the K ring");
+constexpr uint32_t P2_COL_S = 0, P2_COL_O = 256;  // S(h, b) at h * 128 + b * 64; O(h) at 256 + h * 128
+constexpr uint32_t P2_IDESC_S = idesc_bf16_f32(BM, P2_BN, false, false);
+
+template <bool STORE>
+__global__ void __launch_bounds__(P2_NTHREADS, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                        const PrefillArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+    if (pad > (uint32_t)SMEM_SLACK) {
+        if (threadIdx.x == 0) record_error(a.err, PA_DEV_SMEM_ALIGN, (long long)pad);
+        return;
+    }
+    uint8_t *smem = smem_raw + pad;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + P2_OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P2_OFF_TMEM);
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + P2_OFF_FLAGS);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nunits = a.mtiles * a.num_seqs * a.upg;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < P2_NBAR; ++i) {
+            const bool per_warp = (i >= C_PFULL && i < C_PFULL + 4) || i == C_OEMPTY || i == C_OEMPTY + 1;
+            mbar_init(&bar[i], per_warp ? 4u : 1u);  // the softmax warps of a head arrive one each
+        }
+        flags[0] = 0;
+        fence_mbar_init();
+    }
+    if (warp == P2_W_QK) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    uint16_t *sched = reinterpret_cast<uint16_t *>(smem + P2_OFF_SCHED);
+    int nsorted = 0;
+    if (a.sorted) {
+        // Rank the (query tile, sequence) groups by (KV tiles descending, group
+        // id ascending); the K ring holds the keys until the copies start.
+        const int ng = a.mtiles * a.num_seqs;
+        uint64_t *key = reinterpret_cast<uint64_t *>(smem + P2_OFF_K);
+        for (int g = threadIdx.x; g < ng; g += P2_NTHREADS) {
+            const int mt = a.mtiles - 1 - g / a.num_seqs, s = g % a.num_seqs;
+            const int n = group_tiles(a, mt, s);
+            key[g] = n > 0 ? ((uint64_t)n << 32) | (uint32_t)(0xffffffffu - (uint32_t)g) : 0ull;
+            if (n == 0 && mt == 0 && blockIdx.x == 0) {
+                const int Lq = __ldg(a.cu_q + s + 1) - __ldg(a.cu_q + s);
+                const int Lk = __ldg(a.cu_k + s + 1) - __ldg(a.cu_k + s);
+                if (Lq < 0 || Lk < Lq || (a.paged && Lk > a.max_blocks * a.block_size))
+                    record_error(a.err, PA_DEV_BAD_SEQLENS, s);
+            }
+        }
+        __syncthreads();
+        for (int g = threadIdx.x, first = 1; first || g < ng; g += P2_NTHREADS, first = 0) {
+            const uint64_t mine = g < ng ? key[g] : 0ull;
+            int rank = 0, nz = 0;
+            for (int j = 0; j < ng; ++j) {
+                const uint64_t kj = key[j];
+                rank += kj > mine;
+                nz += kj != 0ull;
+            }
+            if (first) nsorted = nz;
+            if (mine != 0ull) sched[rank] = (uint16_t)g;
+        }
+        fence_proxy_async_smem();
+    }
+    if (STORE) {
+        if (warp == 0 && !store_suffix(a, smem + P2_OFF_Q, P2_OFF_BAR - P2_OFF_Q, &bar[C_SUFFIX], lane) && lane == 0)
+            flags[0] = 1;
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncthreads();
+        if (threadIdx.x == 0 && !grid_barrier(a.gbar, gridDim.x)) {
+            record_error(a.err, PA_DEV_TIMEOUT, 440);
+            flags[0] = 1;
+        }
+        __syncthreads();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    nsorted *= a.upg;
+
+    // Every role walks the same units and the same KV-tile counter g, so the
+    // ring stages, S buffers and barrier phases agree.
+    if (STORE && flags[0]) {
+        // The grid barrier gave up: no role starts.
+    } else if (warp == P2_W_QLK || warp == P2_W_V) {
+        // ------------------------------------------------------------ TMA loads
+        const bool is_k = warp == P2_W_QLK;
+        const CUtensorMap *tm = is_k ? &tmk : &tmv;
+        const int off = is_k ? P2_OFF_K : P2_OFF_V;
+        uint64_t *full = &bar[is_k ? C_KFULL : C_VFULL];
+        uint64_t *empty = &bar[is_k ? C_KEMPTY : C_VEMPTY];
+        int *bid = reinterpret_cast<int *>(smem + P2_OFF_BID) + (is_k ? 0 : NBID);
+        if (lane == 0) {
+            if (is_k) prefetch_tensormap(&tmq);
+            prefetch_tensormap(tm);
+        }
+        const int R = a.box_rows;  // rows per box: gcd(block_size, 64)
+        uint32_t g = 0, u = 0, nq = 0;
+        bool ok = true;
+        for (int k = 0, t = cta_unit(a, nsorted, 0, 0, nunits, lane); ok && t < nunits;
+             ++k, t = cta_unit(a, nsorted, k, t, nunits, lane)) {
+            const Unit U = unit_of(a, sched, t);
+            const int32_t *bt = a.bt + (int64_t)U.s * a.max_blocks;
+            if (U.valid && a.paged) {
+                const int nblk = min((U.key_end - 1) / a.block_size + 1, NBID);
+                for (int b = lane; b < nblk; b += 32) bid[b] = __ldg(bt + b);
+            }
+            __syncwarp();
+            if (lane == 0 && U.valid) {
+                const int h0 = 2 * U.h, kvh = h0 / a.group;
+                if (is_k) {
+                    for (int x = 0; ok && x < 2; ++x) {
+                        const int qs = 2 * (u & 1) + x;
+                        ok = wait_or_abort(&bar[C_QEMPTY + qs], ((u >> 1) & 1u) ^ 1u, flags, a.err, 500);
+                        if (ok) {
+                            mbar_arrive_expect_tx(&bar[C_QFULL + qs], TILE_BYTES);
+                            tma_load_4d_plain(smem + P2_OFF_Q + qs * TILE_BYTES, &tmq, 0, U.q0 + U.m0, 0, h0 + x,
+                                              &bar[C_QFULL + qs]);
+                            ++nq;
+                        }
+                    }
+                }
+                for (int j = 0; ok && j < U.n_kv; ++j, ++g) {
+                    const int st = g % P2_KS;
+                    const int kb = j * P2_BN;
+                    const int nsub = (min(P2_BN, U.key_end - kb) + R - 1) / R;
+                    if (!(ok = wait_or_abort(&empty[st], ((g / P2_KS) & 1u) ^ 1u, flags, a.err, 501))) break;
+                    mbar_arrive_expect_tx(&full[st], (uint32_t)nsub * R * D * 2);
+                    uint8_t *dst = smem + off + st * P2_KV_BYTES;
+                    for (int sub = 0; sub < nsub; ++sub) {
+                        const int key = kb + sub * R;
+                        int row;
+                        if (a.paged) {
+                            const int lb = key / a.block_size;
+                            const int blk = lb < NBID ? bid[lb] : __ldg(bt + lb);
+                            if (a.checked && is_k && (blk < 0 || blk >= a.num_blocks))
+                                record_error(a.err, PA_DEV_BAD_BLOCK, (long long)U.s * a.max_blocks + lb);
+                            row = (blk < 0 || blk >= a.num_blocks) ? -2 * R : blk * a.block_size + key % a.block_size;
+                        } else {
+                            row = U.k0 + key;
+                        }
+                        if (a.box_halves == 2) {
+                            tma_load_4d_plain(dst, tm, 0, row, 0, kvh, &full[st]);
+                        } else {
+                            tma_load_4d_plain(dst + sub * R * 128, tm, 0, row, 0, kvh, &full[st]);
+                            tma_load_4d_plain(dst + P2_KV_HALF + sub * R * 128, tm, 0, row, 1, kvh, &full[st]);
+                        }
+                    }
+                }
+                ++u;
+            }
+            ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+        }
+        if (lane == 0 && !ok) {
+            // Let issued copies land before the CTA's shared memory is released.
+            for (uint32_t x = (nq >= (uint32_t)P2_QS ? nq - P2_QS : 0); is_k && x < nq; ++x) {
+                const uint32_t uu = x >> 1, qs = 2 * (uu & 1) + (x & 1);
+                (void)mbar_wait(&bar[C_QFULL + qs], (uu >> 1) & 1u);
+            }
+            for (uint32_t x = (g >= (uint32_t)P2_KS ? g - P2_KS : 0); x < g; ++x)
+                (void)mbar_wait(&full[x % P2_KS], (x / P2_KS) & 1u);
+        }
+    } else if (warp == P2_W_QK || warp == P2_W_PV) {
+        // ------------------------------------------------------------ MMA issuers (lane 0)
+        const bool is_qk = warp == P2_W_QK;
+        uint32_t g = 0, u = 0;
+        bool ok = true, issued = false;
+        for (int k = 0, t = cta_unit(a, nsorted, 0, 0, nunits, lane); ok && t < nunits;
+             ++k, t = cta_unit(a, nsorted, k, t, nunits, lane)) {
+            const Unit U = unit_of(a, sched, t);
+            if (!U.valid) continue;
+            if (lane == 0 && is_qk) {
+                uint64_t qdesc[2];
+                for (int x = 0; x < 2; ++x) {
+                    const int qs = 2 * (u & 1) + x;
+                    ok = ok && wait_or_abort(&bar[C_QFULL + qs], (u >> 1) & 1u, flags, a.err, 510);
+                    qdesc[x] = smem_desc_sw128(smem_addr(smem + P2_OFF_Q + qs * TILE_BYTES), 16, SBO);
+                }
+                for (int j = 0; ok && j < U.n_kv; ++j) {
+                    const uint32_t gg = g + j;
+                    const int ks = gg % P2_KS, b = gg & 1;
+                    if (!(ok = wait_or_abort(&bar[C_KFULL + ks], (gg / P2_KS) & 1u, flags, a.err, 511))) break;
+                    const uint64_t kdesc = smem_desc_sw128(smem_addr(smem + P2_OFF_K + ks * P2_KV_BYTES), 16, SBO);
+                    for (int x = 0; ok && x < 2; ++x) {
+                        // S(x, b) is free once the P.V that read it two tiles ago has completed.
+                        if (!(ok = wait_or_abort(&bar[C_PDONE + 2 * x + b], ((gg >> 1) & 1u) ^ 1u, flags, a.err,
+                                                 512)))
+                            break;
+                        tc_fence_after();
+                        const uint32_t d = tmem + P2_COL_S + x * 128 + b * 64;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t qo = (uint64_t)(((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4);
+                            const uint64_t ko = (uint64_t)(((kk >> 2) * P2_KV_HALF + (kk & 3) * 32) >> 4);
+                            mma_bf16_ss(d, qdesc[x] + qo, kdesc + ko, P2_IDESC_S, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bar[C_SFULL + 2 * x + b]);
+                        issued = true;
+                    }
+                    if (ok) mma_commit(&bar[C_KEMPTY + ks]);
+                }
+            } else if (lane == 0) {
+                for (int j = 0; ok && j < U.n_kv; ++j) {
+                    const uint32_t gg = g + j;
+                    const int vs = gg % P2_VS, b = gg & 1;
+                    if (!(ok = wait_or_abort(&bar[C_VFULL + vs], (gg / P2_VS) & 1u, flags, a.err, 520))) break;
+                    const int kend = min(P2_BN, U.key_end - j * P2_BN);  // keys of this tile that are needed
+                    const int kpad = (kend + 15) & ~15;
+                    const uint32_t vb = smem_addr(smem + P2_OFF_V + vs * P2_KV_BYTES);
+                    if (kend < kpad) {
+                        // Rows kend..kpad-1 are read by the last 16-key step: zero them
+                        // (stale or unloaded data; P is 0 there but 0 * NaN is not 0).
+                        for (int r = kend; r < kpad; ++r)
+                            for (int c = 0; c < 16; ++c)
+                                st_shared_v4(vb + (uint32_t)((c >> 3) * P2_KV_HALF + r * 128 + (((c & 7) ^ (r & 7)) << 4)),
+                                             0, 0, 0, 0);
+                        fence_proxy_async_smem();
+                    }
+                    const uint64_t vdesc = smem_desc_sw128(vb, P2_KV_HALF, SBO);
+                    for (int x = 0; ok && x < 2; ++x) {
+                        if (j == 0 && !(ok = wait_or_abort(&bar[C_OEMPTY + x], (u & 1u) ^ 1u, flags, a.err, 521)))
+                            break;
+                        if (!(ok = wait_or_abort(&bar[C_PFULL + 2 * x + b], (gg >> 1) & 1u, flags, a.err, 522))) break;
+                        tc_fence_after();
+                        const uint32_t pcol = tmem + P2_COL_S + x * 128 + b * 64;
+                        for (int kk = 0; kk < kpad / 16; ++kk)  // 16 keys per step = 8 TMEM columns of P
+                            mma_bf16_ts(tmem + P2_COL_O + x * 128, pcol + kk * 8,
+                                        vdesc + (uint64_t)((kk * 16 * 128) >> 4), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&bar[C_PDONE + 2 * x + b]);
+                        issued = true;
+                    }
+                    if (ok) mma_commit(&bar[C_VEMPTY + vs]);
+                }
+            }
+            g += U.n_kv;
+            ++u;
+            ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+        }
+        if (lane == 0 && !ok && issued) {
+            // Let the issued MMAs finish before TMEM is released.
+            uint64_t *dr = &bar[is_qk ? C_DRAIN : C_DRAIN2];
+            mma_commit(dr);
+            (void)mbar_wait(dr, 0);
+        }
+    } else if (warp >= P2_W_SOFT) {
+        // ------------------------------------------------------------ softmax, epilogue (one head each)
+        const int x = (warp - P2_W_SOFT) >> 2;  // 0: head A, 1: head B
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // tile row == TMEM lane
+        const int tid = threadIdx.x - (P2_W_SOFT + 4 * x) * 32;  // 0..127
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t col_s = P2_COL_S + x * 128, col_o = P2_COL_O + x * 128;
+        const float sl = a.scale_log2;
+        uint32_t g = 0, u = 0;
+        bool ok = true;
+        auto wwait = [&](uint64_t *b, uint32_t parity, int where) -> bool {
+            return __all_sync(FULL, wait_or_abort(b, parity, flags, a.err, where));
+        };
+        int pend_q = -1;  // Q slot whose output store still has to be read out (tid 0)
+        for (int k = 0, t = cta_unit(a, nsorted, 0, 0, nunits, lane); ok && t < nunits;
+             ++k, t = cta_unit(a, nsorted, k, t, nunits, lane)) {
+            const Unit U = unit_of(a, sched, t);
+            if (!U.valid) continue;
+            const int i = U.m0 + row;  // query index in the sequence (>= Lq: padding row)
+            const int pos = (U.Lk - U.Lq) + i;
+            const int key_last = (a.causal ? min(pos, U.Lk - 1) : U.Lk - 1);
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < U.n_kv; ++j) {
+                const uint32_t gg = g + j;
+                const int b = gg & 1;
+                const uint32_t cs = t_lane + col_s + b * 64;
+                if (!(ok = wwait(&bar[C_SFULL + 2 * x + b], (gg >> 1) & 1u, 530))) break;
+                tc_fence_after();
+                uint32_t r[64];
+                tmem_ld32(cs, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                tmem_ld32(cs + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                tmem_ld_wait();
+                const int lim = key_last - j * P2_BN;  // keys j*64 + kk with kk <= lim are visible
+                if (__any_sync(FULL, lim < P2_BN - 1)) {
+#pragma unroll
+                    for (int kk = 0; kk < P2_BN; ++kk)
+                        if (kk > lim) r[kk] = __float_as_uint(-INFINITY);
+                }
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int k2 = 0; k2 < P2_BN / 2; ++k2)
+                    m4[k2 & 3] = max3f(m4[k2 & 3], __uint_as_float(r[2 * k2]), __uint_as_float(r[2 * k2 + 1]));
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                const bool grow = (mx - m_run) * sl > 8.f;
+                const float m_new = grow ? mx : m_run;
+                const float alpha = grow ? fast_exp2((m_run - m_new) * sl) : 1.f;
+                if (j > 0 && __any_sync(FULL, grow)) {
+                    // O must hold P.V up to tile gg-1 before it is rescaled (the one
+                    // before that has completed: the Q.K that wrote this S waited for it).
+                    if (!(ok = wwait(&bar[C_PDONE + 2 * x + ((gg - 1) & 1)], ((gg - 1) >> 1) & 1u, 531))) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(t_lane + col_o + c * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(t_lane + col_o + c * 32, o);
+                    }
+                }
+                l_run *= alpha;
+                m_run = m_new;
+                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run * sl;
+                float2 rs[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+                const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(neg_m, neg_m);
+                uint32_t pk[32];
+#pragma unroll
+                for (int k2 = 0; k2 < 32; ++k2) {
+                    const float2 xx =
+                        fma2(make_float2(__uint_as_float(r[2 * k2]), __uint_as_float(r[2 * k2 + 1])), sl2, nm2);
+                    const float2 pp = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
+                    rs[k2 & 3] = add2(rs[k2 & 3], pp);
+                    pk[k2] = pack_bf16(pp.x, pp.y);
+                }
+                tmem_st32(cs, pk);
+                tmem_st_wait();
+                l_run += ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y)) + ((rs[2].x + rs[2].y) + (rs[3].x + rs[3].y));
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[C_PFULL + 2 * x + b]);
+                if (tid == 0 && pend_q >= 0) {
+                    // The previous unit's output store has read its staging slot by now.
+                    bulk_wait_read0();
+                    mbar_arrive(&bar[C_QEMPTY + pend_q]);
+                    pend_q = -1;
+                }
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l -> bf16 tile in this head's Q slot -> global memory
+            const uint32_t gl = g + U.n_kv - 1;  // the unit's last tile
+            if (!(ok = wwait(&bar[C_PDONE + 2 * x + (gl & 1)], (gl >> 1) & 1u, 532))) break;
+            tc_fence_after();
+            uint32_t o[128];
+            tmem_ld32(t_lane + col_o, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+            tmem_ld32(t_lane + col_o + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+            tmem_ld32(t_lane + col_o + 64, *reinterpret_cast<uint32_t(*)[32]>(&o[64]));
+            tmem_ld32(t_lane + col_o + 96, *reinterpret_cast<uint32_t(*)[32]>(&o[96]));
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[C_OEMPTY + x]);  // O may be overwritten by the next unit
+            const int qs = 2 * (u & 1) + x;
+            const uint32_t os = smem_addr(smem + P2_OFF_Q + qs * TILE_BYTES);
+            const float inv = 1.f / l_run;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const uint32_t *v = &o[8 * c];
+                st_shared_v4(os + sw128_off(row, c),
+                             pack_bf16(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                             pack_bf16(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                             pack_bf16(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                             pack_bf16(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+            }
+            const int head = 2 * U.h + x;
+            const int nrows = min(BM, U.Lq - U.m0);
+            if (nrows == BM) {
+                fence_proxy_async_smem();
+                named_bar_sync(1 + x, 128);
+                if (tid == 0) {
+                    tma_store_4d(&tmo, smem + P2_OFF_Q + qs * TILE_BYTES, 0, U.q0 + U.m0, 0, head);
+                    bulk_commit_group();
+                    pend_q = qs;
+                }
+            } else {
+                named_bar_sync(1 + x, 128);
+#pragma unroll 4
+                for (int it = 0; it < BM * 16 / 128; ++it) {
+                    const int q = it * 128 + tid, rr = q >> 4, c = q & 15;
+                    if (rr < nrows) {
+                        const uint4 v = ld_shared_v4(os + sw128_off(rr, c));
+                        *reinterpret_cast<uint4 *>(a.out + ((int64_t)(U.q0 + U.m0 + rr) * a.Hq + head) * D + c * 8) = v;
+                    }
+                }
+                fence_proxy_async_smem();  // the slot's next Q arrives by TMA (async proxy)
+                named_bar_sync(1 + x, 128);
+                if (tid == 0) pend_q = qs;
+            }
+            g += U.n_kv;
+            ++u;
+        }
+        if (tid == 0 && pend_q >= 0) {
+            bulk_wait_read0();
+            mbar_arrive(&bar[C_QEMPTY + pend_q]);
+        }
+        if (tid == 0) bulk_wait0();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == P2_W_QK) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
 // Per (device, instantiation): the shared-memory attribute has been set
 // (an atomic flag; concurrent first calls may both set the idempotent attribute).
-std::atomic<int> g_attr_done[64][2];
+std::atomic<int> g_attr_done[64][4];
 
 // The fused store's inputs (null: plain prefill).
 struct SuffixStore {
@@ -849,7 +1305,12 @@ pa_status prefill_impl(void *out, const void *q, int64_t q_row_stride, int32_t t
     if (((int64_t)max_seqlen_q + BM - 1) / BM * num_seqs * num_q_heads > 0x7fffffffLL)
         return fail(PA_ERR_UNSUPPORTED, "too many tiles");
     const bool paged = block_tables != nullptr;
-    int R = BN;
+    // Even GQA groups run the paired-head kernel (two q heads of one kv head
+    // per unit, 64-key tiles); other groups the one-head kernel (128-key tiles).
+    const int group = num_q_heads / num_kv_heads;
+    const bool paired = group % 2 == 0;
+    const int tile_keys = paired ? P2_BN : BN;
+    int R = tile_keys;
     if (paged) {
         if (block_size <= 0 || block_size % 16)
             return fail(PA_ERR_UNSUPPORTED, "block_size %d (must be a positive multiple of 16)", block_size);
@@ -858,15 +1319,15 @@ pa_status prefill_impl(void *out, const void *q, int64_t q_row_stride, int32_t t
         if ((int64_t)num_blocks * block_size > 0x7fffffffLL ||
             (int64_t)max_blocks_per_seq * block_size > 0x7fffffffLL)
             return fail(PA_ERR_UNSUPPORTED, "pool or table too large for 32-bit slot indices");
-        while (block_size % R) R >>= 1;  // gcd(block_size, 128) in {16, 32, 64, 128}
+        while (block_size % R) R >>= 1;  // gcd(block_size, tile_keys) in {16, 32, 64(, 128)}
     } else {
         if (total_k <= 0) return fail(PA_ERR_INVALID_ARG, "total_k must be positive for contiguous k/v");
         if (kv_row_stride < (int64_t)num_kv_heads * D || kv_row_stride % 8)
             return fail(PA_ERR_INVALID_ARG, "kv_row_stride must be >= num_kv_heads*head_dim and a multiple of 8");
     }
-    // A box of BN rows holds a whole K/V tile in [half][row][64] order;
+    // A box of tile_keys rows holds a whole K/V tile in [half][row][64] order;
     // shorter boxes (small blocks) are fetched one 64-dim half at a time.
-    const int halves = R == BN ? 2 : 1;
+    const int halves = R == tile_keys ? 2 : 1;
     CUtensorMap tq, tk, tv;
     pa_status st = encode_halves_map(&tq, q, total_q, q_row_stride * 2, num_q_heads, BM, 2);
     if (st != PA_OK) return st;
@@ -887,8 +1348,10 @@ pa_status prefill_impl(void *out, const void *q, int64_t q_row_stride, int32_t t
     A.max_blocks = paged ? max_blocks_per_seq : 0;
     A.num_seqs = num_seqs;
     A.Hq = num_q_heads;
-    A.group = num_q_heads / num_kv_heads;
+    A.group = group;
     A.mtiles = (max_seqlen_q + BM - 1) / BM;
+    A.upg = paired ? num_q_heads / 2 : num_q_heads;
+    A.bn = tile_keys;
     A.block_size = paged ? block_size : 1;
     A.box_rows = R;
     A.box_halves = halves;
@@ -909,39 +1372,40 @@ pa_status prefill_impl(void *out, const void *q, int64_t q_row_stride, int32_t t
     A.total_q = total_q;
     A.gbar = store ? store->gbar : nullptr;
 
-    const int64_t ntiles = (int64_t)A.mtiles * num_seqs * num_q_heads;
+    const int64_t nunits = (int64_t)A.mtiles * num_seqs * A.upg;
     const int sms = sm_count();
     if (sms <= 0) return fail(PA_ERR_CUDA, "no CUDA device");
-    const int64_t grid = std::min<int64_t>(ntiles, sms);  // persistent: one CTA per SM
+    const int64_t grid = std::min<int64_t>(nunits, sms);  // persistent: one CTA per SM
     int dev = 0;
     cudaGetDevice(&dev);
-    const int fi = store ? 1 : 0;
+    using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillArgs);
+    const KernelFn kern = paired ? (store ? prefill_pair_kernel<true> : prefill_pair_kernel<false>)
+                                 : (store ? prefill_kernel<true> : prefill_kernel<false>);
+    const size_t smem_bytes = paired ? P2_SMEM_BYTES : SMEM_BYTES;
+    const int threads = paired ? P2_NTHREADS : NTHREADS;
+    const int fi = (store ? 1 : 0) + (paired ? 2 : 0);
     if (dev >= 0 && dev < 64 && !g_attr_done[dev][fi].load(std::memory_order_acquire)) {
-        cudaError_t e = store ? cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)SMEM_BYTES)
-                              : cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_kernel)");
         g_attr_done[dev][fi].store(1, std::memory_order_release);
     }
     if (!store) {
-        prefill_kernel<false><<<(unsigned)grid, NTHREADS, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
-            tq, tk, tv, to, A);
+        kern<<<(unsigned)grid, threads, smem_bytes, reinterpret_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, A);
         return check_launch("prefill_kernel");
     }
     // The fused store's CTAs wait on one another at the grid barrier: a
     // cooperative launch guarantees they are resident together (one per SM).
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(NTHREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_kernel<true>, tq, tk, tv, to, A);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, to, A);
     if (e != cudaSuccess) return cuda_fail(e, "prefill_kernel (cooperative)");
     return check_launch("prefill_kernel");
 }
