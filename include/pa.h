@@ -224,6 +224,44 @@ PA_API pa_status pa_decode_store(void *out, const void *q, int64_t q_row_stride,
                                  size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_decode_shared_prefix -- pa_decode / pa_decode_store for batches in which
+ * sequences share prefix-cache blocks.  [NV12 §12.8 BlockManager prefix
+ * caching: sequences whose prompts begin with the same full blocks hold the
+ * same physical blocks (ref_count > 1); NV12 §12.6 flash_attn_with_kvcache]
+ *
+ * Same result as pa_decode (new_k == new_v == NULL) or pa_decode_store (both
+ * given, same layout and contract), within the attention tolerance: only the
+ * summation order differs.  Sequences are grouped on the device by the id of
+ * their first block; a group's shared prefix is the longest run of leading
+ * block ids all its members agree on, limited for each member to the full
+ * blocks before the one holding its newest token.  For groups of two or more
+ * sequences a first kernel attends every member's query heads to the shared
+ * prefix once per kv head (each of its K/V rows is read once, not once per
+ * member) and leaves fp32 (m, l, o) partials in the workspace; the decode
+ * kernel then streams only each member's own suffix and merges the prefix
+ * partial into the member's result (log-sum-exp).  Batches without sharing
+ * pay for the grouping pass and one extra launch; prefer pa_decode there.
+ *
+ *   workspace   >= pa_decode_shared_prefix_workspace_size(...) bytes (the
+ *               pa_decode workspace plus the groups and the prefix partials
+ *               of up to 8192 (member, q head) rows: ~8.6 MB more), same
+ *               zero-filling contract as pa_decode.  Members beyond
+ *               8192 / num_q_heads (in batch order) read the shared prefix
+ *               themselves.
+ *   batch       <= 1024.
+ * Every other argument, the ordering and the error behaviour are those of
+ * pa_decode / pa_decode_store.
+ */
+PA_API size_t pa_decode_shared_prefix_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim);
+PA_API pa_status pa_decode_shared_prefix(void *out, const void *q, int64_t q_row_stride, const void *new_k,
+                                         int64_t new_k_row_stride, const void *new_v, int64_t new_v_row_stride,
+                                         void *k_cache, void *v_cache, const int32_t *block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
+                                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t block_size, int32_t num_blocks, float softmax_scale, void *workspace,
+                                         size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_decode_static -- pa_decode for callers that cannot allocate device memory.
  * (An addition of this library: the source pages have no counterpart.)
  *

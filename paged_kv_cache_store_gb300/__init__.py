@@ -43,6 +43,9 @@ SIGNATURES = {
     "pa_decode_static": (C.c_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                    _i32, _f32, _vp]),
     "pa_decode_static_scratch": (C.c_int, [C.POINTER(_vp), C.POINTER(_sz)]),
+    "pa_decode_shared_prefix_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "pa_decode_shared_prefix": (C.c_int, [_vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
+                                          _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]),
     "pa_decode_store": (C.c_int, [_vp, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
                                   _i32, _i32, _i32, _i32, _f32, _vp, _sz, _vp]),
     "pa_prefill_varlen": (C.c_int, [_vp, _vp, _i64, _i32, _vp, _vp, _i64, _i32, _vp, _i32, _vp, _vp, _i32,
@@ -193,21 +196,25 @@ def decode_workspace_size(num_q_heads, num_kv_heads, head_dim) -> int:
     return int(lib().pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim))
 
 
-def decode_workspace(num_q_heads, num_kv_heads, head_dim, device="cuda"):
+def decode_workspace(num_q_heads, num_kv_heads, head_dim, device="cuda", shared_prefix=False):
     """Allocate (with torch) a zero-filled workspace for pa_decode (at most
-    about 6.4 MB; it depends only on the GQA group).  pa_decode leaves it
+    about 6.4 MB; it depends only on the GQA group), or, with shared_prefix,
+    for pa_decode_shared_prefix (about 8.6 MB more).  The calls leave it
     zeroed, so it can be reused by any number of calls on one stream."""
-    n = decode_workspace_size(num_q_heads, num_kv_heads, head_dim)
+    n = (int(lib().pa_decode_shared_prefix_workspace_size(num_q_heads, num_kv_heads, head_dim)) if shared_prefix
+         else decode_workspace_size(num_q_heads, num_kv_heads, head_dim))
     return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, workspace=None, out=None,
-           stream=None, new_k=None, new_v=None):
+           stream=None, new_k=None, new_v=None, shared_prefix=False):
     """Paged decode attention.  q [batch, Hq, D] bf16 (rows may be strided);
     caches [num_blocks, B, Hkv, D]; block_tables int32 [batch, max_blocks];
     context_lens int32 [batch].  Returns out [batch, Hq, D] bf16.  With
     new_k / new_v ([batch, Hkv, D] bf16, rows may be strided) the kernel first
-    stores them at position context_lens-1 (pa_decode_store)."""
+    stores them at position context_lens-1 (pa_decode_store).  With
+    shared_prefix, sequences that share leading blocks read them once
+    (pa_decode_shared_prefix; its workspace is larger)."""
     _need(q, torch.bfloat16, "q")
     _need(k_cache, torch.bfloat16, "k_cache")
     _need(v_cache, torch.bfloat16, "v_cache")
@@ -221,9 +228,21 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, softmax_scale=None, 
         softmax_scale = 1.0 / math.sqrt(d)
     mb = block_tables.shape[1]
     if workspace is None:
-        workspace = decode_workspace(hq, hkv, d, q.device)
+        workspace = decode_workspace(hq, hkv, d, q.device, shared_prefix=shared_prefix)
     if out is None:
         out = torch.empty(batch, hq, d, dtype=torch.bfloat16, device=q.device)
+    if shared_prefix:
+        if new_k is not None or new_v is not None:
+            _need(new_k, torch.bfloat16, "new_k")
+            _need(new_v, torch.bfloat16, "new_v")
+        nk_args = ((_ptr(new_k), _row_stride(new_k, "new_k"), _ptr(new_v), _row_stride(new_v, "new_v"))
+                   if new_k is not None else (None, 0, None, 0))
+        _check(lib().pa_decode_shared_prefix(_ptr(out), _ptr(q), _row_stride(q, "q"), *nk_args, _ptr(k_cache),
+                                             _ptr(v_cache), _ptr(block_tables), mb, _ptr(context_lens), batch, hq, hkv,
+                                             d, B, nb, float(softmax_scale), _ptr(workspace), workspace.numel(),
+                                             _stream(stream)),
+               "pa_decode_shared_prefix")
+        return out
     if new_k is not None or new_v is not None:
         _need(new_k, torch.bfloat16, "new_k")
         _need(new_v, torch.bfloat16, "new_v")

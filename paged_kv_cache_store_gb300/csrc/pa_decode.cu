@@ -66,6 +66,9 @@ constexpr int WPG = 4;            // consumer warps per group
 constexpr int KPW = TILE / WPG;   // keys per consumer warp per tile (one MMA n-pair)
 constexpr float kLazyRescale = 8.f;  // log2 headroom before the running max must move
 constexpr int kMaxBatch = 2048;
+constexpr int kMaxBatchCascade = 1024;   // pa_decode_shared_prefix
+constexpr int kMaxPrefixRows = 8192;     // (member, q head) rows with prefix partials in a workspace
+constexpr int kPrefixSplits = 2;         // the shared prefix's tiles are cut in this many parts
 constexpr int kMaxGrid = 256;     // CTAs of the persistent grid (min(SMs, this))
 constexpr int kMaxRanges = 2 * kMaxGrid;  // a head and a tail range per CTA
 constexpr int kTailShift = 3;  // a CTA's tail range is 1/8 of its share
@@ -111,8 +114,15 @@ struct Cfg {
     static constexpr int OFF_ZERO = OFF_SIDE + 2 * NCW * ROW_BYTES;
     static constexpr int OFF_CUM = OFF_ZERO + ROW_BYTES;   // per-head tile prefix sum [batch + 1] uint32
     __host__ __device__ static constexpr size_t off_ctx(int batch) { return OFF_CUM + 4 * (size_t)(batch + 1); }  // [batch] int
-    __host__ __device__ static constexpr size_t smem_bytes(int batch) { return off_ctx(batch) + 4 * (size_t)batch + 1024; }
+    // With shared prefixes: per sequence its first streamed position and its
+    // prefix-partial entry ([batch] int each).
+    __host__ __device__ static constexpr size_t off_ps(int batch) { return off_ctx(batch) + 4 * (size_t)batch; }
+    __host__ __device__ static constexpr size_t off_pe(int batch) { return off_ps(batch) + 4 * (size_t)batch; }
+    __host__ __device__ static constexpr size_t smem_bytes(int batch, bool cascade = false) {
+        return (cascade ? off_pe(batch) + 4 * (size_t)batch : off_ps(batch)) + 1024;
+    }
     static_assert(smem_bytes(kMaxBatch) <= 232448, "shared memory budget");
+    static_assert(smem_bytes(kMaxBatchCascade, true) <= 232448, "shared memory budget (shared prefixes)");
 };
 
 struct DecodeArgs {
@@ -137,6 +147,16 @@ struct DecodeArgs {
     const uint2 *new_k, *new_v;  // null: plain decode
     int64_t new_k_stride, new_v_stride;  // in 8-byte units
     uint2 *k_cache, *v_cache;
+    // Shared prefixes (pa_decode_shared_prefix): sequences whose leading full
+    // blocks are the same physical blocks stream only their own suffix; the
+    // attention over the shared prefix was computed for all of them by the
+    // prefix kernel, whose (m, l, o) partial per (member, q head) the merge
+    // folds in.
+    int32_t cascade;
+    int32_t max_prefix_seqs;  // members that get a prefix partial (entries in pfx_*)
+    const float *pfx_o;       // [kPrefixSplits][kMaxPrefixRows][D]
+    const float2 *pfx_ml;     // [kPrefixSplits][kMaxPrefixRows]  (m, l) in base 2
+    int *grp;                 // [2][kMaxBatchCascade]: ps and pe of every sequence, written by the prefix kernel
 };
 
 __device__ __forceinline__ int clamp_ctx(const DecodeArgs &a, int b, bool report) {
@@ -192,6 +212,7 @@ struct Ticket {
 // One (sequence, kv head) part of a range.
 struct Seg {
     int b, g, t_begin, t_end, nt, p_begin, p_end;
+    int p0;         // position of the pair's tile 0 (after a shared prefix; 0 otherwise)
     long long pos;  // flat index of tile t_begin
 };
 
@@ -200,19 +221,22 @@ struct Seg {
 struct Walker {
     int b, g, t;
     long long pos, left;
-    __device__ explicit Walker(const Ticket &k) : b(k.b), g(k.g), t(k.t), pos(k.pos), left(k.len) {}
+    const int *ps_s;  // per-sequence first streamed position (null: all 0)
+    __device__ Walker(const Ticket &k, const int *ps) : b(k.b), g(k.g), t(k.t), pos(k.pos), left(k.len), ps_s(ps) {}
     __device__ bool next(const int *ctx_s, int Hkv, int batch, Seg &s) {
         if (left <= 0) return false;
         const int ctx = ctx_s[b];
-        const int nt = (ctx + TILE - 1) / TILE;
+        const int p0 = ps_s ? ps_s[b] : 0;
+        const int nt = (ctx - p0 + TILE - 1) / TILE;
         const int take = (int)min((long long)(nt - t), left);
         s.b = b;
         s.g = g;
         s.t_begin = t;
         s.t_end = t + take;
         s.nt = nt;
-        s.p_begin = t * TILE;
-        s.p_end = min(ctx, s.t_end * TILE);
+        s.p0 = p0;
+        s.p_begin = p0 + t * TILE;
+        s.p_end = min(ctx, p0 + s.t_end * TILE);
         s.pos = pos;
         left -= take;
         pos += take;
@@ -224,6 +248,121 @@ struct Walker {
         return true;
     }
 };
+
+// Shared prefixes [NV12 §12.8 prefix caching: sequences whose prompts begin
+// with the same full blocks hold the same physical blocks, ref_count > 1].
+// Sequence b may share its first nfull_b = (ctx_b - 1) / B blocks (every block
+// before the one holding its newest token).  Sequences are grouped by the id
+// of their first block; the group's leader is its lowest sequence index, and
+// its shared length is the longest run of leading block ids on which every
+// member agrees with the leader, capped by every member's nfull.  Members of
+// groups with two or more sequences and a shared length of at least one block
+// get ps[b] = shared blocks * B (the first position they stream themselves)
+// and a dense entry index pe[b] (batch order, below max_prefix_seqs); every
+// other sequence gets ps = 0, pe = -1.  lead[b] is the leader (or -1) and
+// nmem[L] the number of leader L's members that have an entry.
+// Every thread of the CTA calls it (it synchronises the CTA).  Scratch:
+// (2 * H + batch) ints, H = the smallest power of two >= 2 * batch; lead and
+// nmem are [batch] ints outside the scratch.  The result depends only on the
+// inputs, not on timing: every CTA and kernel that runs it agrees.
+__device__ void find_prefix_groups(int batch, const int32_t *bt, int max_blocks, int block_size,
+                                   int max_prefix_seqs, const int *ctx_s, int *ps_s, int *pe_s, int *lead,
+                                   int *nmem, int *scr, uint32_t *wsum) {
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    int H = 64;
+    while (H < 2 * batch) H <<= 1;
+    int *hkey = scr, *hmin = scr + H, *pmin = scr + 2 * H;  // hash: first block id -> lowest sequence
+    for (int i = tid; i < H; i += nthr) {
+        hkey[i] = -1;
+        hmin[i] = 0x7fffffff;
+    }
+    for (int b = tid; b < batch; b += nthr) {
+        pmin[b] = 0x7fffffff;
+        nmem[b] = 0;
+    }
+    __syncthreads();
+    for (int b = tid; b < batch; b += nthr) {
+        const int nfull = ctx_s[b] > 0 ? (ctx_s[b] - 1) / block_size : 0;
+        const int key = nfull >= 1 ? __ldg(bt + (int64_t)b * max_blocks) : -1;
+        lead[b] = -1;
+        if (key < 0) continue;  // nothing to share, or a padding id
+        uint32_t slot = ((uint32_t)key * 2654435761u) & (uint32_t)(H - 1);
+        for (int probe = 0; probe < H; ++probe) {
+            const int k = atomicCAS(&hkey[slot], -1, key);
+            if (k == -1 || k == key) {
+                atomicMin(&hmin[slot], b);
+                lead[b] = (int)slot;  // the slot for now; the leader after the next step
+                break;
+            }
+            slot = (slot + 1) & (uint32_t)(H - 1);
+        }
+    }
+    __syncthreads();
+    for (int b = tid; b < batch; b += nthr) {
+        if (lead[b] < 0) continue;
+        const int L = hmin[lead[b]];
+        const int nb = (ctx_s[b] - 1) / block_size, nl = (ctx_s[L] - 1) / block_size;
+        int j = min(nb, nl);
+        if (b != L) {
+            // Block 0 agrees by construction; compare four ids per round (loads in flight together).
+            const int n = j;
+            const int32_t *tb = bt + (int64_t)b * max_blocks, *tl = bt + (int64_t)L * max_blocks;
+            for (j = 1; j < n; j += 4) {
+                int d = 4;
+#pragma unroll
+                for (int u = 3; u >= 0; --u)
+                    if (j + u < n && __ldg(tb + j + u) != __ldg(tl + j + u)) d = u;
+                if (d < 4) {
+                    j += d;
+                    break;
+                }
+            }
+            j = min(j, n);
+        }
+        lead[b] = L;
+        atomicMin(&pmin[L], j);
+    }
+    __syncthreads();
+    // Membership needs the group's size: count the sequences per leader.
+    for (int b = tid; b < batch; b += nthr)
+        if (lead[b] >= 0) atomicAdd(&nmem[lead[b]], 1);
+    __syncthreads();
+    // Dense entries in batch order: a block-wide exclusive scan of the member flags.
+    const int per = (batch + nthr - 1) / nthr;
+    const int b0 = tid * per, b1 = min(batch, b0 + per);
+    auto member = [&](int b) -> bool {
+        const int L = lead[b];
+        return L >= 0 && nmem[L] >= 2 && pmin[L] >= 1;
+    };
+    uint32_t run = 0;
+    for (int b = b0; b < b1; ++b) run += member(b) ? 1u : 0u;
+    uint32_t x = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int w2 = 0; w2 < warp; ++w2) before += wsum[w2];
+    uint32_t e = before + x - run;
+    __syncthreads();
+    for (int b = b0; b < b1; ++b) {
+        const bool m = member(b) && (int)e < max_prefix_seqs;
+        e += member(b) ? 1u : 0u;
+        ps_s[b] = m ? pmin[lead[b]] * block_size : 0;
+        pe_s[b] = m ? (int)(e - 1) : -1;
+    }
+    __syncthreads();
+    // Entries per leader (the members the prefix kernel computes).
+    for (int b = tid; b < batch; b += nthr) nmem[b] = 0;
+    __syncthreads();
+    for (int b = tid; b < batch; b += nthr)
+        if (pe_s[b] >= 0) atomicAdd(&nmem[lead[b]], 1);
+    fence_proxy_async_smem();  // the scratch is ring memory that TMA writes next
+    __syncthreads();
+}
 
 // D += A.B for one m16n8k16 tile: A 16x16 bf16 (row-major fragments),
 // B 16x8 bf16 (column fragments), D 16x8 fp32.
@@ -290,6 +429,8 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint32_t *cum = reinterpret_cast<uint32_t *>(smem + C::OFF_CUM);
     int *ctx_s = reinterpret_cast<int *>(smem + C::off_ctx(a.batch));
+    int *ps_s = a.cascade ? reinterpret_cast<int *>(smem + C::off_ps(a.batch)) : nullptr;
+    int *pe_s = a.cascade ? reinterpret_cast<int *>(smem + C::off_pe(a.batch)) : nullptr;
     uint32_t *wsum = reinterpret_cast<uint32_t *>(smem + C::OFF_WSUM);
     Ticket *tks = reinterpret_cast<Ticket *>(smem + C::OFF_TK);
     uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
@@ -334,12 +475,21 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     {
         const int per = (a.batch + C::NTHREADS - 1) / C::NTHREADS;
         const int b0 = threadIdx.x * per, b1 = min(a.batch, b0 + per);
-        uint32_t run = 0;
         for (int b = b0; b < b1; ++b) {
-            const int ctx = clamp_ctx(a, b, blockIdx.x == 0);
-            ctx_s[b] = ctx;
-            run += (uint32_t)((ctx + TILE - 1) / TILE);
+            ctx_s[b] = clamp_ctx(a, b, blockIdx.x == 0);
+            if (a.cascade) {
+                // Shared prefixes: the groups the prefix kernel found (it completed
+                // before griddepcontrol.wait returned).
+                ps_s[b] = __ldcg(a.grp + b);
+                pe_s[b] = __ldcg(a.grp + kMaxBatchCascade + b);
+            }
         }
+        // Tiles of each sequence: its context after the shared prefix.
+        auto ntiles = [&](int b) -> uint32_t {
+            return (uint32_t)((ctx_s[b] - (ps_s ? ps_s[b] : 0) + TILE - 1) / TILE);
+        };
+        uint32_t run = 0;
+        for (int b = b0; b < b1; ++b) run += ntiles(b);
         uint32_t x = run;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -353,7 +503,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
         uint32_t excl = before + x - run;
         for (int b = b0; b < b1; ++b) {
             cum[b] = excl;
-            excl += (uint32_t)((ctx_s[b] + TILE - 1) / TILE);
+            excl += ntiles(b);
         }
         if (threadIdx.x == C::NTHREADS - 1) cum[a.batch] = before + x;
     }
@@ -456,7 +606,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                 const int nblk = (s.p_end - 1) / a.block_size + 1;  // logical blocks of the sequence in use
                 return lb + lane < nblk ? __ldg(a.block_tables + (int64_t)s.b * a.max_blocks + lb + lane) : -1;
             };
-            Walker w(tk);
+            Walker w(tk, ps_s);
             int range_left = tk.len;  // tiles of this range not yet issued
             Seg cur, nxt;
             bool have = w.next(ctx_s, a.Hkv, a.batch, cur);
@@ -490,7 +640,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                         taken = true;
                     }
                     --range_left;
-                    const int p0 = t * TILE;
+                    const int p0 = cur.p0 + t * TILE;
                     const int rows = min(TILE, cur.p_end - p0);
                     const int nsub = (rows + a.box_rows - 1) / a.box_rows;
                     if (lane == 0) mbar_arrive_expect_tx(&fullb[stage], (uint32_t)nsub * a.box_rows * ROW_BYTES);
@@ -554,7 +704,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
         uint32_t k = 0, ti = 0;
         Ticket tk;
         while (take_ticket(ti++, tk)) {
-            Walker w(tk);
+            Walker w(tk, ps_s);
             Seg sg;
             for (int si = 0; w.next(ctx_s, a.Hkv, a.batch, sg); ++si, ++k) {
                 const bool ok = wait_or_abort(&done[k % C::NSLOT], (k / C::NSLOT) & 1, flags, a, 300);
@@ -581,6 +731,28 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sfree[k % C::NSLOT]);
+                if (pe_s && sg.t_begin == 0 && pe_s[sg.b] >= 0) {
+                    // The pair's first part also carries the attention over the
+                    // shared prefix, computed for all members by the prefix kernel.
+                    const int64_t row0 = (int64_t)pe_s[sg.b] * a.Hq + (int64_t)sg.g * G;
+#pragma unroll
+                    for (int sp2 = 0; sp2 < kPrefixSplits; ++sp2)
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const int64_t row = (int64_t)sp2 * kMaxPrefixRows + row0 + h;
+                        const float2 ml = __ldcg(a.pfx_ml + row);
+                        const float4 po = __ldcg(reinterpret_cast<const float4 *>(a.pfx_o + row * D) + lane);
+                        const float mn = fmaxf(M[h], ml.x);
+                        const float f0 = M[h] == -INFINITY ? 0.f : fast_exp2(M[h] - mn);
+                        const float f1 = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - mn);
+                        L[h] = fmaf(L[h], f0, ml.y * f1);
+                        O[h][0] = fmaf(O[h][0], f0, po.x * f1);
+                        O[h][1] = fmaf(O[h][1], f0, po.y * f1);
+                        O[h][2] = fmaf(O[h][2], f0, po.z * f1);
+                        O[h][3] = fmaf(O[h][3], f0, po.w * f1);
+                        M[h] = mn;
+                    }
+                }
                 const int64_t bh0 = (int64_t)sg.b * a.Hq + (int64_t)sg.g * G;  // first q-head row of (b, g)
                 if (sg.t_begin == 0 && sg.t_end == sg.nt) {  // the whole pair: final output
                     if (!ok) continue;
@@ -731,7 +903,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     uint32_t nt_mine = 0, k = 0, ti = 0;  // tiles of this warp's group, segments, tickets
     Ticket tk;
     while (take_ticket(ti++, tk)) {
-        Walker w(tk);
+        Walker w(tk, ps_s);
         Seg sg;
         for (; w.next(ctx_s, a.Hkv, a.batch, sg); ++k) {
             if (wait_or_abort(&qfull[k & 1], (k >> 1) & 1, flags, a, 200 + warp)) {
@@ -754,7 +926,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
             long long st_slot = 0;
             uint2 st_k = make_uint2(0, 0), st_v = make_uint2(0, 0);
             if (STORE && sg.t_end == sg.nt) {
-                const int pn = sg.p_end - 1, tn = pn / TILE, kn = pn % TILE;
+                const int pn = sg.p_end - 1, tn = (pn - sg.p0) / TILE, kn = (pn - sg.p0) % TILE;
                 if ((int)((sg.pos + (tn - sg.t_begin)) % C::NGRP) == grp && kn / KPW == wig) {
                     const int blk = __ldg(a.block_tables + (int64_t)sg.b * a.max_blocks + pn / a.block_size);
                     if (blk >= 0 && blk < a.num_blocks) {  // else the box reads as zeros, as unfused
@@ -778,7 +950,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                 if (wait_or_abort(&kfull[stage], ph, flags, a, 210 + warp)) {
                     const uint32_t ks = smem_addr(smem + stage * C::STAGE_BYTES);
                     const uint32_t vs = ks + TILE * ROW_BYTES;
-                    const int nvalid = min(TILE, sg.p_end - t * TILE);
+                    const int nvalid = min(TILE, sg.p_end - (sg.p0 + t * TILE));
                     const bool st_here = STORE && t == st_t;
                     if (st_here) {  // lane l holds bytes 8l..8l+7 of each row
                         st_shared_v2(side_k + 8 * lane, st_k);
@@ -872,6 +1044,301 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Prefix kernel (pa_decode_shared_prefix).  For every group of sequences that
+// share leading blocks (find_prefix_groups), the attention of all members'
+// query heads over the shared prefix, as fp32 (m, l, o) partials that the
+// decode kernel's merge folds into each member's result.  A work item is one
+// kv head and a chunk of up to 64 query rows (64 / G members with their G
+// heads); its CTA reads each K/V tile of the prefix once (TMA, 3-stage ring)
+// and each of its 4 consumer warps runs one m16 row tile over every key
+// (mma.sync m16n8k16, online softmax in base 2, exact running max).
+// ---------------------------------------------------------------------------
+constexpr int PFX_WARPS = 4;                       // consumer warps, one m16 row tile each
+constexpr int PFX_ROWS = 16 * PFX_WARPS;           // query rows per work item
+constexpr int PFX_STAGES = 3;
+constexpr int PFX_THREADS = 32 * (PFX_WARPS + 1);  // + the TMA warp (the last)
+constexpr int PFX_STAGE_BYTES = 2 * TILE * ROW_BYTES;
+constexpr int PFX_OFF_BAR = PFX_STAGES * PFX_STAGE_BYTES;  // full, empty [PFX_STAGES] each
+constexpr int PFX_OFF_ZERO = PFX_OFF_BAR + 64;             // one zero row (keys past the prefix)
+constexpr int PFX_OFF_MEM = PFX_OFF_ZERO + ROW_BYTES;      // the item's members [PFX_ROWS] int
+constexpr int PFX_OFF_WSUM = PFX_OFF_MEM + 4 * PFX_ROWS;   // scan scratch [PFX_THREADS / 32] uint32
+constexpr int PFX_OFF_ARR = PFX_OFF_WSUM + 64;             // ctx, ps, pe, lead, nmem, chunk base [batch + 1]
+__host__ __device__ constexpr size_t pfx_smem_bytes(int batch) { return PFX_OFF_ARR + 24 * (size_t)(batch + 1) + 1024; }
+static_assert(pfx_smem_bytes(kMaxBatchCascade) <= 232448, "prefix kernel shared memory");
+
+template <int G>
+__global__ void __launch_bounds__(PFX_THREADS, 1)
+    decode_prefix_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                         const DecodeArgs a, float *pfx_o, float2 *pfx_ml) {
+    constexpr int MPI = PFX_ROWS / G;  // members per work item
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + PFX_OFF_BAR);
+    uint64_t *empty = full + PFX_STAGES;
+    int *mem = reinterpret_cast<int *>(smem + PFX_OFF_MEM);
+    uint32_t *wsum = reinterpret_cast<uint32_t *>(smem + PFX_OFF_WSUM);
+    int *ctx_s = reinterpret_cast<int *>(smem + PFX_OFF_ARR);
+    int *ps_s = ctx_s + (a.batch + 1), *pe_s = ps_s + (a.batch + 1), *lead = pe_s + (a.batch + 1);
+    int *nmem = lead + (a.batch + 1), *cbase = nmem + (a.batch + 1);
+    __shared__ int s_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool producer = warp == PFX_WARPS;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < PFX_STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], PFX_WARPS);
+        }
+        s_flag = 0;
+        fence_mbar_init();
+    }
+    if (producer && lane == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The decode kernel launched behind this one may start its set-up; it
+    // reads the partials only after this grid has completed.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x < ROW_BYTES / 16) st_shared_zero16(smem_addr(smem + PFX_OFF_ZERO) + 16 * threadIdx.x);
+    for (int b = threadIdx.x; b < a.batch; b += PFX_THREADS) ctx_s[b] = clamp_ctx(a, b, false);
+    __syncthreads();
+    find_prefix_groups(a.batch, a.block_tables, a.max_blocks, a.block_size, a.max_prefix_seqs, ctx_s, ps_s, pe_s,
+                       lead, nmem, reinterpret_cast<int *>(smem), wsum);
+    // The groups, for the decode kernel launched behind this one.
+    if (blockIdx.x == 0)
+        for (int b = threadIdx.x; b < a.batch; b += PFX_THREADS) {
+            a.grp[b] = ps_s[b];
+            a.grp[kMaxBatchCascade + b] = pe_s[b];
+        }
+    // Chunks of MPI members per group, numbered in leader order (nmem is 0 for
+    // sequences that lead no group): a block-wide exclusive scan.
+    {
+        const int per = (a.batch + PFX_THREADS - 1) / PFX_THREADS;
+        const int b0 = threadIdx.x * per, b1 = min(a.batch, b0 + per);
+        int run = 0;
+        for (int b = b0; b < b1; ++b) run += (nmem[b] + MPI - 1) / MPI;
+        int x = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[warp] = (uint32_t)x;
+        __syncthreads();
+        int before = 0;
+        for (int w2 = 0; w2 < warp; ++w2) before += (int)wsum[w2];
+        int c = before + x - run;
+        for (int b = b0; b < b1; ++b) {
+            cbase[b] = c;
+            c += (nmem[b] + MPI - 1) / MPI;
+        }
+        if (threadIdx.x == PFX_THREADS - 1) cbase[a.batch] = before + x;
+    }
+    __syncthreads();
+    const int nchunks = cbase[a.batch];
+    const int nitems = nchunks * a.Hkv * kPrefixSplits;  // (split, kv head, chunk)
+    const uint64_t pol = policy_evict_first();
+    uint32_t tc = 0;  // tiles through the ring (every role counts the same)
+    bool ok = true;
+    for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+        const int split = it / (nchunks * a.Hkv), g = (it / nchunks) % a.Hkv, ci = it % nchunks;
+        int L = 0;  // the group: the last leader whose chunk base is <= ci
+        {
+            int lo = 0, hi = a.batch - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (cbase[mid] <= ci) lo = mid; else hi = mid - 1;
+            }
+            L = lo;
+        }
+        const int c = ci - cbase[L];
+        __syncthreads();  // the previous item's member list is no longer read
+        if (warp == 0) {
+            // Members of L with an entry, in batch order; this chunk's MPI of them.
+            int seen = 0;
+            for (int b0 = L; b0 < a.batch; b0 += 32) {
+                const int b = b0 + lane;
+                const bool m = b < a.batch && lead[b] == L && pe_s[b] >= 0;
+                const unsigned bal = __ballot_sync(FULL, m);
+                const int r = seen + __popc(bal & ((1u << lane) - 1u));
+                if (m && r >= c * MPI && r < (c + 1) * MPI) mem[r - c * MPI] = b;
+                seen += __popc(bal);
+                if (seen >= (c + 1) * MPI) break;
+            }
+            if (lane == 0) s_flag = min(MPI, seen - c * MPI);  // members in this chunk
+        }
+        __syncthreads();
+        const int nm = s_flag;
+        const int P = ps_s[L];  // shared positions (a multiple of the block size)
+        const int ntall = (P + TILE - 1) / TILE;
+        // This split's tiles: [t0, t0 + nt) of the prefix (possibly none).
+        const int t0 = (int)((int64_t)ntall * split / kPrefixSplits);
+        const int nt = (int)((int64_t)ntall * (split + 1) / kPrefixSplits) - t0;
+        if (producer) {
+            if (lane == 0) {
+                for (int t = t0; ok && t < t0 + nt; ++t, ++tc) {
+                    const int st = tc % PFX_STAGES;
+                    ok = mbar_wait(&empty[st], ((tc / PFX_STAGES) & 1u) ^ 1u);
+                    if (!ok) {
+                        record_error(a.err, PA_DEV_TIMEOUT, 150);
+                        break;
+                    }
+                    const int p0 = t * TILE, rows = min(TILE, P - p0);
+                    const int nsub = (rows + a.box_rows - 1) / a.box_rows;
+                    mbar_arrive_expect_tx(&full[st], 2u * nsub * a.box_rows * ROW_BYTES);
+                    uint8_t *dst = smem + st * PFX_STAGE_BYTES;
+                    for (int sub = 0; sub < nsub; ++sub) {
+                        const int ps = p0 + sub * a.box_rows;
+                        const int blk = __ldg(a.block_tables + (int64_t)L * a.max_blocks + ps / a.block_size);
+                        long long slot = (long long)blk * a.block_size + ps % a.block_size;
+                        if (blk < 0 || blk >= a.num_blocks) slot = -2LL * a.box_rows;  // reads as zeros
+                        tma_load_4d(dst + sub * a.box_rows * ROW_BYTES, &tmk, 0, (int)slot, 0, g, &full[st], pol);
+                        tma_load_4d(dst + TILE * ROW_BYTES + sub * a.box_rows * ROW_BYTES, &tmv, 0, (int)slot, 0, g,
+                                    &full[st], pol);
+                    }
+                }
+            }
+            tc = __shfl_sync(FULL, tc, 0);
+            ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+            continue;
+        }
+        // ---- consumer warp: rows 16 * warp + (g4, g4 + 8) of the item
+        const int g4 = lane >> 2, t4 = lane & 3, mi = lane >> 3, r8 = lane & 7;
+        int rb[2], rh[2];  // member sequence (or -1) and q head of the two rows this thread holds
+        for (int i = 0; i < 2; ++i) {
+            const int r = 16 * warp + g4 + 8 * i;
+            rb[i] = r / G < nm ? mem[r / G] : -1;
+            rh[i] = g * G + r % G;
+        }
+        uint32_t qa[8][4];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const uint32_t *qr = reinterpret_cast<const uint32_t *>(a.q + (int64_t)max(rb[i], 0) * a.q_row_stride +
+                                                                       (int64_t)rh[i] * D);
+                qa[kk][i] = rb[i] >= 0 ? __ldg(qr + 8 * kk + t4) : 0u;          // cols 16kk + 2t4, +1
+                qa[kk][i + 2] = rb[i] >= 0 ? __ldg(qr + 8 * kk + 4 + t4) : 0u;  // cols 16kk + 8 + 2t4, +1
+            }
+        float o[16][4];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+        const int br = a.box_rows;
+        auto key_off = [&](int kk) -> uint32_t { return (uint32_t)((kk / br) * (br * ROW_BYTES) + (kk % br) * 128); };
+        const uint32_t half_stride = (uint32_t)br * 128;
+        const uint32_t zero_row = smem_addr(smem + PFX_OFF_ZERO);
+        for (int t = t0; t < t0 + nt; ++t, ++tc) {
+            const int st = tc % PFX_STAGES;
+            if (ok && !mbar_wait(&full[st], (tc / PFX_STAGES) & 1u)) {
+                record_error(a.err, PA_DEV_TIMEOUT, 151);
+                ok = false;
+            }
+            ok = __all_sync(FULL, ok);
+            if (ok) {
+                const uint32_t ks = smem_addr(smem + st * PFX_STAGE_BYTES), vs = ks + TILE * ROW_BYTES;
+                const int nvalid = min(TILE, P - t * TILE);
+                float sc[8][4];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+                for (int kg = 0; kg < 4; ++kg) {  // 16 keys at a time: n-tiles 2kg, 2kg+1
+                    const uint32_t krow = key_off(16 * kg + (mi >> 1) * 8 + r8);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const int chunk = 2 * kk + (mi & 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(ks + krow + (chunk >> 3) * half_stride + ((uint32_t)((chunk & 7) ^ r8) << 4), b0, b1, b2,
+                                b3);
+                        mma16816(sc[2 * kg], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                        mma16816(sc[2 * kg + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+                    }
+                }
+                // Online softmax (base 2) of the two rows; keys past the prefix are masked.
+                float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = 8 * j + 2 * t4 + (e & 1);
+                        sc[j][e] = key < nvalid ? sc[j][e] * a.scale_log2 : -INFINITY;
+                        mx[e >> 1] = fmaxf(mx[e >> 1], sc[j][e]);
+                    }
+                float alpha[2], mu[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    mx[i] = fmaxf(mx[i], __shfl_xor_sync(FULL, mx[i], 1));
+                    mx[i] = fmaxf(mx[i], __shfl_xor_sync(FULL, mx[i], 2));
+                    const float mn = fmaxf(m_run[i], mx[i]);
+                    alpha[i] = m_run[i] == -INFINITY ? 0.f : fast_exp2(m_run[i] - mn);
+                    m_run[i] = mn;
+                    mu[i] = mn == -INFINITY ? 0.f : mn;
+                    l_run[i] *= alpha[i];
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    o[j][0] *= alpha[0];
+                    o[j][1] *= alpha[0];
+                    o[j][2] *= alpha[1];
+                    o[j][3] *= alpha[1];
+                }
+                uint32_t pa[4][4];  // A fragments of P for the 4 16-key steps
+#pragma unroll
+                for (int kg = 0; kg < 4; ++kg)
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const float *v = sc[2 * kg + h2];
+                        const float p0 = fast_exp2(v[0] - mu[0]), p1 = fast_exp2(v[1] - mu[0]);
+                        const float p2 = fast_exp2(v[2] - mu[1]), p3 = fast_exp2(v[3] - mu[1]);
+                        l_run[0] += p0 + p1;
+                        l_run[1] += p2 + p3;
+                        pa[kg][2 * h2] = pack_bf16(p0, p1);      // row g4
+                        pa[kg][2 * h2 + 1] = pack_bf16(p2, p3);  // row g4 + 8
+                    }
+#pragma unroll
+                for (int kg = 0; kg < 4; ++kg) {
+                    const int vkey = 16 * kg + (mi & 1) * 8 + r8;
+                    const bool zero = vkey >= nvalid;  // stale rows may hold NaN; P is 0 there
+                    const uint32_t vrow = key_off(vkey);
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        const int chunk = j + (mi >> 1);
+                        const uint32_t ad = zero ? zero_row + 16 * chunk
+                                                 : vs + vrow + (chunk >> 3) * half_stride +
+                                                       ((uint32_t)((chunk & 7) ^ r8) << 4);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(ad, b0, b1, b2, b3);
+                        mma16816(o[j], pa[kg][0], pa[kg][1], pa[kg][2], pa[kg][3], b0, b1);
+                        mma16816(o[j + 1], pa[kg][0], pa[kg][1], pa[kg][2], pa[kg][3], b2, b3);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        if (!ok) continue;
+        // ---- the rows' partials: (m, l) and unnormalised o
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            l_run[i] += __shfl_xor_sync(FULL, l_run[i], 1);
+            l_run[i] += __shfl_xor_sync(FULL, l_run[i], 2);
+            if (rb[i] < 0) continue;
+            // A split with no tile leaves (-inf, 0, 0): the merge skips it.
+            const int64_t row = (int64_t)split * kMaxPrefixRows + (int64_t)pe_s[rb[i]] * a.Hq + rh[i];
+            if (t4 == 0) pfx_ml[row] = make_float2(m_run[i], l_run[i]);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                *reinterpret_cast<float2 *>(pfx_o + row * D + 8 * j + 2 * t4) = make_float2(o[j][2 * i], o[j][2 * i + 1]);
+        }
+    }
+    if (producer && lane == 0 && !ok) {
+        // Let issued copies land before the CTA's shared memory goes away.
+        for (uint32_t x = (tc >= (uint32_t)PFX_STAGES ? tc - PFX_STAGES : 0); x < tc; ++x)
+            (void)mbar_wait(&full[x % PFX_STAGES], (x / PFX_STAGES) & 1u);
+    }
+}
+
 // Per (device, instantiation): the shared-memory attribute has been set.
 // Two threads making their first call together may both set it (the call is
 // idempotent); the flag itself is an atomic, so there is no data race.
@@ -884,19 +1351,49 @@ pa_status launch(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &
     cudaGetDevice(&dev);
     const int gi = (G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3) + (STORE ? 4 : 0);
     if (dev >= 0 && dev < 64 && !g_attr_done[dev][gi].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<G, STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)Cfg<G>::smem_bytes(kMaxBatch));
+        cudaError_t e = cudaFuncSetAttribute(
+            decode_kernel<G, STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            (int)std::max(Cfg<G>::smem_bytes(kMaxBatch), Cfg<G>::smem_bytes(kMaxBatchCascade, true)));
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_kernel)");
         g_attr_done[dev][gi].store(1, std::memory_order_release);
     }
     // Programmatic dependent launch: the grid may start while the previous
     // kernel on the stream finishes; it reads nothing before griddepcontrol.wait.
     return launch_pdl(decode_kernel<G, STORE>, dim3((unsigned)grid), dim3(Cfg<G>::NTHREADS),
-                      Cfg<G>::smem_bytes(a.batch), st, "decode_kernel", tk, tv, a);
+                      Cfg<G>::smem_bytes(a.batch, a.cascade != 0), st, "decode_kernel", tk, tv, a);
+}
+
+std::atomic<int> g_pfx_attr_done[64][4];
+
+// The prefix kernel for shared prefixes, launched (programmatic dependent
+// launch) right before the decode kernel that folds its partials in.
+template <int G>
+pa_status launch_prefix(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int sms, cudaStream_t st) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+    if (dev >= 0 && dev < 64 && !g_pfx_attr_done[dev][gi].load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(decode_prefix_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)pfx_smem_bytes(kMaxBatchCascade));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_prefix_kernel)");
+        g_pfx_attr_done[dev][gi].store(1, std::memory_order_release);
+    }
+    // Work items: (kv head, chunk of PFX_ROWS / G members of one group); at
+    // most batch / 2 groups and batch members.
+    constexpr int MPI = PFX_ROWS / G;
+    const int64_t bound = (int64_t)a.Hkv * kPrefixSplits * ((a.batch + MPI - 1) / MPI + a.batch / 2);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, bound));
+    return launch_pdl(decode_prefix_kernel<G>, dim3((unsigned)grid), dim3(PFX_THREADS), pfx_smem_bytes(a.batch), st,
+                      "decode_prefix_kernel", tk, tv, a, const_cast<float *>(a.pfx_o), const_cast<float2 *>(a.pfx_ml));
 }
 
 template <int G>
-pa_status launch_g(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int grid, cudaStream_t st) {
+pa_status launch_g(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &tv, int grid, int sms,
+                   cudaStream_t st) {
+    if (a.cascade) {
+        const pa_status s = launch_prefix<G>(a, tk, tv, sms, st);
+        if (s != PA_OK) return s;
+    }
     return a.new_k ? launch<G, true>(a, tk, tv, grid, st) : launch<G, false>(a, tk, tv, grid, st);
 }
 
@@ -906,6 +1403,7 @@ pa_status launch_g(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap
 // partials, two slots of G heads per range.
 struct WsLayout {
     size_t ctr_off, cnt_off, ml_off, o_off, total;
+    size_t grp_off, pfx_ml_off, pfx_o_off, total_prefix;  // pa_decode_shared_prefix: groups and prefix partials
 };
 
 WsLayout ws_layout(int G) {
@@ -917,6 +1415,10 @@ WsLayout ws_layout(int G) {
     L.ml_off = up(L.cnt_off + (size_t)kMaxRanges * sizeof(int));
     L.o_off = up(L.ml_off + slots * sizeof(float2));
     L.total = L.o_off + slots * D * sizeof(float);
+    L.grp_off = up(L.total);
+    L.pfx_ml_off = up(L.grp_off + 2 * (size_t)kMaxBatchCascade * sizeof(int));
+    L.pfx_o_off = up(L.pfx_ml_off + (size_t)kPrefixSplits * kMaxPrefixRows * sizeof(float2));
+    L.total_prefix = L.pfx_o_off + (size_t)kPrefixSplits * kMaxPrefixRows * D * sizeof(float);
     return L;
 }
 
@@ -943,10 +1445,12 @@ pa_status decode_impl(void *out, const void *q, int64_t q_row_stride, void *k_ca
                       int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                       int32_t num_blocks, float softmax_scale, void *workspace, size_t workspace_bytes,
                       const void *new_k, int64_t new_k_row_stride, const void *new_v, int64_t new_v_row_stride,
-                      pa_stream_t stream) {
+                      pa_stream_t stream, bool cascade = false) {
     if (batch < 0) return fail(PA_ERR_INVALID_ARG, "batch < 0");
     if (batch == 0) return PA_OK;
     if (batch > kMaxBatch) return fail(PA_ERR_UNSUPPORTED, "batch %d > %d", batch, kMaxBatch);
+    if (cascade && batch > kMaxBatchCascade)
+        return fail(PA_ERR_UNSUPPORTED, "batch %d > %d with shared prefixes", batch, kMaxBatchCascade);
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
         return fail(PA_ERR_INVALID_ARG, "null pointer");
     if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads)
@@ -973,8 +1477,9 @@ pa_status decode_impl(void *out, const void *q, int64_t q_row_stride, void *k_ca
     if (!(softmax_scale > 0.f) || !isfinite(softmax_scale))
         return fail(PA_ERR_INVALID_ARG, "softmax_scale must be positive and finite");
     const WsLayout W = ws_layout(G);
-    if (!workspace || workspace_bytes < W.total)
-        return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", W.total,
+    const size_t need = cascade ? W.total_prefix : W.total;
+    if (!workspace || workspace_bytes < need)
+        return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                     workspace ? workspace_bytes : (size_t)0);
     if (!aligned16(workspace)) return fail(PA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
 
@@ -1014,6 +1519,11 @@ pa_status decode_impl(void *out, const void *q, int64_t q_row_stride, void *k_ca
     A.new_v_stride = new_v_row_stride / 4;
     A.k_cache = static_cast<uint2 *>(k_cache);
     A.v_cache = static_cast<uint2 *>(v_cache);
+    A.cascade = cascade ? 1 : 0;
+    A.max_prefix_seqs = kMaxPrefixRows / num_q_heads;
+    A.pfx_ml = cascade ? reinterpret_cast<const float2 *>(ws + W.pfx_ml_off) : nullptr;
+    A.pfx_o = cascade ? reinterpret_cast<const float *>(ws + W.pfx_o_off) : nullptr;
+    A.grp = cascade ? reinterpret_cast<int *>(ws + W.grp_off) : nullptr;
 
     const int sms = std::min(sm_count(), kMaxGrid);
     if (sms <= 0) return fail(PA_ERR_CUDA, "no CUDA device");
@@ -1026,10 +1536,10 @@ pa_status decode_impl(void *out, const void *q, int64_t q_row_stride, void *k_ca
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, (tiles_bound + kMinTilesPerCta - 1) / kMinTilesPerCta));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (G) {
-        case 1: return launch_g<1>(A, tk, tv, grid, s);
-        case 2: return launch_g<2>(A, tk, tv, grid, s);
-        case 4: return launch_g<4>(A, tk, tv, grid, s);
-        default: return launch_g<8>(A, tk, tv, grid, s);
+        case 1: return launch_g<1>(A, tk, tv, grid, sms, s);
+        case 2: return launch_g<2>(A, tk, tv, grid, sms, s);
+        case 4: return launch_g<4>(A, tk, tv, grid, sms, s);
+        default: return launch_g<8>(A, tk, tv, grid, sms, s);
     }
 }
 
@@ -1066,6 +1576,32 @@ pa_status pa_decode_store(void *out, const void *q, int64_t q_row_stride, const 
     return decode_impl(out, q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch,
                        num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, softmax_scale, workspace,
                        workspace_bytes, new_k, new_k_row_stride, new_v, new_v_row_stride, stream);
+}
+
+size_t pa_decode_shared_prefix_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim) {
+    using namespace pa;
+    if (pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim) == 0) return 0;
+    return ws_layout(num_q_heads / num_kv_heads).total_prefix;
+}
+
+pa_status pa_decode_shared_prefix(void *out, const void *q, int64_t q_row_stride, const void *new_k,
+                                  int64_t new_k_row_stride, const void *new_v, int64_t new_v_row_stride, void *k_cache,
+                                  void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *context_lens, int32_t batch, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                  float softmax_scale, void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+    using namespace pa;
+    if (batch > 0 && (new_k != nullptr) != (new_v != nullptr))
+        return fail(PA_ERR_INVALID_ARG, "new_k and new_v must both be given or both be null");
+    if (batch > 0 && new_k) {
+        if (!aligned16(new_k) || !aligned16(new_v)) return fail(PA_ERR_INVALID_ARG, "new_k/new_v must be 16-byte aligned");
+        const int64_t row = (int64_t)num_kv_heads * D;
+        if (new_k_row_stride < row || new_v_row_stride < row || new_k_row_stride % 8 || new_v_row_stride % 8)
+            return fail(PA_ERR_INVALID_ARG, "new_k/new_v row strides must be >= num_kv_heads*head_dim and multiples of 8");
+    }
+    return decode_impl(out, q, q_row_stride, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, softmax_scale, workspace,
+                       workspace_bytes, new_k, new_k_row_stride, new_v, new_v_row_stride, stream, true);
 }
 
 }  // extern "C"
