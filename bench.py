@@ -5,9 +5,11 @@ decode workload, the Qwen3-8B attention shape: batch 256, 32 q / 8 kv heads,
 head_dim 128, block_size 256, context_lens lognormal (median 1024, capped
 8192), sequences 0..127 sharing their first 4 physical blocks (prefix cache,
 ref_count 128), pool = 1.2x the blocks needed, random block permutation, bf16
-N(0,1).  The step is one launch of the fused kernel (pa_decode_store): each
-sequence's new K/V row is stored to its slot and the split-KV GQA decode
-attention reads every context row through the block tables.  All inputs are
+N(0,1).  The step is one call of pa_decode_shared_prefix with the new token's
+store fused: a prefix kernel attends the 128 sharing sequences' query heads to
+their 4 shared blocks once per kv head, then the split-KV GQA decode kernel
+stores each sequence's new K/V row to its slot, reads every other context row
+through the block tables and merges the prefix partials.  All inputs are
 resident in HBM before the timed region; L2 is flushed (a 256 MiB write)
 before every timed step.  `value` is decode tokens/s (one layer) over all
 ranks; `e2e` is the same metric through the public API with the step's
@@ -48,8 +50,9 @@ METRIC = "paged decode attn tokens/s and HBM GB/s vs GB300 peak; prefill TFLOP/s
 HEADLINE_CONFIG = 3
 WORKLOAD = ("qwen3-8b decode step, 1 layer: batch 256, 32 q / 8 kv heads, head_dim 128, block_size 256, "
             "context_lens lognormal (median 1024, sigma 1, capped 8192), sequences 0..127 share their first 4 "
-            "physical blocks (prefix cache), pool = 1.2x blocks needed, random block permutation, "
-            "store of the new token fused into the split-KV decode kernel (pa_decode_store)")
+            "physical blocks (prefix cache), pool = 1.2x blocks needed, random block permutation; "
+            "pa_decode_shared_prefix with the new token's store fused (shared prefix attended once per kv head, "
+            "split-KV decode over each sequence's own blocks)")
 SUB_DECODE_CONFIGS = (1, 2, 4)
 FALLBACK_HBM_GBS = 6800.0
 
@@ -469,12 +472,16 @@ def run_ours(args):
     slots = torch.empty(inp.batch, dtype=torch.int32, device=dev)
     out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
     wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev)
+    wsx = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev, shared_prefix=True)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     by = decode_bytes(inp)
     L2 = (f"flushed (256 MiB write) before every timed step; K/V pool {kc.numel() * 4 / 2**30:.2f} GiB > L2")
 
-    def step():  # one kernel: the decode kernel stores the new K/V rows, then attends
+    def step():  # prefix kernel + decode kernel (which stores the new K/V rows, then attends)
+        pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsx, out=out, new_k=nk, new_v=nv, shared_prefix=True)
+
+    def step_plain():  # one kernel, no grouping: every sequence streams its whole context
         pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out, new_k=nk, new_v=nv)
 
     def step_unfused():  # the same work as three launches
@@ -484,6 +491,7 @@ def run_ours(args):
 
     for _ in range(max(3, args.warmup)):
         step()
+        step_plain()
         step_unfused()
     torch.cuda.synchronize()
     _check_device(pa)
@@ -523,8 +531,9 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = job_throughput(ws, inp.batch, args.steps, total_ms)
 
-    # The same step as three launches (slot mapping, store, decode: programmatic
-    # dependent launches back to back), for comparison.
+    # The same step without grouping (one launch of the fused kernel), and as
+    # three launches (slot mapping, store, decode), for comparison.
+    plain_ms = sum(_event_times(step_plain, args.steps, stream, flush)) / args.steps
     unfused_ms = sum(_event_times(step_unfused, args.steps, stream, flush)) / args.steps
     # The plain decode launch alone (store done before it).
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -572,7 +581,8 @@ def run_ours(args):
             flush.zero_()
             e2e_ev[i - 2][0].record(stream)
         d_pack.copy_(h_pack, non_blocking=True)
-        pa.decode(e_q, kc, vc, e_bt, e_ctx, inp.scale, workspace=wsp, out=out, new_k=e_nk, new_v=e_nv)
+        pa.decode(e_q, kc, vc, e_bt, e_ctx, inp.scale, workspace=wsx, out=out, new_k=e_nk, new_v=e_nv,
+                  shared_prefix=True)
         h_out.copy_(out, non_blocking=True)
         if i >= 2:
             e2e_ev[i - 2][1].record(stream)
@@ -595,7 +605,7 @@ def run_ours(args):
     if rank == 0:
         achieved = by["unique"] / (ms_per_step / 1000.0) / 1e9
         achieved_logical = by["logical"] / (ms_per_step / 1000.0) / 1e9
-        traffic = recorded_traffic(f"decode_kernel<{inp.num_q_heads // inp.num_kv_heads}, store>", "qwen3-8b")
+        traffic = recorded_traffic("decode_prefix_kernel<4> + decode_kernel<4, store>", "qwen3-8b")
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -603,7 +613,9 @@ def run_ours(args):
             "data": "synthetic (seeded N(0,1) bf16, random block tables)",
             "config": {"workload": WORKLOAD, "global_batch": inp.batch * ws, "seq_len": "lognormal(1024), cap 8192",
                        "parallelism": f"replicas x{ws}", "l2": L2},
-            "roofline": {"bound": "hbm", "kernel": "decode_kernel<4, store> (pa_decode_store)", "achieved": achieved,
+            "roofline": {"bound": "hbm",
+                         "kernel": "decode_prefix_kernel<4> + decode_kernel<4, store> (one pa_decode_shared_prefix call)",
+                         "achieved": achieved,
                          "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
                          "frac_of_nominal_8TBps": achieved / 8000.0, "traffic": traffic,
                          "algorithmic_bytes_per_launch": by["unique"],
@@ -611,13 +623,16 @@ def run_ours(args):
                          "logical": {"algorithmic_bytes_per_launch": by["logical"], "achieved": achieved_logical,
                                      "frac": achieved_logical / hbm,
                                      "basis": "shared prefix rows counted once per sequence that reads them"},
-                         "launch_ms": ms_per_step, "plain_decode_ms": sum(dec_ms) / len(dec_ms),
-                         "store_ms": sum(store_ms) / len(store_ms)},
+                         "launch_ms": ms_per_step, "duration_basis": "the whole call (both kernels), CUDA events",
+                         "plain_decode_ms": sum(dec_ms) / len(dec_ms), "store_ms": sum(store_ms) / len(store_ms)},
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps,
+            "gpu_launches": 2 * args.steps,
             "sustained": {"steps": n_sustain, "seconds": sum(sus_ms) / 1000.0,
                           "ms_median": float(np.median(sus_ms)),
                           "note": "the same flushed step back to back before the timed region, for the clock record"},
+            "plain_fused_step": {"ms_per_step": plain_ms, "kernels": "decode_kernel<4, store> (pa_decode_store, no grouping)",
+                                 "tokens_per_s": ws * inp.batch / (plain_ms / 1000.0),
+                                 "frac_unique_bytes": by["unique"] / (plain_ms / 1000.0) / 1e9 / hbm},
             "unfused_step": {"ms_per_step": unfused_ms, "kernels": "slot_mapping_decode + store_kvcache + decode",
                              "tokens_per_s": ws * inp.batch / (unfused_ms / 1000.0)},
             "clocks": clk.summary(),
@@ -674,6 +689,12 @@ def run_report(args):
         out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
         wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev)
         ms = timed(lambda: pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out, new_k=nk, new_v=nv))
+        ms_plain = None
+        if cfg == 3:  # the shared-prefix call is the one that counts; the plain fused step beside it
+            ms_plain = ms
+            wsx = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev, shared_prefix=True)
+            ms = timed(lambda: pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsx, out=out, new_k=nk, new_v=nv,
+                                         shared_prefix=True))
         t0 = time.perf_counter()
         want = oracle_decode_step(inp, O, nthr)
         oracle_s = time.perf_counter() - t0
@@ -684,6 +705,8 @@ def run_report(args):
         by = decode_bytes(inp)
         gbs = by["unique"] / (ms / 1000.0) / 1e9
         note = f" ({by['logical'] / (ms / 1000.0) / 1e9:,.0f} logical)" if by["logical"] != by["unique"] else ""
+        if ms_plain is not None:
+            note += f"; without grouping {ms_plain * 1000:.1f} us, {by['unique'] / (ms_plain / 1000.0) / 1e9:,.0f}"
         lines.append(f"| {cfg} {inp.name} | {ms * 1000:.1f} us | {inp.batch / (ms / 1000.0):,.0f} | "
                      f"{gbs:,.0f}{note} | — | {100 * gbs / hbm:.1f} % of {hbm:.0f} ({kind}) | "
                      f"{oracle_s:.2f} s on {nthr} / {oracle_1:.2f} s | {err.max():.2e} / {err.mean():.2e} |")
@@ -725,7 +748,8 @@ def run_profile_case(args):
     store) with context lengths ~ U[1, 1536], about 190 MB of K/V (more than
     the 129 MB L2, a fraction of the full case), for multi-pass captures.
     decode-qwen3-8b: the headline workload itself (about 2.4 GB on the
-    device), for single-pass captures (DRAM bytes and duration).
+    device; pa_decode_shared_prefix: a prefix kernel and a decode kernel
+    per call), for single-pass captures (DRAM bytes and duration).
     prefill: the prefill workload (plain prefill launches after one store).
     Each runs `warmup` then `steps` launches with an L2 flush before each."""
     import torch
@@ -757,10 +781,11 @@ def run_profile_case(args):
     nk, nv = _to_dev(inp.new_k, dev, True), _to_dev(inp.new_v, dev, True)
     bt, ctx = _to_dev(inp.block_tables, dev), _to_dev(inp.context_lens, dev)
     out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
-    wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev)
+    shared = args.profile_case == "decode-qwen3-8b"  # the headline call: shared prefix grouped
+    wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev, shared_prefix=shared)
     for _ in range(args.warmup + args.steps):
         flush.zero_()
-        pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out, new_k=nk, new_v=nv)
+        pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out, new_k=nk, new_v=nv, shared_prefix=shared)
     torch.cuda.synchronize()
     _check_device(pa)
     print(f"profile case: {inp.name}: {inp.batch} seqs, {int(inp.context_lens.sum())} context tokens, "
