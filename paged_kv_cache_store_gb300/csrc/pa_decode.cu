@@ -102,8 +102,9 @@ struct Cfg {
     static constexpr int OFF_Q = STAGES * STAGE_BYTES;          // q slots [2][G][D] bf16
     static constexpr int OFF_SLOT = OFF_Q + 2 * Q_BYTES;        // merge slots [NSLOT][SLOT_FLOATS] f32
     static constexpr int OFF_BAR = OFF_SLOT + NSLOT * SLOT_FLOATS * 4;
-    // kfull, vfull, empty [STAGES]; qfull, qempty, done, sfree [2]; tfull, tempty [NTK]
-    static constexpr int NBAR = 3 * STAGES + 8 + 2 * NTK;
+    // kfull, vfull, empty (the V half), kempty (the K half) [STAGES]; qfull,
+    // qempty, done, sfree [2]; tfull, tempty [NTK]
+    static constexpr int NBAR = 4 * STAGES + 8 + 2 * NTK;
     static constexpr int OFF_FLAGS = OFF_BAR + NBAR * 8;   // [0]: abort
     static constexpr int OFF_TK = OFF_FLAGS + 16;          // Ticket [NTK]
     static constexpr int OFF_WSUM = OFF_TK + NTK * 32;     // scan scratch [NWARPS] uint32
@@ -435,8 +436,9 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     Ticket *tks = reinterpret_cast<Ticket *>(smem + C::OFF_TK);
     uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *vfull = kfull + C::STAGES;
-    uint64_t *empty = vfull + C::STAGES;
-    uint64_t *qfull = empty + C::STAGES;
+    uint64_t *empty = vfull + C::STAGES;   // the stage's V half was read
+    uint64_t *kempty = empty + C::STAGES;  // the stage's K half was read (after Q.K, before P.V)
+    uint64_t *qfull = kempty + C::STAGES;
     uint64_t *qempty = qfull + 2;
     uint64_t *done = qempty + 2;
     uint64_t *sfree = done + 2;
@@ -450,6 +452,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
             mbar_init(&kfull[s], 1);
             mbar_init(&vfull[s], 1);
             mbar_init(&empty[s], WPG);
+            mbar_init(&kempty[s], WPG);
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(&qfull[k], 1);
@@ -632,7 +635,10 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                     const int tg = (int)((cur.pos + (t - cur.t_begin)) % C::NGRP);  // consumer group of the tile
                     const uint32_t n = tg ? n1++ : n0++;
                     const int stage = tg + C::NGRP * (int)(n % C::SPG);
-                    if (lane == 0) ok = wait_or_abort(&empty[stage], ((n / C::SPG) & 1) ^ 1, flags, a, 101);
+                    // Each half of a stage is refilled once the consumers read it: K after
+                    // their Q.K, V after their P.V.
+                    if (lane == 0)
+                        ok = wait_or_abort(isk ? &kempty[stage] : &empty[stage], ((n / C::SPG) & 1) ^ 1, flags, a, 101);
                     ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
                     if (!ok) break;
                     if (isk && lane == 0 && !taken && range_left <= 2) {
@@ -973,6 +979,9 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
                         mma16816(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
                         mma16816(sc[1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
                     }
+                    // The K half is no longer read: let the K producer refill it now.
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&kempty[stage]);
                     // ---- online softmax (base 2) with a lazy reference max
                     const int key0 = wig * KPW + 2 * t4;
                     float x[4];

@@ -212,3 +212,35 @@ def test_prefill_store_argument_checks(L):
     assert _prefill_store(L, hq=12) == pa.PA_ERR_INVALID_ARG   # the prefill's own checks follow
     assert _prefill_store(L, d=64) == pa.PA_ERR_UNSUPPORTED
     assert _prefill_store(L, B=24) == pa.PA_ERR_UNSUPPORTED
+
+
+def test_shared_prefix_argument_checks(L):
+    """pa_decode_shared_prefix: its own checks (new rows both or neither,
+    batch <= 1024, the larger workspace), then pa_decode's; every case fails
+    (or has nothing to do) before any launch."""
+    p = C.c_void_p(256)
+    base = L.pa_decode_workspace_size(32, 8, 128)
+    full = L.pa_decode_shared_prefix_workspace_size(32, 8, 128)
+    # the groups and 8192 (member, head) rows of prefix partials in two splits, after the decode workspace
+    assert full >= base + 2 * 8192 * (128 * 4 + 8)
+    assert full <= base + 2 * 8192 * (128 * 4 + 8) + 2 * 1024 * 4 + 1024
+    assert L.pa_decode_shared_prefix_workspace_size(24, 8, 128) == 0
+
+    def call(**kw):
+        a = dict(out=p, q=p, qs=4096, nk=p, nks=1024, nv=p, nvs=1024, k=p, v=p, bt=p, mb=16, ctx=p, batch=4,
+                 hq=32, hkv=8, d=128, B=256, nb=64, scale=0.088, ws=p, wsb=full, stream=None)
+        a.update(kw)
+        return L.pa_decode_shared_prefix(a["out"], a["q"], a["qs"], a["nk"], a["nks"], a["nv"], a["nvs"], a["k"],
+                                         a["v"], a["bt"], a["mb"], a["ctx"], a["batch"], a["hq"], a["hkv"], a["d"],
+                                         a["B"], a["nb"], a["scale"], a["ws"], a["wsb"], a["stream"])
+
+    assert call(batch=0) == pa.PA_OK
+    assert call(nv=None) == pa.PA_ERR_INVALID_ARG                  # new K without new V
+    assert call(nk=None) == pa.PA_ERR_INVALID_ARG
+    assert call(nk=C.c_void_p(264)) == pa.PA_ERR_INVALID_ARG       # unaligned
+    assert call(nks=1000) == pa.PA_ERR_INVALID_ARG                 # stride below Hkv*D
+    assert call(batch=1025) == pa.PA_ERR_UNSUPPORTED               # beyond the grouping's batch
+    assert call(wsb=base) == pa.PA_ERR_WORKSPACE                   # the plain decode workspace is too small
+    assert "workspace" in _msg(L)
+    assert call(hq=24) == pa.PA_ERR_UNSUPPORTED                    # pa_decode's own checks still apply
+    assert call(scale=-1.0) == pa.PA_ERR_INVALID_ARG

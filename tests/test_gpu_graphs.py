@@ -67,6 +67,47 @@ def test_fused_decode_step_replays():
         assert torch.equal(kc_g, kc_e) and torch.equal(vc_g, vc_e), f"step {i}"
 
 
+def test_shared_prefix_decode_step_replays():
+    """The shared-prefix decode step (grouping + prefix kernel + decode kernel
+    with the fused store), captured once and replayed for successive steps
+    with new query and new-token rows and growing contexts: equal to eager
+    calls."""
+    ctx0 = [1100, 1030, 1500, 300, 2000, 1025]
+    base = make_decode("graph-sp", 23, 6, 32, 8, ctx0, shared_prefix_seqs=3, shared_prefix_blocks=4,
+                       extra_table_cols=1)
+    steps = 3
+
+    class Rows:
+        def __init__(self, i):
+            self.q = normal_bf16(200 + i, 1, (6, 32, 128))
+            self.new_k = normal_bf16(200 + i, 2, (6, 8, 128))
+            self.new_v = normal_bf16(200 + i, 3, (6, 8, 128))
+    news = [Rows(i) for i in range(steps)]
+    kc_g, vc_g = dev_bf16(base.k_cache), dev_bf16(base.v_cache)
+    kc_e, vc_e = dev_bf16(base.k_cache), dev_bf16(base.v_cache)
+    bt, ctx = dev_i32(base.block_tables), dev_i32(base.context_lens)
+    q, nk, nv = dev_bf16(news[0].q), dev_bf16(news[0].new_k), dev_bf16(news[0].new_v)
+    out = torch.empty(6, 32, 128, dtype=torch.bfloat16, device="cuda")
+    ws_g = pa.decode_workspace(32, 8, 128, shared_prefix=True)
+    ws_e = pa.decode_workspace(32, 8, 128, shared_prefix=True)
+    g = capture(lambda: pa.decode(q, kc_g, vc_g, bt, ctx, base.scale, workspace=ws_g, out=out, new_k=nk, new_v=nv,
+                                  shared_prefix=True))
+    pa.decode(q, kc_e, vc_e, bt, ctx, base.scale, workspace=ws_e, new_k=nk, new_v=nv, shared_prefix=True)
+    lens = base.context_lens.copy()
+    for i in range(steps):
+        lens = lens + 1 if i else lens
+        ctx.copy_(torch.from_numpy(lens.astype(np.int32)))
+        q.copy_(dev_bf16(news[i].q))
+        nk.copy_(dev_bf16(news[i].new_k))
+        nv.copy_(dev_bf16(news[i].new_v))
+        g.replay()
+        want = pa.decode(q, kc_e, vc_e, bt, ctx, base.scale, workspace=ws_e, new_k=nk, new_v=nv, shared_prefix=True)
+        torch.cuda.synchronize()
+        assert pa.get_device_error() == (0, 0)
+        assert torch.equal(out, want), f"step {i}"
+        assert torch.equal(kc_g, kc_e) and torch.equal(vc_g, vc_e), f"step {i}"
+
+
 @pytest.mark.parametrize("fused", [False, True])
 def test_prefill_step_replays(fused):
     """Slot mapping + store + prefill (three launches), or the fused store +
