@@ -419,9 +419,9 @@ def measure_prefill(args, dev, stream, flush, bf16_peak):
             "total_q": p.total_q, "ms_prefill": pre_ms, "ms_slotmap_store": slotmap_store_ms, "ms_store": store_ms,
             "ms_step_3_launches": step3_ms, "ms_step_fused": fused_ms,
             "algorithmic_flops": flops,
-            "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": tflops, "peak": bf16_peak,
+            "roofline": {"bound": "tensor", "kernel": "prefill_pair_kernel<0>", "achieved": tflops, "peak": bf16_peak,
                          "unit": "TFLOP/s", "frac": tflops / bf16_peak, "peak_kind": "burst (timed alone)",
-                         "traffic": recorded_traffic("prefill_kernel<0>", "prefill", PREFILL_SOURCES)},
+                         "traffic": recorded_traffic("prefill_pair_kernel<0>", "prefill", PREFILL_SOURCES)},
             "store_gbs": store_bytes / (store_ms / 1000.0) / 1e9}
 
 
