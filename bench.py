@@ -605,7 +605,7 @@ def run_ours(args):
     if rank == 0:
         achieved = by["unique"] / (ms_per_step / 1000.0) / 1e9
         achieved_logical = by["logical"] / (ms_per_step / 1000.0) / 1e9
-        traffic = recorded_traffic("decode_prefix_kernel<4> + decode_kernel<4, store>", "qwen3-8b")
+        traffic = recorded_traffic("decode_prefix_tc_kernel<4> + decode_kernel<4, store>", "qwen3-8b")
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,

@@ -55,6 +55,7 @@
 #include <mutex>
 
 #include "pa_internal.cuh"
+#include "pa_tcgen05.cuh"
 
 namespace pa {
 namespace {
@@ -1063,6 +1064,75 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
 // and each of its 4 consumer warps runs one m16 row tile over every key
 // (mma.sync m16n8k16, online softmax in base 2, exact running max).
 // ---------------------------------------------------------------------------
+// Set-up shared by both prefix kernels (every thread of the CTA calls it):
+// context lengths, the groups (CTA 0 also publishes them for the decode
+// kernel) and the chunks of `mpi` members per group, numbered in leader
+// order (cbase[L] = first chunk of leader L, cbase[batch] = all chunks).
+// Returns the number of chunks.
+__device__ int prefix_setup(const DecodeArgs &a, int mpi, int *scr, int *ctx_s, int *ps_s, int *pe_s, int *lead,
+                            int *nmem, int *cbase, uint32_t *wsum) {
+    const int nthr = blockDim.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int b = threadIdx.x; b < a.batch; b += nthr) ctx_s[b] = clamp_ctx(a, b, false);
+    __syncthreads();
+    find_prefix_groups(a.batch, a.block_tables, a.max_blocks, a.block_size, a.max_prefix_seqs, ctx_s, ps_s, pe_s,
+                       lead, nmem, scr, wsum);
+    if (blockIdx.x == 0)
+        for (int b = threadIdx.x; b < a.batch; b += nthr) {
+            a.grp[b] = ps_s[b];
+            a.grp[kMaxBatchCascade + b] = pe_s[b];
+        }
+    // nmem is 0 for sequences that lead no group: a block-wide exclusive scan.
+    const int per = (a.batch + nthr - 1) / nthr;
+    const int b0 = threadIdx.x * per, b1 = min(a.batch, b0 + per);
+    int run = 0;
+    for (int b = b0; b < b1; ++b) run += (nmem[b] + mpi - 1) / mpi;
+    int x = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = (uint32_t)x;
+    __syncthreads();
+    int before = 0;
+    for (int w2 = 0; w2 < warp; ++w2) before += (int)wsum[w2];
+    int c = before + x - run;
+    for (int b = b0; b < b1; ++b) {
+        cbase[b] = c;
+        c += (nmem[b] + mpi - 1) / mpi;
+    }
+    if (threadIdx.x == nthr - 1) cbase[a.batch] = before + x;
+    __syncthreads();
+    return cbase[a.batch];
+}
+
+// The group of chunk ci: the last leader whose chunk base is <= ci.
+__device__ __forceinline__ int chunk_leader(const int *cbase, int batch, int ci) {
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cbase[mid] <= ci) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// One warp: the members of leader L that have an entry, in batch order;
+// chunk c's `mpi` of them go to mem[0..).  Returns how many (all lanes).
+__device__ int chunk_members(int L, int c, int mpi, int batch, const int *lead, const int *pe_s, int *mem) {
+    const int lane = threadIdx.x & 31;
+    int seen = 0;
+    for (int b0 = L; b0 < batch; b0 += 32) {
+        const int b = b0 + lane;
+        const bool m = b < batch && lead[b] == L && pe_s[b] >= 0;
+        const unsigned bal = __ballot_sync(FULL, m);
+        const int r = seen + __popc(bal & ((1u << lane) - 1u));
+        if (m && r >= c * mpi && r < (c + 1) * mpi) mem[r - c * mpi] = b;
+        seen += __popc(bal);
+        if (seen >= (c + 1) * mpi) break;
+    }
+    return min(mpi, seen - c * mpi);
+}
+
 constexpr int PFX_WARPS = 4;                       // consumer warps, one m16 row tile each
 constexpr int PFX_ROWS = 16 * PFX_WARPS;           // query rows per work item
 constexpr int PFX_STAGES = 3;
@@ -1110,72 +1180,20 @@ __global__ void __launch_bounds__(PFX_THREADS, 1)
     // reads the partials only after this grid has completed.
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x < ROW_BYTES / 16) st_shared_zero16(smem_addr(smem + PFX_OFF_ZERO) + 16 * threadIdx.x);
-    for (int b = threadIdx.x; b < a.batch; b += PFX_THREADS) ctx_s[b] = clamp_ctx(a, b, false);
-    __syncthreads();
-    find_prefix_groups(a.batch, a.block_tables, a.max_blocks, a.block_size, a.max_prefix_seqs, ctx_s, ps_s, pe_s,
-                       lead, nmem, reinterpret_cast<int *>(smem), wsum);
-    // The groups, for the decode kernel launched behind this one.
-    if (blockIdx.x == 0)
-        for (int b = threadIdx.x; b < a.batch; b += PFX_THREADS) {
-            a.grp[b] = ps_s[b];
-            a.grp[kMaxBatchCascade + b] = pe_s[b];
-        }
-    // Chunks of MPI members per group, numbered in leader order (nmem is 0 for
-    // sequences that lead no group): a block-wide exclusive scan.
-    {
-        const int per = (a.batch + PFX_THREADS - 1) / PFX_THREADS;
-        const int b0 = threadIdx.x * per, b1 = min(a.batch, b0 + per);
-        int run = 0;
-        for (int b = b0; b < b1; ++b) run += (nmem[b] + MPI - 1) / MPI;
-        int x = run;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(FULL, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) wsum[warp] = (uint32_t)x;
-        __syncthreads();
-        int before = 0;
-        for (int w2 = 0; w2 < warp; ++w2) before += (int)wsum[w2];
-        int c = before + x - run;
-        for (int b = b0; b < b1; ++b) {
-            cbase[b] = c;
-            c += (nmem[b] + MPI - 1) / MPI;
-        }
-        if (threadIdx.x == PFX_THREADS - 1) cbase[a.batch] = before + x;
-    }
-    __syncthreads();
-    const int nchunks = cbase[a.batch];
+    const int nchunks =
+        prefix_setup(a, MPI, reinterpret_cast<int *>(smem), ctx_s, ps_s, pe_s, lead, nmem, cbase, wsum);
     const int nitems = nchunks * a.Hkv * kPrefixSplits;  // (split, kv head, chunk)
     const uint64_t pol = policy_evict_first();
     uint32_t tc = 0;  // tiles through the ring (every role counts the same)
     bool ok = true;
     for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
         const int split = it / (nchunks * a.Hkv), g = (it / nchunks) % a.Hkv, ci = it % nchunks;
-        int L = 0;  // the group: the last leader whose chunk base is <= ci
-        {
-            int lo = 0, hi = a.batch - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (cbase[mid] <= ci) lo = mid; else hi = mid - 1;
-            }
-            L = lo;
-        }
+        const int L = chunk_leader(cbase, a.batch, ci);
         const int c = ci - cbase[L];
         __syncthreads();  // the previous item's member list is no longer read
         if (warp == 0) {
-            // Members of L with an entry, in batch order; this chunk's MPI of them.
-            int seen = 0;
-            for (int b0 = L; b0 < a.batch; b0 += 32) {
-                const int b = b0 + lane;
-                const bool m = b < a.batch && lead[b] == L && pe_s[b] >= 0;
-                const unsigned bal = __ballot_sync(FULL, m);
-                const int r = seen + __popc(bal & ((1u << lane) - 1u));
-                if (m && r >= c * MPI && r < (c + 1) * MPI) mem[r - c * MPI] = b;
-                seen += __popc(bal);
-                if (seen >= (c + 1) * MPI) break;
-            }
-            if (lane == 0) s_flag = min(MPI, seen - c * MPI);  // members in this chunk
+            const int n = chunk_members(L, c, MPI, a.batch, lead, pe_s, mem);
+            if (lane == 0) s_flag = n;  // members in this chunk
         }
         __syncthreads();
         const int nm = s_flag;
@@ -1348,6 +1366,332 @@ __global__ void __launch_bounds__(PFX_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Prefix kernel on the 5th-generation tensor cores (block sizes that are a
+// multiple of 64, so the shared prefix is whole 64-key tiles and a K or V
+// tile is one TMA box [2 halves][64 rows][128 B]).  A work item is 128 rows
+// -- 128 / G members x the G q heads of one kv head -- against one key
+// split of the group's prefix: S = Q.K^T (M = 128, N = 64, K = 128) into one
+// of two TMEM buffers, a row-per-thread online softmax (base 2, lazy
+// rescaling of O), P written back over S as bf16, O += P.V (P from TMEM).
+// Roles: warp 0 loads K and V tiles, warp 1 issues Q.K (and owns TMEM),
+// warp 2 issues P.V, warp 3 lists the item's members, warps 4..7 (TMEM lane
+// quarters 0..3) load Q, run the softmax and write the (m, l, o) partials.
+// ---------------------------------------------------------------------------
+constexpr int TCP_THREADS = 256;
+constexpr int TCP_W_LOAD = 0, TCP_W_QK = 1, TCP_W_PV = 2, TCP_W_MEM = 3, TCP_W_SOFT = 4;
+constexpr int TCP_ROWS = 128;
+constexpr int TCP_ST = 3;                               // K/V ring stages
+constexpr int TCP_KV = TILE * ROW_BYTES;                // one K or V tile: 16 KiB
+constexpr int TCP_QHALF = TCP_ROWS * 128;               // [128 rows][64 dims] of Q
+constexpr int TCP_OFF_Q = 0;                            // Q [2 halves][128 rows][128 B]
+constexpr int TCP_OFF_K = TCP_OFF_Q + 2 * TCP_QHALF;
+constexpr int TCP_OFF_V = TCP_OFF_K + TCP_ST * TCP_KV;
+constexpr int TCP_OFF_BAR = TCP_OFF_V + TCP_ST * TCP_KV;
+enum {
+    T_KFULL = 0, T_KEMPTY = T_KFULL + TCP_ST, T_VFULL = T_KEMPTY + TCP_ST, T_VEMPTY = T_VFULL + TCP_ST,
+    T_SFULL = T_VEMPTY + TCP_ST /* [2] */, T_PFULL = T_SFULL + 2 /* [2] */, T_PDONE = T_PFULL + 2 /* [2] */,
+    T_QFULL = T_PDONE + 2, T_QEMPTY, T_OEMPTY, T_DRAIN, T_DRAIN2, TCP_NBAR
+};
+constexpr int TCP_OFF_TMEM = TCP_OFF_BAR + TCP_NBAR * 8;
+constexpr int TCP_OFF_FLAGS = TCP_OFF_TMEM + 16;          // [0]: abort, [1]: members in the item
+constexpr int TCP_OFF_MEM = TCP_OFF_FLAGS + 16;           // the item's members [TCP_ROWS] int
+constexpr int TCP_OFF_WSUM = TCP_OFF_MEM + 4 * TCP_ROWS;  // scan scratch [8] uint32
+constexpr int TCP_OFF_ARR = TCP_OFF_WSUM + 64;            // ctx, ps, pe, lead, nmem, chunk base [batch + 1]
+__host__ __device__ constexpr size_t tcp_smem_bytes(int batch) { return TCP_OFF_ARR + 24 * (size_t)(batch + 1) + 1024; }
+static_assert(tcp_smem_bytes(kMaxBatchCascade) <= 232448, "tcgen05 prefix kernel shared memory");
+// The grouping scratch (a hash of 2 * 2048 ints for 1024 sequences, then
+// batch ints) lives in the K and V rings before the first copy.
+static_assert(4 * (2 * 2048 + kMaxBatchCascade) <= 2 * TCP_ST * TCP_KV, "grouping scratch fits in the rings");
+constexpr uint32_t TCP_TMEM_COLS = 256;                   // S [2][64 columns], O [128 columns]
+constexpr uint32_t TCP_COL_S = 0, TCP_COL_O = 128;
+constexpr uint32_t TCP_SBO = 1024;                        // 8 rows x 128 B between core-matrix groups
+constexpr uint32_t TCP_IDESC_S = idesc_bf16_f32(TCP_ROWS, TILE, false, false);  // Q, K both K-major
+constexpr uint32_t TCP_IDESC_PV = idesc_bf16_f32(TCP_ROWS, D, false, true);     // P from TMEM, V MN-major
+
+__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+template <int G>
+__global__ void __launch_bounds__(TCP_THREADS, 1)
+    decode_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                            const DecodeArgs a, float *pfx_o, float2 *pfx_ml) {
+    constexpr int MPI = TCP_ROWS / G;  // members per work item
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + TCP_OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + TCP_OFF_TMEM);
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + TCP_OFF_FLAGS);
+    int *mem = reinterpret_cast<int *>(smem + TCP_OFF_MEM);
+    uint32_t *wsum = reinterpret_cast<uint32_t *>(smem + TCP_OFF_WSUM);
+    int *ctx_s = reinterpret_cast<int *>(smem + TCP_OFF_ARR);
+    int *ps_s = ctx_s + (a.batch + 1), *pe_s = ps_s + (a.batch + 1), *lead = pe_s + (a.batch + 1);
+    int *nmem = lead + (a.batch + 1), *cbase = nmem + (a.batch + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < TCP_NBAR; ++i) {
+            const bool per_warp = i == T_PFULL || i == T_PFULL + 1 || i == T_QFULL || i == T_OEMPTY;
+            mbar_init(&bar[i], per_warp ? 4u : 1u);  // the four softmax warps arrive one each
+        }
+        flags[0] = 0;
+        fence_mbar_init();
+    }
+    if (warp == TCP_W_LOAD && lane == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+    }
+    if (warp == TCP_W_QK) {
+        tmem_alloc(tmem_slot, TCP_TMEM_COLS);
+        tmem_relinquish();
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The decode kernel launched behind this one may start its set-up; it
+    // reads the partials only after this grid has completed.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int nchunks =
+        prefix_setup(a, MPI, reinterpret_cast<int *>(smem + TCP_OFF_K), ctx_s, ps_s, pe_s, lead, nmem, cbase, wsum);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int nitems = nchunks * a.Hkv * kPrefixSplits;  // (split, kv head, chunk)
+    uint32_t tc = 0, ui = 0;  // tiles through the ring, items with tiles (every role counts the same)
+    bool ok = true, issued = false;
+    uint32_t nk = 0, nv = 0;  // copies issued (loader)
+    for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+        const int split = it / (nchunks * a.Hkv), g = (it / nchunks) % a.Hkv, ci = it % nchunks;
+        const int L = chunk_leader(cbase, a.batch, ci);
+        __syncthreads();  // the previous item's member list is no longer read
+        if (warp == TCP_W_MEM) {
+            const int n = chunk_members(L, ci - cbase[L], MPI, a.batch, lead, pe_s, mem);
+            if (lane == 0) flags[1] = n;
+        }
+        __syncthreads();
+        const int nm = flags[1];
+        const int ntall = ps_s[L] / TILE;  // the shared prefix: whole tiles
+        const int t0 = (int)((int64_t)ntall * split / kPrefixSplits);
+        const int nt = (int)((int64_t)ntall * (split + 1) / kPrefixSplits) - t0;
+        if (warp == TCP_W_LOAD) {
+            if (lane == 0) {
+                for (int j = 0; ok && j < nt; ++j) {
+                    const uint32_t gg = tc + j;
+                    const int st = gg % TCP_ST;
+                    const int p0 = (t0 + j) * TILE;
+                    const int blk = __ldg(a.block_tables + (int64_t)L * a.max_blocks + p0 / a.block_size);
+                    const int row = (blk < 0 || blk >= a.num_blocks) ? -2 * TILE : blk * a.block_size + p0 % a.block_size;
+                    if (!(ok = wait_or_abort(&bar[T_KEMPTY + st], ((gg / TCP_ST) & 1u) ^ 1u, flags, a, 160))) break;
+                    mbar_arrive_expect_tx(&bar[T_KFULL + st], TCP_KV);
+                    tma_load_4d_plain(smem + TCP_OFF_K + st * TCP_KV, &tmk, 0, row, 0, g, &bar[T_KFULL + st]);
+                    ++nk;
+                    if (!(ok = wait_or_abort(&bar[T_VEMPTY + st], ((gg / TCP_ST) & 1u) ^ 1u, flags, a, 161))) break;
+                    mbar_arrive_expect_tx(&bar[T_VFULL + st], TCP_KV);
+                    tma_load_4d_plain(smem + TCP_OFF_V + st * TCP_KV, &tmv, 0, row, 0, g, &bar[T_VFULL + st]);
+                    ++nv;
+                }
+            }
+        } else if (warp == TCP_W_QK) {
+            if (lane == 0 && nt > 0) {
+                ok = ok && wait_or_abort(&bar[T_QFULL], ui & 1u, flags, a, 162);
+                tc_fence_after();
+                const uint64_t qdesc = smem_desc_sw128(smem_addr(smem + TCP_OFF_Q), 16, TCP_SBO);
+                for (int j = 0; ok && j < nt; ++j) {
+                    const uint32_t gg = tc + j;
+                    const int st = gg % TCP_ST, b = gg & 1;
+                    if (!(ok = wait_or_abort(&bar[T_KFULL + st], (gg / TCP_ST) & 1u, flags, a, 163))) break;
+                    // S(b) is free once the P.V that read it two tiles ago has completed.
+                    if (!(ok = wait_or_abort(&bar[T_PDONE + b], ((gg >> 1) & 1u) ^ 1u, flags, a, 164))) break;
+                    tc_fence_after();
+                    const uint64_t kdesc = smem_desc_sw128(smem_addr(smem + TCP_OFF_K + st * TCP_KV), 16, TCP_SBO);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t qo = (uint64_t)(((kk >> 2) * TCP_QHALF + (kk & 3) * 32) >> 4);
+                        const uint64_t ko = (uint64_t)(((kk >> 2) * (TCP_KV / 2) + (kk & 3) * 32) >> 4);
+                        mma_bf16_ss(tmem + TCP_COL_S + b * TILE, qdesc + qo, kdesc + ko, TCP_IDESC_S, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bar[T_SFULL + b]);
+                    mma_commit(&bar[T_KEMPTY + st]);
+                    issued = true;
+                }
+                if (ok) mma_commit(&bar[T_QEMPTY]);  // every Q.K of the item has read Q
+            }
+        } else if (warp == TCP_W_PV) {
+            if (lane == 0 && nt > 0) {
+                for (int j = 0; ok && j < nt; ++j) {
+                    const uint32_t gg = tc + j;
+                    const int st = gg % TCP_ST, b = gg & 1;
+                    if (!(ok = wait_or_abort(&bar[T_VFULL + st], (gg / TCP_ST) & 1u, flags, a, 165))) break;
+                    // O is free once the previous item's partials were read out of it.
+                    if (j == 0 && !(ok = wait_or_abort(&bar[T_OEMPTY], (ui & 1u) ^ 1u, flags, a, 166))) break;
+                    if (!(ok = wait_or_abort(&bar[T_PFULL + b], (gg >> 1) & 1u, flags, a, 167))) break;
+                    tc_fence_after();
+                    const uint64_t vdesc =
+                        smem_desc_sw128(smem_addr(smem + TCP_OFF_V + st * TCP_KV), TCP_KV / 2, TCP_SBO);
+#pragma unroll
+                    for (int kk = 0; kk < TILE / 16; ++kk)  // 16 keys per step = 8 TMEM columns of P
+                        mma_bf16_ts(tmem + TCP_COL_O, tmem + TCP_COL_S + b * TILE + kk * 8,
+                                    vdesc + (uint64_t)((kk * 16 * 128) >> 4), TCP_IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bar[T_PDONE + b]);
+                    mma_commit(&bar[T_VEMPTY + st]);
+                    issued = true;
+                }
+            }
+        } else if (warp >= TCP_W_SOFT) {
+            const int quarter = warp & 3;
+            const int row = quarter * 32 + lane;  // item row == TMEM lane
+            const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+            const float sl = a.scale_log2;
+            const int mrow = row / G, hrow = g * G + row % G;  // member slot and q head of the row
+            const int brow = mrow < nm ? mem[mrow] : -1;
+            auto wwait = [&](uint64_t *bb, uint32_t parity, int where) -> bool {
+                return __all_sync(FULL, wait_or_abort(bb, parity, flags, a, where));
+            };
+            float m_run = -INFINITY, l_run = 0.f;
+            if (nt > 0 && ok) {
+                // Q rows of the item (zeros for rows past the members), once the
+                // previous item's Q.K products have read the tile.
+                if ((ok = wwait(&bar[T_QEMPTY], (ui & 1u) ^ 1u, 170))) {
+                    const uint4 *src =
+                        reinterpret_cast<const uint4 *>(a.q + (int64_t)max(brow, 0) * a.q_row_stride + (int64_t)hrow * D);
+                    const uint32_t qs = smem_addr(smem + TCP_OFF_Q);
+                    uint4 v[16];  // all loads in flight before the first store
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) v[c] = brow >= 0 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        st_shared_u4(qs + (uint32_t)((c >> 3) * TCP_QHALF + row * 128 + (((c & 7) ^ (row & 7)) << 4)),
+                                     v[c]);
+                    fence_proxy_async_smem();  // the MMA reads Q through the async proxy
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar[T_QFULL]);
+                }
+            }
+            for (int j = 0; ok && j < nt; ++j) {
+                const uint32_t gg = tc + j;
+                const int b = gg & 1;
+                const uint32_t cs = t_lane + TCP_COL_S + b * TILE;
+                if (!(ok = wwait(&bar[T_SFULL + b], (gg >> 1) & 1u, 171))) break;
+                tc_fence_after();
+                uint32_t r[TILE];
+                tmem_ld32(cs, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                tmem_ld32(cs + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                tmem_ld_wait();
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int k2 = 0; k2 < TILE / 2; ++k2)
+                    m4[k2 & 3] = max3(m4[k2 & 3], __uint_as_float(r[2 * k2]), __uint_as_float(r[2 * k2 + 1]));
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                // Lazy rescaling: the reference max moves only when a score
+                // exceeds it by more than 2^kLazyRescale.
+                const bool grow = (mx - m_run) * sl > kLazyRescale;
+                const float m_new = grow ? mx : m_run;
+                const float alpha = grow ? fast_exp2((m_run - m_new) * sl) : 1.f;
+                if (j > 0 && __any_sync(FULL, grow)) {
+                    // O must hold P.V up to the previous tile before it is rescaled.
+                    if (!(ok = wwait(&bar[T_PDONE + ((gg - 1) & 1)], ((gg - 1) >> 1) & 1u, 172))) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(t_lane + TCP_COL_O + c * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(t_lane + TCP_COL_O + c * 32, o);
+                    }
+                }
+                l_run *= alpha;
+                m_run = m_new;
+                const float neg_m = -m_run * sl;
+                float rs[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[TILE / 2];
+#pragma unroll
+                for (int k2 = 0; k2 < TILE / 2; ++k2) {
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(r[2 * k2]), sl, neg_m));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(r[2 * k2 + 1]), sl, neg_m));
+                    rs[k2 & 3] += p0 + p1;
+                    pk[k2] = pack_bf16(p0, p1);
+                }
+                tmem_st32(cs, pk);  // P over the first 32 columns of S(b)
+                tmem_st_wait();
+                l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[T_PFULL + b]);
+            }
+            // ---- the rows' partials: (m, l) in base 2 and unnormalised o
+            if (nt > 0 && ok) {
+                const uint32_t gl = tc + nt - 1;  // the item's last tile
+                if ((ok = wwait(&bar[T_PDONE + (gl & 1)], (gl >> 1) & 1u, 173))) {
+                    tc_fence_after();
+                    uint32_t o[D];
+                    tmem_ld32(t_lane + TCP_COL_O, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+                    tmem_ld32(t_lane + TCP_COL_O + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+                    tmem_ld32(t_lane + TCP_COL_O + 64, *reinterpret_cast<uint32_t(*)[32]>(&o[64]));
+                    tmem_ld32(t_lane + TCP_COL_O + 96, *reinterpret_cast<uint32_t(*)[32]>(&o[96]));
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar[T_OEMPTY]);  // O may be overwritten by the next item
+                    // Rows through shared memory (the rings are idle: every tile of
+                    // the item was consumed and the next item's copies start after
+                    // the item barrier), so that each warp writes whole 512-byte rows.
+                    // Staging row r at r * 528 B: 16-byte chunks of consecutive rows
+                    // fall in different banks.
+                    const uint32_t stg = smem_addr(smem + TCP_OFF_K) + (uint32_t)(quarter * 32) * 528u;
+#pragma unroll
+                    for (int c = 0; c < D / 4; ++c)
+                        st_shared_u4(stg + (uint32_t)lane * 528u + 16u * c, make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
+                    const int64_t rg_me =
+                        brow >= 0 ? (int64_t)split * kMaxPrefixRows + (int64_t)pe_s[brow] * a.Hq + hrow : -1;
+                    if (rg_me >= 0) pfx_ml[rg_me] = make_float2(m_run * sl, l_run);
+                    __syncwarp();
+                    for (int rr = 0; rr < 32; ++rr) {  // the warp's rows, one at a time
+                        const int64_t rg = __shfl_sync(FULL, rg_me, rr);
+                        if (rg < 0) continue;
+                        uint4 w;
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                                     : "r"(stg + (uint32_t)rr * 528u + 16u * lane));
+                        reinterpret_cast<uint4 *>(pfx_o + rg * D)[lane] = w;
+                    }
+                    fence_proxy_async_smem();  // the next item's copies write this memory
+                }
+            } else if (nt == 0 && brow >= 0) {
+                // A split with no tile leaves (-inf, 0, 0): the merge skips it.
+                const int64_t rg = (int64_t)split * kMaxPrefixRows + (int64_t)pe_s[brow] * a.Hq + hrow;
+                float4 *dst = reinterpret_cast<float4 *>(pfx_o + rg * D);
+                for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                pfx_ml[rg] = make_float2(-INFINITY, 0.f);
+            }
+        }
+        tc += nt;
+        if (nt > 0) ++ui;
+    }
+    // ---- wind-down: nothing in flight may outlive the CTA's shared memory or TMEM
+    if (warp == TCP_W_LOAD && lane == 0 && !ok) {
+        for (uint32_t x = (nk >= (uint32_t)TCP_ST ? nk - TCP_ST : 0); x < nk; ++x)
+            (void)mbar_wait(&bar[T_KFULL + x % TCP_ST], (x / TCP_ST) & 1u);
+        for (uint32_t x = (nv >= (uint32_t)TCP_ST ? nv - TCP_ST : 0); x < nv; ++x)
+            (void)mbar_wait(&bar[T_VFULL + x % TCP_ST], (x / TCP_ST) & 1u);
+    }
+    if ((warp == TCP_W_QK || warp == TCP_W_PV) && lane == 0 && flags[0] && issued) {
+        uint64_t *dr = &bar[warp == TCP_W_QK ? T_DRAIN : T_DRAIN2];
+        mma_commit(dr);
+        (void)mbar_wait(dr, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == TCP_W_QK) tmem_dealloc(tmem, TCP_TMEM_COLS);
+}
+
 // Per (device, instantiation): the shared-memory attribute has been set.
 // Two threads making their first call together may both set it (the call is
 // idempotent); the flag itself is an atomic, so there is no data race.
@@ -1373,6 +1717,7 @@ pa_status launch(const DecodeArgs &a, const CUtensorMap &tk, const CUtensorMap &
 }
 
 std::atomic<int> g_pfx_attr_done[64][4];
+std::atomic<int> g_tcp_attr_done[64][4];
 
 // The prefix kernel for shared prefixes, launched (programmatic dependent
 // launch) right before the decode kernel that folds its partials in.
@@ -1387,13 +1732,26 @@ pa_status launch_prefix(const DecodeArgs &a, const CUtensorMap &tk, const CUtens
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_prefix_kernel)");
         g_pfx_attr_done[dev][gi].store(1, std::memory_order_release);
     }
-    // Work items: (kv head, chunk of PFX_ROWS / G members of one group); at
+    // Work items: (key split, kv head, chunk of MPI members of one group); at
     // most batch / 2 groups and batch members.
-    constexpr int MPI = PFX_ROWS / G;
-    const int64_t bound = (int64_t)a.Hkv * kPrefixSplits * ((a.batch + MPI - 1) / MPI + a.batch / 2);
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, bound));
-    return launch_pdl(decode_prefix_kernel<G>, dim3((unsigned)grid), dim3(PFX_THREADS), pfx_smem_bytes(a.batch), st,
-                      "decode_prefix_kernel", tk, tv, a, const_cast<float *>(a.pfx_o), const_cast<float2 *>(a.pfx_ml));
+    auto grid_for = [&](int mpi) {
+        const int64_t bound = (int64_t)a.Hkv * kPrefixSplits * ((a.batch + mpi - 1) / mpi + a.batch / 2);
+        return (int)std::max<int64_t>(1, std::min<int64_t>(sms, bound));
+    };
+    if (a.box_rows == TILE) {  // whole 64-key tiles: the tensor-core kernel
+        if (dev >= 0 && dev < 64 && !g_tcp_attr_done[dev][gi].load(std::memory_order_acquire)) {
+            cudaError_t e = cudaFuncSetAttribute(decode_prefix_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)tcp_smem_bytes(kMaxBatchCascade));
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode_prefix_tc_kernel)");
+            g_tcp_attr_done[dev][gi].store(1, std::memory_order_release);
+        }
+        return launch_pdl(decode_prefix_tc_kernel<G>, dim3((unsigned)grid_for(TCP_ROWS / G)), dim3(TCP_THREADS),
+                          tcp_smem_bytes(a.batch), st, "decode_prefix_tc_kernel", tk, tv, a,
+                          const_cast<float *>(a.pfx_o), const_cast<float2 *>(a.pfx_ml));
+    }
+    return launch_pdl(decode_prefix_kernel<G>, dim3((unsigned)grid_for(PFX_ROWS / G)), dim3(PFX_THREADS),
+                      pfx_smem_bytes(a.batch), st, "decode_prefix_kernel", tk, tv, a, const_cast<float *>(a.pfx_o),
+                      const_cast<float2 *>(a.pfx_ml));
 }
 
 template <int G>

@@ -115,6 +115,32 @@ def test_shared_prefix_large_group():
     check(inp)
 
 
+def test_shared_prefix_one_block_of_64():
+    """A shared prefix of one 64-key tile: three of the four key splits have
+    no tile and leave empty partials."""
+    ctx = [200, 65, 130, 300]
+    inp = make_decode("one tile", 46, len(ctx), 32, 8, ctx, block_size=64)
+    share(inp, [(0, [1, 2, 3], 1)])
+    check(inp)
+
+
+def test_shared_prefix_two_chunks_gqa1():
+    """GQA group 1: 128 members per work item, so 140 members need two."""
+    rng = np.random.default_rng(47)
+    ctx = list(rng.integers(2 * 256 + 1, 1200, size=140))
+    inp = make_decode("gqa1 140", 47, len(ctx), 8, 8, ctx, shared_prefix_seqs=140, shared_prefix_blocks=2)
+    check(inp)
+
+
+def test_shared_prefix_members_past_the_partial_rows():
+    """64 q heads: 8192 partial rows hold 128 members; the other 12 members of
+    the group read the shared prefix themselves."""
+    rng = np.random.default_rng(48)
+    ctx = list(rng.integers(2 * 256 + 1, 900, size=140))
+    inp = make_decode("cap", 48, len(ctx), 64, 8, ctx, shared_prefix_seqs=140, shared_prefix_blocks=2)
+    check(inp)
+
+
 def test_shared_prefix_without_sharing_equals_pa_decode():
     inp = decode_config(2)  # no shared blocks
     kc, vc = dev_bf16(inp.k_cache), dev_bf16(inp.v_cache)
