@@ -614,7 +614,7 @@ def run_ours(args):
             "config": {"workload": WORKLOAD, "global_batch": inp.batch * ws, "seq_len": "lognormal(1024), cap 8192",
                        "parallelism": f"replicas x{ws}", "l2": L2},
             "roofline": {"bound": "hbm",
-                         "kernel": "decode_prefix_kernel<4> + decode_kernel<4, store> (one pa_decode_shared_prefix call)",
+                         "kernel": "decode_prefix_tc_kernel<4> + decode_kernel<4, store> (one pa_decode_shared_prefix call)",
                          "achieved": achieved,
                          "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
                          "frac_of_nominal_8TBps": achieved / 8000.0, "traffic": traffic,
