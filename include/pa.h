@@ -155,7 +155,7 @@ PA_API pa_status pa_slot_mapping_prefill(int32_t *slot_mapping, const int32_t *b
 /*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs.
  * It depends only on the GQA group (num_q_heads / num_kv_heads) and is at
- * most about 6.4 MB; 0 for shapes pa_decode does not support.
+ * most about 4.3 MB; 0 for shapes pa_decode does not support.
  */
 PA_API size_t pa_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim);
 
