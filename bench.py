@@ -750,6 +750,9 @@ def run_profile_case(args):
     decode-qwen3-8b: the headline workload itself (about 2.4 GB on the
     device; pa_decode_shared_prefix: a prefix kernel and a decode kernel
     per call), for single-pass captures (DRAM bytes and duration).
+    decode-shared-small: the same shape at batch 64 (32/8 heads, lognormal
+    contexts, sequences 0..31 share their first 4 blocks; about 0.4 GB of
+    K/V), pa_decode_shared_prefix, for multi-pass captures of both kernels.
     prefill: the prefill workload (plain prefill launches after one store).
     Each runs `warmup` then `steps` launches with an L2 flush before each."""
     import torch
@@ -775,13 +778,19 @@ def run_profile_case(args):
     if args.profile_case == "decode-small":
         rng = np.random.default_rng(1002)
         inp = make_decode("qwen3-0.6b decode b64 h16/8 ctx~U[1,1536]", 2, 64, 16, 8, rng.integers(1, 1537, size=64))
+    elif args.profile_case == "decode-shared-small":
+        rng = np.random.default_rng(1003)
+        ctx = np.clip(np.round(1024.0 * np.exp(rng.standard_normal(64))), 1, 8192).astype(np.int64)
+        ctx[:32] = np.maximum(ctx[:32], 4 * 256 + 1)
+        inp = make_decode("qwen3-8b shape b64 h32/8 ctx~lognormal(1024) 32 seqs share 4 blocks", 3, 64, 32, 8, ctx,
+                          shared_prefix_seqs=32, shared_prefix_blocks=4)
     else:
         inp = decode_config(HEADLINE_CONFIG)
     kc, vc, q = _to_dev(inp.k_cache, dev, True), _to_dev(inp.v_cache, dev, True), _to_dev(inp.q, dev, True)
     nk, nv = _to_dev(inp.new_k, dev, True), _to_dev(inp.new_v, dev, True)
     bt, ctx = _to_dev(inp.block_tables, dev), _to_dev(inp.context_lens, dev)
     out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
-    shared = args.profile_case == "decode-qwen3-8b"  # the headline call: shared prefix grouped
+    shared = args.profile_case in ("decode-qwen3-8b", "decode-shared-small")  # shared prefix grouped
     wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev, shared_prefix=shared)
     for _ in range(args.warmup + args.steps):
         flush.zero_()
@@ -807,7 +816,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--report", action="store_true",
                     help="print the per-configuration results table (markdown) instead of the JSON line")
-    ap.add_argument("--profile-case", choices=["decode-small", "decode-qwen3-8b", "prefill"], default=None,
+    ap.add_argument("--profile-case", choices=["decode-small", "decode-qwen3-8b", "decode-shared-small", "prefill"],
+                    default=None,
                     help="run only a small launch sequence for an ncu capture (no JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
