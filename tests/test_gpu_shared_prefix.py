@@ -81,7 +81,7 @@ def test_shared_prefix_interleaved_groups(store):
     check(inp, store=store)
 
 
-@pytest.mark.parametrize("B", [16, 48, 64, 256])
+@pytest.mark.parametrize("B", [16, 48, 64, 128, 256, 512])
 def test_shared_prefix_block_sizes(B):
     ctx = [9 * B + 5, 6 * B + 1, 7 * B + 30, 4 * B + 2, 12 * B]
     inp = make_decode(f"B={B}", 42 + B, len(ctx), 16, 8, ctx, block_size=B)
