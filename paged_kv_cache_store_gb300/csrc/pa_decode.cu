@@ -115,6 +115,8 @@ struct Cfg {
     static constexpr int OFF_SIDE = OFF_WSUM + 64;
     static constexpr int OFF_ZERO = OFF_SIDE + 2 * NCW * ROW_BYTES;
     static constexpr int OFF_CUM = OFF_ZERO + ROW_BYTES;   // per-head tile prefix sum [batch + 1] uint32
+    static_assert(OFF_SIDE % 16 == 0 && OFF_ZERO % 16 == 0, "ldmatrix reads these rows: 16-byte aligned");
+    static_assert(OFF_Q % 16 == 0 && OFF_SLOT % 16 == 0, "vector accesses: 16-byte aligned");
     __host__ __device__ static constexpr size_t off_ctx(int batch) { return OFF_CUM + 4 * (size_t)(batch + 1); }  // [batch] int
     // With shared prefixes: per sequence its first streamed position and its
     // prefix-partial entry ([batch] int each).
