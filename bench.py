@@ -10,8 +10,9 @@ store fused: a prefix kernel attends the 128 sharing sequences' query heads to
 their 4 shared blocks once per kv head, then the split-KV GQA decode kernel
 stores each sequence's new K/V row to its slot, reads every other context row
 through the block tables and merges the prefix partials.  All inputs are
-resident in HBM before the timed region; L2 is flushed (a 256 MiB write)
-before every timed step.  `value` is decode tokens/s (one layer) over all
+resident in HBM before the timed region; L2 is flushed before every timed
+step (a 256 MiB write, then a 256 MiB read of another buffer, so that the
+step starts with no line of its inputs and no dirty line in L2).  `value` is decode tokens/s (one layer) over all
 ranks; `e2e` is the same metric through the public API with the step's
 inputs copied from pinned host memory and the output copied back inside the
 timed region.  The roofline counts the bytes the step must move with every
@@ -74,7 +75,8 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
-DECODE_SOURCES = ["paged_kv_cache_store_gb300/csrc/pa_decode.cu", "paged_kv_cache_store_gb300/csrc/pa_internal.cuh"]
+DECODE_SOURCES = ["paged_kv_cache_store_gb300/csrc/pa_decode.cu", "paged_kv_cache_store_gb300/csrc/pa_tcgen05.cuh",
+                  "paged_kv_cache_store_gb300/csrc/pa_internal.cuh"]
 PREFILL_SOURCES = ["paged_kv_cache_store_gb300/csrc/pa_prefill.cu", "paged_kv_cache_store_gb300/csrc/pa_tcgen05.cuh",
                    "paged_kv_cache_store_gb300/csrc/pa_internal.cuh"]
 
@@ -303,12 +305,32 @@ def _to_dev(a, dev, bf=False):
     return (t.view(torch.bfloat16) if bf else t).to(dev)
 
 
+class L2Flush:
+    """Leaves L2 cold and clean before a timed call: a 256 MiB write evicts
+    every line the call could reuse, then a 256 MiB read of a second buffer
+    writes the first buffer's dirty lines back to HBM before the timed region
+    starts.  After the write alone, L2 (129 MB) is full of dirty lines and
+    the timed call would pay for writing them back as its first reads
+    allocate lines (3-7 us on the decode workloads)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+        self.s = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.s)
+
+
 def _event_times(fn, steps, stream, flush):
     """Per-call CUDA-event times (ms) of `steps` calls of fn, L2 flushed before each."""
     import torch
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a_, b_ in ev:
-        flush.zero_()
+        flush()
         a_.record(stream)
         fn()
         b_.record(stream)
@@ -390,7 +412,7 @@ def measure_prefill(args, dev, stream, flush, bf16_peak):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     torch.cuda.synchronize()
     for e in evs:
-        flush.zero_()
+        flush()
         step(e)
     torch.cuda.synchronize()
     _check_device(pa)
@@ -448,7 +470,7 @@ def measure_sampler(args, dev, stream, flush, hbm_peak):
     return {"workload": sp.name + ", fp32 Exp(1) draws", "ms": ms, "algorithmic_bytes": alg,
             "roofline": {"bound": "hbm", "kernel": "sample_gumbel_kernel", "achieved": gbs, "peak": hbm_peak,
                          "unit": "GB/s", "frac": gbs / hbm_peak, "traffic": None},
-            "l2": "flushed (256 MiB write) before every timed call; inputs 58 MB"}
+            "l2": "flushed (256 MiB write + 256 MiB read) before every timed call; inputs 58 MB"}
 
 
 def run_ours(args):
@@ -473,10 +495,10 @@ def run_ours(args):
     out = torch.empty(inp.batch, inp.num_q_heads, inp.head_dim, dtype=torch.bfloat16, device=dev)
     wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev)
     wsx = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev, shared_prefix=True)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     by = decode_bytes(inp)
-    L2 = (f"flushed (256 MiB write) before every timed step; K/V pool {kc.numel() * 4 / 2**30:.2f} GiB > L2")
+    L2 = (f"flushed (256 MiB write + 256 MiB read) before every timed step; K/V pool {kc.numel() * 4 / 2**30:.2f} GiB > L2")
 
     def step():  # prefix kernel + decode kernel (which stores the new K/V rows, then attends)
         pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsx, out=out, new_k=nk, new_v=nv, shared_prefix=True)
@@ -499,7 +521,7 @@ def run_ours(args):
     def flushed_steps(n):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         for a_, b_ in ev:
-            flush.zero_()
+            flush()
             a_.record(stream)
             step()
             b_.record(stream)
@@ -538,7 +560,7 @@ def run_ours(args):
     # The plain decode launch alone (store done before it).
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         pa.slot_mapping_decode(bt, ctx, inp.block_size, out=slots)
         kev[i][0].record(stream)
         pa.store_kvcache(nk, nv, kc, vc, slots)
@@ -578,7 +600,7 @@ def run_ours(args):
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps + 2):
         if i >= 2:
-            flush.zero_()
+            flush()
             e2e_ev[i - 2][0].record(stream)
         d_pack.copy_(h_pack, non_blocking=True)
         pa.decode(e_q, kc, vc, e_bt, e_ctx, inp.scale, workspace=wsx, out=out, new_k=e_nk, new_v=e_nv,
@@ -595,7 +617,7 @@ def run_ours(args):
     del kc, vc, flush
     torch.cuda.empty_cache()
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     sub = {}
     for cfg in SUB_DECODE_CONFIGS:
         sub[f"decode_config{cfg}"] = measure_decode_config(cfg, args, dev, stream, flush, hbm)
@@ -666,7 +688,7 @@ def run_report(args):
     nthr = OP.host_threads()
     dev = torch.device("cuda", 0)
     hbm, bf16_peak, kind = peaks()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     def timed(fn):
@@ -759,7 +781,7 @@ def run_profile_case(args):
     import paged_kv_cache_store_gb300 as pa
     from paged_kv_cache_store_gb300.workloads import make_decode, decode_config, prefill_config
     dev = torch.device("cuda", 0)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     if args.profile_case == "prefill":
         p = prefill_config(5)
         kc, vc, q = _to_dev(p.k_cache, dev, True), _to_dev(p.v_cache, dev, True), _to_dev(p.q, dev, True)
@@ -769,7 +791,7 @@ def run_profile_case(args):
         out = torch.empty(p.total_q, p.num_q_heads, p.head_dim, dtype=torch.bfloat16, device=dev)
         mq, mk = int(p.seqlens_q.max()), int(p.seqlens_k.max())
         for _ in range(args.warmup + args.steps):
-            flush.zero_()
+            flush()
             pa.prefill_varlen(q, kc, vc, cq, ck, mq, mk, p.scale, block_tables=bt, out=out)
         torch.cuda.synchronize()
         _check_device(pa)
@@ -793,7 +815,7 @@ def run_profile_case(args):
     shared = args.profile_case in ("decode-qwen3-8b", "decode-shared-small")  # shared prefix grouped
     wsp = pa.decode_workspace(inp.num_q_heads, inp.num_kv_heads, inp.head_dim, dev, shared_prefix=shared)
     for _ in range(args.warmup + args.steps):
-        flush.zero_()
+        flush()
         pa.decode(q, kc, vc, bt, ctx, inp.scale, workspace=wsp, out=out, new_k=nk, new_v=nv, shared_prefix=shared)
     torch.cuda.synchronize()
     _check_device(pa)
