@@ -7,13 +7,17 @@
 //
 // How (GB300 design):
 //  * Work is a flat list of 64-position tiles ordered (sequence, kv head,
-//    tile).  Its first 7/8 is cut into one contiguous range per CTA of a
-//    persistent grid (one CTA per SM); the last 1/8 into small chunk ranges
-//    that CTAs take from an atomic counter once their own range is done, so
-//    the CTAs that stream faster absorb the tail.  A range holds whole
-//    (sequence, kv head) segments in its middle and at most one part-segment
-//    at each end.  Every CTA rebuilds the per-sequence tile counts and their
-//    prefix sum from context_lens in shared memory.
+//    tile), cut into one contiguous share per CTA of a persistent grid (one
+//    CTA per SM).  The shares are equal in cost, not in tiles: a (sequence,
+//    kv head) pair costs 1.5 tiles' worth on top of its tiles (its q rows,
+//    block-id fetch and merge), so a CTA whose share holds many short pairs
+//    streams fewer tiles.  The first 7/8 of each share is the CTA's own
+//    range; the last 1/8 a tail range that CTAs take from an atomic counter
+//    once their own range is done, so the CTAs that stream faster absorb the
+//    tail.  A range holds whole (sequence, kv head) segments in its middle
+//    and at most one part-segment at each end.  Every CTA rebuilds the
+//    per-sequence tile counts, their costs and both prefix sums from
+//    context_lens in shared memory, then the table of range starts.
 //  * Two producer warps issue TMA tile loads (cp.async.bulk.tensor, 64 rows x
 //    256 B per K or V tile; a row is one token of one kv head) into a
 //    4-stage shared-memory ring guarded by mbarriers: one warp the K tiles
@@ -73,6 +77,15 @@ constexpr int kPrefixSplits = 2;         // the shared prefix's tiles are cut in
 constexpr int kMaxGrid = 256;     // CTAs of the persistent grid (min(SMs, this))
 constexpr int kMaxRanges = 2 * kMaxGrid;  // a head and a tail range per CTA
 constexpr int kTailShift = 3;  // a CTA's tail range is 1/8 of its share
+// The work is split by cost, not by tiles: a (sequence, kv head) pair costs
+// kCostTile per tile plus kCostPair for the work it carries whatever its
+// length (its q rows, its block-id fetch, the merge of its result and, for
+// a member of a shared prefix, the fold of the prefix partial).
+#ifndef PA_PAIR_COST
+#define PA_PAIR_COST 6
+#endif
+constexpr int kCostTile = 4;
+constexpr int kCostPair = PA_PAIR_COST;
 constexpr int NTK = 4;            // tickets in flight (ranges handed from the K warp to the others)
 constexpr int kMinTilesPerCta = 8;  // grid = min(SMs, tile bound / this)
 constexpr unsigned FULL = 0xffffffffu;
@@ -114,7 +127,8 @@ struct Cfg {
     // keys past the context.  Never written by TMA.
     static constexpr int OFF_SIDE = OFF_WSUM + 64;
     static constexpr int OFF_ZERO = OFF_SIDE + 2 * NCW * ROW_BYTES;
-    static constexpr int OFF_CUM = OFF_ZERO + ROW_BYTES;   // per-head tile prefix sum [batch + 1] uint32
+    static constexpr int OFF_RT = OFF_ZERO + ROW_BYTES;    // range starts [2 * kMaxGrid + 1] int64
+    static constexpr int OFF_CUM = OFF_RT + (8 * (2 * kMaxGrid + 1) + 15) / 16 * 16;  // per-head tile prefix sum [batch + 1] uint32
     static_assert(OFF_SIDE % 16 == 0 && OFF_ZERO % 16 == 0, "ldmatrix reads these rows: 16-byte aligned");
     static_assert(OFF_Q % 16 == 0 && OFF_SLOT % 16 == 0, "vector accesses: 16-byte aligned");
     __host__ __device__ static constexpr size_t off_ctx(int batch) { return OFF_CUM + 4 * (size_t)(batch + 1); }  // [batch] int
@@ -173,34 +187,25 @@ __device__ __forceinline__ int clamp_ctx(const DecodeArgs &a, int b, bool report
 }
 
 // The tiles of pair (b, g) are [Hkv*CT_b + g*nt_b, ... + nt_b) in the flat
-// list, nt_b = ceil(ctx_b / TILE), CT_b = sum_{b' < b} nt_b'.  CTA j's share
-// is base + (j < rem) tiles from j*base + min(j, rem); its last 1/8 (the
-// tail) is a separate range that any CTA may take from the tail counter once
-// its own head range is done.  Range 2j is CTA j's head, 2j+1 its tail, so
-// range indices follow the flat order (a range may be empty).
-struct Split {
-    long long base, rem;
+// list, nt_b = ceil(ctx_b / TILE), CT_b = sum_{b' < b} nt_b'.  The list is
+// cut into 2 * grid ranges that follow the flat order: range 2j is CTA j's
+// head, 2j+1 its tail, a separate range that any CTA may take from the tail
+// counter once its own head range is done (a range may be empty).  The cuts
+// divide the list's cost (kCostTile per tile, kCostPair per pair) into equal
+// shares, a tail being 1/8 of its CTA's share; st[r] is the first tile of
+// range r and st[2 * grid] the number of tiles.
+struct Ranges {
+    const long long *st;
     int grid;
-    __device__ void init(long long total, int grid_) {
-        grid = grid_;
-        base = total / grid;
-        rem = total % grid;
-    }
-    __device__ long long cta_start(int j) const { return (long long)j * base + min((long long)j, rem); }
-    __device__ long long cta_len(int j) const { return base + (j < rem ? 1 : 0); }
-    __device__ long long tail_len(int j) const { return cta_len(j) >> kTailShift; }
-    __device__ long long start(int r) const {
-        const int j = r >> 1;
-        return cta_start(j) + ((r & 1) ? cta_len(j) - tail_len(j) : 0);
-    }
-    __device__ long long len(int r) const {
-        const int j = r >> 1;
-        return (r & 1) ? tail_len(j) : cta_len(j) - tail_len(j);
-    }
+    __device__ long long start(int r) const { return st[r]; }
+    __device__ long long len(int r) const { return st[r + 1] - st[r]; }
     __device__ int owner(long long x) const {  // the (non-empty) range holding tile x
-        const long long cut = rem * (base + 1);
-        const int j = (int)(x < cut ? x / (base + 1) : rem + (x - cut) / base);
-        return 2 * j + (x >= cta_start(j) + cta_len(j) - tail_len(j) ? 1 : 0);
+        int lo = 0, hi = 2 * grid - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (st[mid] <= x) lo = mid; else hi = mid - 1;
+        }
+        return lo;
     }
 };
 
@@ -476,8 +481,12 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (threadIdx.x < ROW_BYTES / 16) st_shared_zero16(smem_addr(smem + C::OFF_ZERO) + 16 * threadIdx.x);
-    // Per-sequence tile counts and their exclusive prefix sum: each thread
-    // takes a run of `per` sequences, then a block-wide scan of the run sums.
+    // Per-sequence tile counts and their exclusive prefix sum, and the same
+    // for the sequences' costs (per kv head): each thread takes a run of `per`
+    // sequences, then a block-wide scan of the run sums.  The cost sums live
+    // in the first ring stage, which no copy writes before the set-up ends.
+    unsigned long long *ccum = reinterpret_cast<unsigned long long *>(smem);  // [batch + 1]
+    unsigned long long *wsum_c = ccum + kMaxBatch + 1;                         // [NWARPS]
     {
         const int per = (a.batch + C::NTHREADS - 1) / C::NTHREADS;
         const int b0 = threadIdx.x * per, b1 = min(a.batch, b0 + per);
@@ -494,28 +503,89 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
         auto ntiles = [&](int b) -> uint32_t {
             return (uint32_t)((ctx_s[b] - (ps_s ? ps_s[b] : 0) + TILE - 1) / TILE);
         };
+        auto cost = [&](uint32_t n) -> unsigned long long {
+            return n ? (unsigned long long)kCostTile * n + kCostPair : 0ull;
+        };
         uint32_t run = 0;
-        for (int b = b0; b < b1; ++b) run += ntiles(b);
+        unsigned long long runc = 0;
+        for (int b = b0; b < b1; ++b) {
+            const uint32_t n = ntiles(b);
+            run += n;
+            runc += cost(n);
+        }
         uint32_t x = run;
+        unsigned long long xc = runc;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(FULL, x, o);
-            if (lane >= o) x += y;
+            const unsigned long long yc = __shfl_up_sync(FULL, xc, o);
+            if (lane >= o) {
+                x += y;
+                xc += yc;
+            }
         }
-        if (lane == 31) wsum[warp] = x;
+        if (lane == 31) {
+            wsum[warp] = x;
+            wsum_c[warp] = xc;
+        }
         __syncthreads();
         uint32_t before = 0;
-        for (int w2 = 0; w2 < warp; ++w2) before += wsum[w2];
+        unsigned long long before_c = 0;
+        for (int w2 = 0; w2 < warp; ++w2) {
+            before += wsum[w2];
+            before_c += wsum_c[w2];
+        }
         uint32_t excl = before + x - run;
+        unsigned long long excl_c = before_c + xc - runc;
         for (int b = b0; b < b1; ++b) {
             cum[b] = excl;
-            excl += ntiles(b);
+            ccum[b] = excl_c;
+            const uint32_t n = ntiles(b);
+            excl += n;
+            excl_c += cost(n);
         }
-        if (threadIdx.x == C::NTHREADS - 1) cum[a.batch] = before + x;
+        if (threadIdx.x == C::NTHREADS - 1) {
+            cum[a.batch] = before + x;
+            ccum[a.batch] = before_c + xc;
+        }
     }
     __syncthreads();
-    Split sp;
-    sp.init((long long)cum[a.batch] * a.Hkv, gridDim.x);
+    // The range starts: cut the cost into gridDim.x equal shares (the last 1/8
+    // of each a tail) and map every cut to the first tile at or after it.  A
+    // cut inside a pair's fixed cost goes to the pair's first tile; one inside
+    // a tile's cost to the nearer tile boundary.
+    long long *rt = reinterpret_cast<long long *>(smem + C::OFF_RT);
+    {
+        const long long ctot = (long long)a.Hkv * (long long)ccum[a.batch];
+        const long long ntot = (long long)a.Hkv * cum[a.batch];
+        const int grid = (int)gridDim.x;
+        for (int r = threadIdx.x; r <= 2 * grid; r += C::NTHREADS) {
+            long long xr = ctot;
+            if (r < 2 * grid) {
+                const int j = r >> 1;
+                const long long x0 = ctot * j / grid, x1 = ctot * (j + 1) / grid;
+                xr = (r & 1) ? x1 - ((x1 - x0) >> kTailShift) : x0;
+            }
+            long long pos = ntot;
+            if (xr < ctot) {
+                int lo = 0, hi = a.batch - 1;  // the last sequence whose costs start at or before xr
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if ((long long)a.Hkv * (long long)ccum[mid] <= xr) lo = mid; else hi = mid - 1;
+                }
+                const long long nt = (long long)(cum[lo + 1] - cum[lo]);
+                const long long pc = kCostTile * nt + kCostPair;  // one pair of sequence lo
+                const long long rem = xr - (long long)a.Hkv * (long long)ccum[lo];
+                const long long g = rem / pc, r2 = rem - g * pc;
+                const long long t = r2 <= kCostPair ? 0 : min(nt, (r2 - kCostPair + kCostTile / 2) / kCostTile);
+                pos = (long long)a.Hkv * cum[lo] + g * nt + t;
+            }
+            rt[r] = pos;
+        }
+    }
+    fence_proxy_async_smem();  // the ring's first stage is written by TMA from here on
+    __syncthreads();
+    const Ranges sp{rt, (int)gridDim.x};
     // Sequences with no context produce zeros.
     if (warp < C::NCW) {
         for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
