@@ -17,7 +17,9 @@
 //    tail.  A range holds whole (sequence, kv head) segments in its middle
 //    and at most one part-segment at each end.  Every CTA rebuilds the
 //    per-sequence tile counts, their costs and both prefix sums from
-//    context_lens in shared memory, then the table of range starts.
+//    context_lens in shared memory, then the table of range starts.  Launches
+//    with fewer than 16 tiles per CTA are split by tiles alone (closed form),
+//    as their time is latency, not their slowest share.
 //  * Two producer warps issue TMA tile loads (cp.async.bulk.tensor, 64 rows x
 //    256 B per K or V tile; a row is one token of one kv head) into a
 //    4-stage shared-memory ring guarded by mbarriers: one warp the K tiles
@@ -86,6 +88,9 @@ constexpr int kTailShift = 3;  // a CTA's tail range is 1/8 of its share
 #endif
 constexpr int kCostTile = 4;
 constexpr int kCostPair = PA_PAIR_COST;
+// Below this many tiles per CTA a launch is bound by latency, not by its
+// slowest share, and the pairs cost nothing extra (an even split by tiles).
+constexpr int kCostMinTilesPerCta = 16;
 constexpr int NTK = 4;            // tickets in flight (ranges handed from the K warp to the others)
 constexpr int kMinTilesPerCta = 8;  // grid = min(SMs, tile bound / this)
 constexpr unsigned FULL = 0xffffffffu;
@@ -195,11 +200,29 @@ __device__ __forceinline__ int clamp_ctx(const DecodeArgs &a, int b, bool report
 // shares, a tail being 1/8 of its CTA's share; st[r] is the first tile of
 // range r and st[2 * grid] the number of tiles.
 struct Ranges {
-    const long long *st;
+    const long long *st;  // null: the closed form below (equal shares of tiles)
     int grid;
-    __device__ long long start(int r) const { return st[r]; }
-    __device__ long long len(int r) const { return st[r + 1] - st[r]; }
+    long long base, rem;  // closed form: CTA j's share is base + (j < rem) tiles
+    __device__ long long cta_start(int j) const { return (long long)j * base + min((long long)j, rem); }
+    __device__ long long cta_len(int j) const { return base + (j < rem ? 1 : 0); }
+    __device__ long long start(int r) const {
+        if (st) return st[r];
+        const int j = r >> 1;
+        const long long cl = cta_len(j);
+        return cta_start(j) + ((r & 1) ? cl - (cl >> kTailShift) : 0);
+    }
+    __device__ long long len(int r) const {
+        if (st) return st[r + 1] - st[r];
+        const long long cl = cta_len(r >> 1);
+        return (r & 1) ? (cl >> kTailShift) : cl - (cl >> kTailShift);
+    }
     __device__ int owner(long long x) const {  // the (non-empty) range holding tile x
+        if (!st) {
+            const long long cut = rem * (base + 1);
+            const int j = (int)(x < cut ? x / (base + 1) : rem + (x - cut) / base);
+            const long long cl = cta_len(j);
+            return 2 * j + (x >= cta_start(j) + cl - (cl >> kTailShift) ? 1 : 0);
+        }
         int lo = 0, hi = 2 * grid - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -555,37 +578,52 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     // cut inside a pair's fixed cost goes to the pair's first tile; one inside
     // a tile's cost to the nearer tile boundary.
     long long *rt = reinterpret_cast<long long *>(smem + C::OFF_RT);
-    {
-        const long long ctot = (long long)a.Hkv * (long long)ccum[a.batch];
-        const long long ntot = (long long)a.Hkv * cum[a.batch];
+    const long long ntot = (long long)a.Hkv * cum[a.batch];
+    // Small launches are split by tiles alone, in closed form.
+    const bool by_cost = ntot >= (long long)kCostMinTilesPerCta * (long long)gridDim.x;
+    if (by_cost) {
         const int grid = (int)gridDim.x;
-        for (int r = threadIdx.x; r <= 2 * grid; r += C::NTHREADS) {
-            long long xr = ctot;
-            if (r < 2 * grid) {
-                const int j = r >> 1;
-                const long long x0 = ctot * j / grid, x1 = ctot * (j + 1) / grid;
-                xr = (r & 1) ? x1 - ((x1 - x0) >> kTailShift) : x0;
-            }
-            long long pos = ntot;
-            if (xr < ctot) {
-                int lo = 0, hi = a.batch - 1;  // the last sequence whose costs start at or before xr
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if ((long long)a.Hkv * (long long)ccum[mid] <= xr) lo = mid; else hi = mid - 1;
+        const long long ctot = (long long)a.Hkv * (long long)ccum[a.batch];
+        // One cut per thread; in 32-bit arithmetic when the costs fit (64-bit
+        // division is a long software sequence).
+        auto fill = [&](auto zero) {
+            using I = decltype(zero);
+            const I hkv = (I)a.Hkv, wt = (I)kCostTile, wp = (I)kCostPair;
+            const I total = (I)ctot, base = total / (I)grid, rem = total % (I)grid;
+            for (int r = threadIdx.x; r <= 2 * grid; r += C::NTHREADS) {
+                I xr = total;
+                if (r < 2 * grid) {
+                    // Share j: base units, one more for the first rem CTAs.
+                    const I j = (I)(r >> 1);
+                    const I x0 = j * base + (j < rem ? j : rem), len = base + (j < rem ? (I)1 : (I)0);
+                    xr = (r & 1) ? x0 + len - (len >> kTailShift) : x0;
                 }
-                const long long nt = (long long)(cum[lo + 1] - cum[lo]);
-                const long long pc = kCostTile * nt + kCostPair;  // one pair of sequence lo
-                const long long rem = xr - (long long)a.Hkv * (long long)ccum[lo];
-                const long long g = rem / pc, r2 = rem - g * pc;
-                const long long t = r2 <= kCostPair ? 0 : min(nt, (r2 - kCostPair + kCostTile / 2) / kCostTile);
-                pos = (long long)a.Hkv * cum[lo] + g * nt + t;
+                long long pos = ntot;
+                if (xr < total) {
+                    int lo = 0, hi = a.batch - 1;  // the last sequence whose costs start at or before xr
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (hkv * (I)ccum[mid] <= xr) lo = mid; else hi = mid - 1;
+                    }
+                    const I nt = (I)(cum[lo + 1] - cum[lo]);
+                    const I pc = wt * nt + wp;  // one pair of sequence lo
+                    const I rm = xr - hkv * (I)ccum[lo];
+                    const I g = rm / pc, r2 = rm - g * pc;
+                    I t = 0;
+                    if (r2 > wp) {
+                        t = (r2 - wp + wt / 2) / wt;
+                        if (t > nt) t = nt;
+                    }
+                    pos = (long long)a.Hkv * cum[lo] + (long long)(g * nt + t);
+                }
+                rt[r] = pos;
             }
-            rt[r] = pos;
-        }
+        };
+        if (ctot < (1ll << 31)) fill(0u); else fill(0ll);
     }
     fence_proxy_async_smem();  // the ring's first stage is written by TMA from here on
     __syncthreads();
-    const Ranges sp{rt, (int)gridDim.x};
+    const Ranges sp{by_cost ? rt : nullptr, (int)gridDim.x, ntot / (long long)gridDim.x, ntot % (long long)gridDim.x};
     // Sequences with no context produce zeros.
     if (warp < C::NCW) {
         for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
