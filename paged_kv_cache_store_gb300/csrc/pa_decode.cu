@@ -11,8 +11,8 @@
 //    CTA per SM).  The shares are equal in cost, not in tiles: a (sequence,
 //    kv head) pair costs 1.5 tiles' worth on top of its tiles (its q rows,
 //    block-id fetch and merge), so a CTA whose share holds many short pairs
-//    streams fewer tiles.  The first 7/8 of each share is the CTA's own
-//    range; the last 1/8 a tail range that CTAs take from an atomic counter
+//    streams fewer tiles.  The first 15/16 of each share is the CTA's own
+//    range; the last 1/16 a tail range that CTAs take from an atomic counter
 //    once their own range is done, so the CTAs that stream faster absorb the
 //    tail.  A range holds whole (sequence, kv head) segments in its middle
 //    and at most one part-segment at each end.  Every CTA rebuilds the
@@ -78,7 +78,7 @@ constexpr int kMaxPrefixRows = 8192;     // (member, q head) rows with prefix pa
 constexpr int kPrefixSplits = 2;         // the shared prefix's tiles are cut in this many parts
 constexpr int kMaxGrid = 256;     // CTAs of the persistent grid (min(SMs, this))
 constexpr int kMaxRanges = 2 * kMaxGrid;  // a head and a tail range per CTA
-constexpr int kTailShift = 3;  // a CTA's tail range is 1/8 of its share
+constexpr int kTailShift = 4;  // a CTA's tail range is 1/16 of its share
 // The work is split by cost, not by tiles: a (sequence, kv head) pair costs
 // kCostTile per tile plus kCostPair for the work it carries whatever its
 // length (its q rows, its block-id fetch, the merge of its result and, for
@@ -197,7 +197,7 @@ __device__ __forceinline__ int clamp_ctx(const DecodeArgs &a, int b, bool report
 // head, 2j+1 its tail, a separate range that any CTA may take from the tail
 // counter once its own head range is done (a range may be empty).  The cuts
 // divide the list's cost (kCostTile per tile, kCostPair per pair) into equal
-// shares, a tail being 1/8 of its CTA's share; st[r] is the first tile of
+// shares, a tail being 1/16 of its CTA's share; st[r] is the first tile of
 // range r and st[2 * grid] the number of tiles.
 struct Ranges {
     const long long *st;  // null: the closed form below (equal shares of tiles)
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
         }
     }
     __syncthreads();
-    // The range starts: cut the cost into gridDim.x equal shares (the last 1/8
+    // The range starts: cut the cost into gridDim.x equal shares (the last 1/16
     // of each a tail) and map every cut to the first tile at or after it.  A
     // cut inside a pair's fixed cost goes to the pair's first tile; one inside
     // a tile's cost to the nearer tile boundary.
